@@ -1,0 +1,341 @@
+"""Pins for the CPU oracle: each check ties a part of the oracle to something
+other than itself (a library routine, a closed form, brute force on tiny
+inputs, an invariant of the method, a number printed on the pages)."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_diffusion_moe_gb300 import synth
+from tests.helpers import bits, layer_to_oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _bf16_bits_of(vals):
+    return bits(torch.tensor(np.asarray(vals), dtype=torch.float32).to(torch.bfloat16))
+
+
+# --------------------------------------------------------------------- bf16
+
+
+def test_bf16_rounding_matches_torch():
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn(200_000, generator=g, dtype=torch.float64) * 3.0
+    # exact float32 halfway cases between two bf16 neighbours
+    base = torch.randn(1000, generator=g).to(torch.bfloat16).to(torch.float32)
+    half = (base.view(torch.int32) | 0x8000).view(torch.float32).to(torch.float64)
+    x = torch.cat([x, half, torch.tensor([0.0, -0.0, 1.0, -2.5, 1e-30, 3e38], dtype=torch.float64)])
+    want = x.to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    got = O.round_to_bf16(x.numpy())
+    assert np.array_equal(got, want)
+
+
+def test_bf16_decode_matches_torch():
+    g = torch.Generator().manual_seed(2)
+    t = torch.randn(10_000, generator=g).to(torch.bfloat16)
+    assert np.array_equal(O.bf16_to_f64(bits(t)), t.to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------------ rmsnorm
+
+
+@pytest.mark.parametrize("H", [8, 256, 2048])
+def test_rms_norm_closed_forms(H):
+    eps = 1e-6
+    c = -3.25
+    xn = O.rms_norm(np.full((1, H), c), eps)
+    assert np.allclose(xn, c / math.sqrt(c * c + eps), rtol=1e-15, atol=0)
+    s = 7.0
+    x = np.zeros((1, H))
+    x[0, 3] = s
+    xn = O.rms_norm(x, eps)
+    assert xn[0, 3] == pytest.approx(s / math.sqrt(s * s / H + eps), rel=1e-14)
+    assert np.count_nonzero(xn) == 1
+
+
+def test_silu_identities():
+    z = np.linspace(-30, 30, 1001)
+    assert np.allclose(O.silu(z) - O.silu(-z), z, rtol=0, atol=1e-12)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    assert O.silu(np.array([40.0]))[0] == pytest.approx(40.0, rel=1e-15)
+    assert O.silu(np.array([1.0]))[0] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)
+
+
+# ------------------------------------------------------------------- router
+
+
+def _planted_router(logit_vals, H=8):
+    """Router rows with one nonzero (bf16-exact) entry each, so that an
+    all-ones input (RMSNorm -> bf16 1.0) yields exactly these logits."""
+    E = len(logit_vals)
+    w = np.zeros((E, H), dtype=np.float32)
+    for e, v in enumerate(logit_vals):
+        w[e, (3 * e + 1) % H] = v
+    return bits(torch.from_numpy(w).to(torch.bfloat16))
+
+
+def test_route_planted_logits_and_tie_break():
+    vals = [0.5, 2.0, -1.0, 2.0, 0.25, -4.0]
+    wr = _planted_router(vals, H=8)
+    xb = O.round_to_bf16(O.rms_norm(np.ones((1, 8)), 1e-6))
+    assert np.all(xb == 1.0)
+    logits, p, idx, w = O.route(xb, wr, 3)
+    assert np.array_equal(logits[0], np.array(vals))
+    assert list(idx[0]) == [1, 3, 0]  # tie at 2.0 -> lower id first
+    denom = 2 * math.exp(2.0) + math.exp(0.5)
+    assert w[0, 0] == pytest.approx(math.exp(2.0) / denom, rel=1e-14)
+    assert w[0, 2] == pytest.approx(math.exp(0.5) / denom, rel=1e-14)
+    # a bias reorders the selection
+    bias = np.array([3.0, 0, 0, 0, 0, 0], dtype=np.float32)
+    _, _, idx_b, _ = O.route(xb, wr, 2, bias)
+    assert list(idx_b[0]) == [0, 1]
+
+
+def test_route_topk_is_max_sum_subset_bruteforce():
+    rng = np.random.default_rng(3)
+    E, H, K = 9, 16, 3
+    wr = _bf16_bits_of(rng.normal(0, 0.3, (E, H)))
+    xb = O.round_to_bf16(O.rms_norm(rng.normal(size=(20, H)), 1e-6))
+    logits, p, idx, w = O.route(xb, wr, K)
+    for t in range(20):
+        best = max(itertools.combinations(range(E), K), key=lambda s: sum(logits[t, list(s)]))
+        assert set(idx[t]) == set(best)
+        assert len(set(idx[t])) == K
+        assert math.fsum(p[t]) == pytest.approx(1.0, abs=1e-12)
+        assert math.fsum(w[t]) == pytest.approx(1.0, abs=1e-12)
+        # renormalised probabilities = softmax restricted to the chosen logits
+        sel = logits[t, idx[t]]
+        ref = [math.exp(v - max(sel)) for v in sel]
+        ref = [v / math.fsum(ref) for v in ref]
+        assert np.allclose(w[t], ref, rtol=1e-12, atol=0)
+
+
+# ------------------------------------------------------------------ experts
+
+
+def test_swiglu_expert_closed_form_nonsquare():
+    # H = 3, F = 2: gate picks x0 and x2, up = 2 * gate, down maps
+    # h0 -> out2 and h1 -> out0 (out1 stays 0).
+    gate = np.array([[1, 0, 0], [0, 0, 1]], dtype=np.float32)
+    up = 2.0 * gate
+    gu = _bf16_bits_of(np.concatenate([gate, up]))
+    down = _bf16_bits_of(np.array([[0, 1], [0, 0], [1, 0]], dtype=np.float32))
+    xb = np.array([[0.5, -7.0, -1.25]])
+    out = O.swiglu_expert(xb, gu, down)
+
+    def h(v):
+        s = v / (1.0 + math.exp(-v))
+        return float(O.round_to_bf16(np.array([s * 2.0 * v]))[0])
+
+    assert out[0, 0] == pytest.approx(h(-1.25), rel=1e-15)
+    assert out[0, 1] == 0.0
+    assert out[0, 2] == pytest.approx(h(0.5), rel=1e-15)
+
+
+def _tiny_layer(seed=0, zipf=None):
+    return synth.make_layer(synth.TINY, seed, 0, "cpu", zipf_s=zipf)
+
+
+@pytest.mark.parametrize("zipf", [None, 1.2])
+def test_sparse_moe_equals_dense_bruteforce(zipf):
+    d = synth.TINY
+    L = layer_to_oracle(_tiny_layer(0, zipf))
+    x = synth.make_x(d, 8, 0).numpy()
+    sparse = O.moe_layer(x, L, d.top_k, d.rms_eps)["x_out"]
+    dense = O.moe_layer_dense(x, L, d.top_k, d.rms_eps)
+    assert np.allclose(sparse, dense, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_identical_experts_ignore_routing():
+    """With every routed expert equal, the combine weights sum to one, so the
+    output equals that expert plus the shared expert whatever the routing."""
+    d = synth.TINY
+    L = layer_to_oracle(_tiny_layer(1))
+    L["gate_up"] = np.repeat(L["gate_up"][:1], d.n_experts, axis=0)
+    L["down"] = np.repeat(L["down"][:1], d.n_experts, axis=0)
+    x = synth.make_x(d, 8, 1).numpy()
+    out = O.moe_layer(x, L, d.top_k, d.rms_eps)
+    xb = out["xb"]
+    want = x + O.swiglu_expert(xb, L["gate_up"][0], L["down"][0]) \
+        + O.swiglu_expert(xb, L["sh_gate_up"], L["sh_down"])
+    assert np.allclose(out["x_out"], want, rtol=1e-12, atol=1e-12)
+    # zero routed experts -> only the shared expert remains
+    L["gate_up"] = np.zeros_like(L["gate_up"])
+    out = O.moe_layer(x, L, d.top_k, d.rms_eps)
+    assert np.allclose(out["x_out"], x + O.swiglu_expert(xb, L["sh_gate_up"], L["sh_down"]),
+                       rtol=1e-13, atol=1e-13)
+
+
+def test_teacher_forced_routing_uses_given_experts():
+    d = synth.TINY
+    L = layer_to_oracle(_tiny_layer(2))
+    x = synth.make_x(d, 8, 2).numpy()
+    free = O.moe_layer(x, L, d.top_k, d.rms_eps)
+    forced = O.moe_layer(x, L, d.top_k, d.rms_eps, force_idx=free["idx"])
+    assert np.array_equal(free["x_out"], forced["x_out"])
+    other = (free["idx"] + 1) % d.n_experts
+    forced2 = O.moe_layer(x, L, d.top_k, d.rms_eps, force_idx=other)
+    assert not np.allclose(forced2["x_out"], free["x_out"])
+
+
+# --------------------------------------------------------------------- head
+
+
+def test_head_stats_bruteforce_fsum():
+    rng = np.random.default_rng(4)
+    V, M, mask = 50, 3, 17
+    z = rng.normal(0, 3, (M, V))
+    st = O.head_stats(z, mask)
+    for p in range(M):
+        vals = [(z[p, v], v) for v in range(V) if v != mask]
+        m = max(v for v, _ in vals)
+        a = min(i for v, i in vals if v == m)
+        lse = m + math.log(math.fsum(math.exp(v - m) for v, _ in vals))
+        assert st["argmax"][p] == a
+        assert st["max_logit"][p] == m
+        assert st["lse"][p] == pytest.approx(lse, rel=1e-14)
+        assert st["max_prob"][p] == pytest.approx(math.exp(m - lse), rel=1e-13)
+
+
+def test_head_stats_closed_forms():
+    V = 1024
+    z = np.full((2, V), 1.5)
+    st = O.head_stats(z, 0)
+    # all logits equal, mask id 0 excluded -> lowest non-mask id, p = 1/(V-1)
+    assert list(st["argmax"]) == [1, 1]
+    assert st["max_prob"][0] == pytest.approx(1.0 / (V - 1), rel=1e-13)
+    assert st["lse"][0] == pytest.approx(1.5 + math.log(V - 1), rel=1e-14)
+    # the mask token never wins, even with the largest logit
+    z = np.zeros((1, V))
+    z[0, 5] = 50.0
+    z[0, 9] = 10.0
+    st = O.head_stats(z, 5)
+    assert st["argmax"][0] == 9
+    assert st["max_logit"][0] == 10.0
+
+
+def test_head_logits_planted_row_and_scale():
+    d = synth.TINY
+    rng = np.random.default_rng(5)
+    x = rng.normal(size=(2, d.hidden))
+    head = rng.normal(0, 0.02, (d.vocab, d.hidden))
+    xb = O.round_to_bf16(O.rms_norm(x, d.rms_eps))
+    head[700] = xb[0] * 0.05      # aligned with position 0
+    head[33] = xb[1] * 0.05       # aligned with position 1
+    hb = _bf16_bits_of(head)
+    z = O.head_logits(x, hb, d.rms_eps, alpha=np.array([1.0, 2.0]))
+    st = O.head_stats(z, d.mask_id)
+    assert list(st["argmax"]) == [700, 33]
+    z1 = O.head_logits(x, hb, d.rms_eps)
+    assert np.allclose(z[1], 2.0 * z1[1], rtol=1e-15)
+
+
+# ------------------------------------------------------------------- unmask
+
+
+def test_unmask_golden_cases():
+    with open(os.path.join(HERE, "golden", "unmask_rule_cases.json")) as f:
+        g = json.load(f)
+    for c in g["cases"]:
+        t, m, com = O.unmask(c["tokens"], c["masked"], c["argmax"], c["max_prob"],
+                             c["threshold"], c["block"])
+        assert list(t) == c["want_tokens"], c["name"]
+        assert list(m) == c["want_masked"], c["name"]
+        assert [int(v) for v in com] == c["want_committed"], c["name"]
+
+
+# ---------------------------------------------------------- denoise loop
+
+
+def _tiny_model(seed=0, n_pos=8):
+    d = synth.TINY
+    return {
+        "dims": {"top_k": d.top_k, "rms_eps": d.rms_eps, "mask_id": d.mask_id},
+        "layers": [layer_to_oracle(_tiny_layer(seed))],
+        "embed": bits(synth.make_embed(d, seed)),
+        "head": bits(synth.make_head(d, seed)),
+        "ctx": synth.make_ctx(d, n_pos, seed).numpy(),
+    }
+
+
+@pytest.mark.parametrize("alpha_val", [1.0, 60.0])
+def test_denoise_loop_invariants(alpha_val):
+    d = synth.TINY
+    n = 8
+    model = _tiny_model(0, n)
+    tok, msk = synth.masked_block(d, n)
+    alpha = np.full(n, alpha_val)
+    res = O.denoise_block(tok.numpy(), msk.numpy(), model, 0.95, d.block, max_steps=n, alpha=alpha)
+    hist = res["history"]
+    assert not res["masked"].any()
+    assert 1 <= res["steps"] <= n
+    first = hist[0]
+    # every slot ends with the token it predicted while still masked at step 1
+    assert np.array_equal(res["tokens"], first["argmax"])
+    assert not np.any(res["tokens"] == d.mask_id)
+    prev_masked = msk.numpy()
+    for st in hist:
+        # never re-masks, always progresses
+        assert not np.any((prev_masked == 0) & (st["masked"] == 1))
+        assert st["committed"].sum() >= 1
+        prev_masked = st["masked"]
+    # commit order: all slots above the threshold at step 1, then one per step
+    # in descending probability
+    p1 = first["max_prob"].astype(np.float32)
+    above = p1 > np.float32(0.95)
+    if above.any():
+        assert np.array_equal(first["committed"], above)
+        assert res["steps"] == 1 + int((~above).sum())
+    else:
+        assert res["steps"] == n
+    rest = [p for p in np.argsort(-p1, kind="stable") if not above[p]]
+    later = [int(np.nonzero(st["committed"])[0][0]) for st in hist[1 if above.any() else 0:]]
+    assert later == rest[:len(later)]
+
+
+def test_denoise_four_steps_tiny_config():
+    d = synth.TINY
+    model = _tiny_model(0, 8)
+    tok, msk = synth.masked_block(d, 8)
+    res = O.denoise_block(tok.numpy(), msk.numpy(), model, 0.95, d.block, max_steps=4)
+    assert res["steps"] == 4
+    assert int(res["masked"].sum()) == 8 - 4   # random head: one commit per step
+
+
+# ------------------------------------------------------- byte model / shapes
+
+
+def test_clover_shape_sums_match_pages():
+    """Files, 'What Clover is': one expert is 3,145,728 parameters; routed
+    experts are 32,212,254,720; the head is 508,559,360."""
+    c = synth.CLOVER
+    assert c.expert_params == 3_145_728
+    assert c.n_layers * c.n_experts * c.expert_params == 32_212_254_720
+    assert c.vocab * c.hidden == 508_559_360
+    assert c.expert_bytes == 6_291_456
+
+
+def test_uniform_routing_union_matches_closed_form():
+    """Files, 'The expert selection': a 32-token block under independent
+    routing touches 256(1-(1-8/256)^32) ~ 163.3 experts (their simulation:
+    163.4). The oracle's router on the synthetic Clover-shaped inputs must
+    land there."""
+    c = synth.CLOVER
+    closed = c.n_experts * (1 - (1 - c.top_k / c.n_experts) ** 32)
+    assert closed == pytest.approx(163.31, abs=0.01)
+    wr = bits(synth.make_router(c, 12345, 0))
+    unions = []
+    for b in range(40):
+        x = synth.make_x(c, 32, 1000 + b).numpy()
+        xb = O.round_to_bf16(O.rms_norm(x, c.rms_eps))
+        _, _, idx, _ = O.route(xb, wr, c.top_k)
+        unions.append(len(np.unique(idx)))
+    mean = float(np.mean(unions))
+    assert abs(mean - closed) < 2.5, mean
+    assert abs(mean - 163.4) < 2.5
