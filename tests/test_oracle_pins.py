@@ -339,3 +339,16 @@ def test_uniform_routing_union_matches_closed_form():
     mean = float(np.mean(unions))
     assert abs(mean - closed) < 2.5, mean
     assert abs(mean - 163.4) < 2.5
+
+
+def test_embed_closed_form():
+    """Input assembly x_p = E[t_p] + c_p: with a planted table (row v holds the
+    constant v/4) and context c_p = p/8, x_p is (t_p/4 + p/8) everywhere."""
+    V, H = 12, 6
+    table = np.repeat((np.arange(V, dtype=np.float32) / 4.0)[:, None], H, axis=1)
+    tb = _bf16_bits_of(table)
+    tokens = np.array([11, 3, 3, 0])
+    ctx = np.repeat((np.arange(4) / 8.0)[:, None], H, axis=1)
+    x = O.embed(tokens, tb, ctx)
+    want = (tokens / 4.0 + np.arange(4) / 8.0)[:, None] * np.ones((1, H))
+    assert np.array_equal(x, want)
