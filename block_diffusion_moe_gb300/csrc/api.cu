@@ -1,0 +1,610 @@
+// Host side of the C ABI declared in include/clover.h: argument checks,
+// workspace layout, TMA descriptors, kernel launches and the denoise loop.
+#include <cudaTypedefs.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/clover.h"
+#include "kernels.cuh"
+#include "sm100.cuh"
+
+using namespace clover;
+
+namespace {
+
+thread_local char g_err[512] = {0};
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(CLOVER_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Control block at the start of every workspace (and of each sub-workspace
+// of the denoise workspace). Words that must be zero when a call starts are
+// either reset by the kernels that use them or kept zero between calls.
+constexpr size_t kCtrlBytes = 256;
+enum CtrlWord : int {
+  kCtrlErr = 0,          // kernel status bits
+  kCtrlUnitCtr = 1,      // expert kernel work counter (reset by the permutation kernel)
+  kCtrlMaskedLeft = 2,   // positions still masked after the last head call
+  kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
+  kCtrlCommitted = 4,    // positions committed by the last head call
+  kCtrlTokenGroups = 8,  // [8] routing arrival counters (reset by their last CTA)
+};
+
+struct MoeLayout {
+  size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, logits, xg, hbuf, yslot, bytes;
+};
+
+MoeLayout moe_layout(const clover_dims& d, int M) {
+  MoeLayout L;
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    const size_t r = o;
+    o = align_up(o + b, 256);
+    return r;
+  };
+  const size_t H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
+  const size_t R = static_cast<size_t>(M) * K + M;
+  L.gu_done = take((E + 1) * 4);
+  L.dn_done = take((H / 128) * 4);
+  L.n_active = take(4);
+  L.act = take(E * 4);
+  L.cnt = take(E * 4);
+  L.off = take(E * 4);
+  L.tok_slot = take(M * K * 4);
+  L.topk_idx = take(M * K * 4);
+  L.topk_w = take(M * K * 4);
+  L.logits = take(static_cast<size_t>(M) * E * 4);
+  L.xg = take(R * H * 2);
+  L.hbuf = take(R * F * 2);
+  L.yslot = take(R * H * 4);
+  L.bytes = o;
+  return L;
+}
+
+struct HeadLayout {
+  size_t xn, part_m, part_s, part_a, bytes;
+};
+
+HeadLayout head_layout(const clover_dims& d, int M) {
+  HeadLayout L;
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    const size_t r = o;
+    o = align_up(o + b, 256);
+    return r;
+  };
+  L.xn = take(static_cast<size_t>(M) * d.hidden * 2);
+  L.part_m = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
+  L.part_s = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
+  L.part_a = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
+  L.bytes = o;
+  return L;
+}
+
+// Denoise workspace: [ctrl | moe ctrl | head ctrl | x | moe data | head data]
+struct DenoiseLayout {
+  size_t moe_ctrl, head_ctrl, x, moe, head, bytes;
+};
+
+DenoiseLayout denoise_layout(const clover_dims& d, int M) {
+  DenoiseLayout L;
+  L.moe_ctrl = kCtrlBytes;
+  L.head_ctrl = 2 * kCtrlBytes;
+  L.x = 3 * kCtrlBytes;
+  L.moe = align_up(L.x + static_cast<size_t>(M) * d.hidden * 4, 256);
+  L.head = align_up(L.moe + moe_layout(d, M).bytes, 256);
+  L.bytes = align_up(L.head + head_layout(d, M).bytes, 256);
+  return L;
+}
+
+int check_dims(const clover_dims* d) {
+  if (d == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "dims is NULL");
+  if (d->hidden <= 0 || d->n_experts <= 0 || d->top_k <= 0 || d->d_ff <= 0 || d->vocab <= 0)
+    return fail(CLOVER_ERR_INVALID_ARG, "dims must be positive");
+  if (!(d->rms_eps >= 0.f) || d->rms_eps > 1.f) return fail(CLOVER_ERR_INVALID_ARG, "rms_eps out of range");
+  if (d->hidden % 128 != 0 || d->hidden > 16384)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "hidden=%d: must be a multiple of 128, at most 16384", d->hidden);
+  if (d->d_ff % 64 != 0 || d->d_ff > 16384)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "d_ff=%d: must be a multiple of 64, at most 16384", d->d_ff);
+  if (d->n_experts > kMaxExperts) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "n_experts=%d > %d", d->n_experts, kMaxExperts);
+  if (d->top_k > kMaxTopK || d->top_k > d->n_experts)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "top_k=%d: must be <= 32 and <= n_experts", d->top_k);
+  if (d->vocab < 2) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "vocab=%d < 2", d->vocab);
+  if (d->mask_id < 0 || d->mask_id >= d->vocab)
+    return fail(CLOVER_ERR_INVALID_ARG, "mask_id=%d outside [0, vocab)", d->mask_id);
+  return CLOVER_OK;
+}
+
+int check_tokens(int M) {
+  if (M < 1 || M > kMaxTokens) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "tokens=%d outside [1, %d]", M, kMaxTokens);
+  return CLOVER_OK;
+}
+
+int check_layer(const clover_moe_layer* l, int i) {
+  if (l == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "layer %d is NULL", i);
+  const void* ps[] = {l->router_w, l->gate_up, l->down, l->sh_gate_up, l->sh_down};
+  for (const void* p : ps) {
+    if (p == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "layer %d: NULL weight pointer", i);
+    if (!aligned16(p)) return fail(CLOVER_ERR_INVALID_ARG, "layer %d: weight pointer not 16-byte aligned", i);
+  }
+  return CLOVER_OK;
+}
+
+// ------------------------------------------------------------ device info
+
+struct DevInfo {
+  int sms = 0;
+};
+
+int device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(CLOVER_ERR_CUDA, "device ordinal %d unsupported", dev);
+  std::lock_guard<std::mutex> g(mu);
+  if (cache[dev].sms == 0) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    cache[dev].sms = sms;
+  }
+  *out = cache[dev];
+  return CLOVER_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder() {
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  static cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSuccess;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr) {
+    if (err != cudaSuccess) return cuda_fail(err, "cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)");
+    return fail(CLOVER_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  }
+  return CLOVER_OK;
+}
+
+// bf16 matrix [rows][cols], row-major; box = 64 columns x box_rows rows with
+// 128-byte swizzle (the layout the UMMA descriptors expect).
+int encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, const char* what) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CLOVER_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
+  return CLOVER_OK;
+}
+
+// ------------------------------------------------------------- profiling
+
+struct ProfileHook {
+  cudaEvent_t* begin = nullptr;
+  cudaEvent_t* end = nullptr;
+  int cap = 0;
+  int count = 0;
+} g_prof;
+
+// ------------------------------------------------------------- launches
+
+struct Plan {
+  int sms;
+};
+
+int record(cudaEvent_t ev, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(ev, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return CLOVER_OK;
+}
+
+// Route + permutation + experts for one layer. ctrl: this call's MoE control
+// block; err: status word to flag.
+int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const float* x_in, float* x_out,
+                      int32_t* out_idx, float* out_w, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
+                      cudaStream_t stream) {
+  const MoeLayout L = moe_layout(d, M);
+  const int H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
+  const int MK = M * K;
+  bf16* xg = reinterpret_cast<bf16*>(data + L.xg);
+  bf16* hbuf = reinterpret_cast<bf16*>(data + L.hbuf);
+  int32_t* topk_idx = reinterpret_cast<int32_t*>(data + L.topk_idx);
+  float* topk_w = reinterpret_cast<float*>(data + L.topk_w);
+
+  RouteArgs ra;
+  ra.x = x_in;
+  ra.wr = reinterpret_cast<const bf16*>(layer.router_w);
+  ra.bias = layer.router_bias;
+  ra.logits = reinterpret_cast<float*>(data + L.logits);
+  ra.xn_rows = xg + static_cast<size_t>(MK) * H;
+  ra.tg_ctr = ctrl + kCtrlTokenGroups;
+  ra.topk_idx = topk_idx;
+  ra.topk_w = topk_w;
+  ra.M = M;
+  ra.H = H;
+  ra.E = E;
+  ra.K = K;
+  ra.eps = d.rms_eps;
+  cudaError_t e = launch_route(ra, stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "launch route");
+
+  PermArgs pa;
+  pa.topk_idx = topk_idx;
+  pa.topk_w = topk_w;
+  pa.tok_slot = reinterpret_cast<int32_t*>(data + L.tok_slot);
+  pa.cnt = reinterpret_cast<int*>(data + L.cnt);
+  pa.off = reinterpret_cast<int*>(data + L.off);
+  pa.act = reinterpret_cast<int*>(data + L.act);
+  pa.n_active = reinterpret_cast<int*>(data + L.n_active);
+  pa.unit_ctr = ctrl + kCtrlUnitCtr;
+  pa.gu_done = reinterpret_cast<int*>(data + L.gu_done);
+  pa.dn_done = reinterpret_cast<int*>(data + L.dn_done);
+  pa.xg = xg;
+  pa.out_idx = out_idx;
+  pa.out_w = out_w;
+  pa.M = M;
+  pa.H = H;
+  pa.E = E;
+  pa.K = K;
+  e = launch_perm(pa, std::max(1, std::min(MK, plan.sms)), stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "launch perm");
+
+  ExpertArgs xa;
+  memset(&xa, 0, sizeof(xa));
+  const int R = MK + M;
+  int rc;
+  if ((rc = encode_bf16_2d(&xa.tm_gu, layer.gate_up, static_cast<uint64_t>(E) * 2 * F, H, 64, "gate_up"))) return rc;
+  if ((rc = encode_bf16_2d(&xa.tm_sgu, layer.sh_gate_up, 2ull * F, H, 64, "shared gate_up"))) return rc;
+  if ((rc = encode_bf16_2d(&xa.tm_dn, layer.down, static_cast<uint64_t>(E) * H, F, 128, "down"))) return rc;
+  if ((rc = encode_bf16_2d(&xa.tm_sdn, layer.sh_down, H, F, 128, "shared down"))) return rc;
+  if ((rc = encode_bf16_2d(&xa.tm_xg, xg, R, H, 16, "gathered inputs"))) return rc;
+  if ((rc = encode_bf16_2d(&xa.tm_h, hbuf, R, F, 16, "swiglu outputs"))) return rc;
+  xa.x_in = x_in;
+  xa.x_out = x_out;
+  xa.hbuf = hbuf;
+  xa.yslot = reinterpret_cast<float*>(data + L.yslot);
+  xa.n_active = pa.n_active;
+  xa.act = pa.act;
+  xa.cnt = pa.cnt;
+  xa.off = pa.off;
+  xa.tok_slot = pa.tok_slot;
+  xa.topk_w = topk_w;
+  xa.unit_ctr = pa.unit_ctr;
+  xa.gu_done = pa.gu_done;
+  xa.dn_done = pa.dn_done;
+  xa.err = err;
+  xa.M = M;
+  xa.H = H;
+  xa.F = F;
+  xa.E = E;
+  xa.K = K;
+  const int nb = (M + 15) & ~15;
+  const size_t fixed = expert_smem_bytes(0, 0, nb) + static_cast<size_t>(4 * 16) * 8;
+  const size_t budget = static_cast<size_t>(kSmemBudget) - fixed;
+  int sa, sb;
+  if (nb <= 64) {
+    sa = sb = static_cast<int>(std::min<size_t>(16, budget / (kATileBytes + static_cast<size_t>(nb) * 128)));
+  } else {
+    sb = 3;
+    sa = static_cast<int>(std::min<size_t>(16, (budget - static_cast<size_t>(sb) * nb * 128) / kATileBytes));
+  }
+  xa.stages_a = sa;
+  xa.stages_b = sb;
+  xa.nb_max = nb;
+  const size_t smem = expert_smem_bytes(sa, sb, nb);
+  if (g_prof.begin && g_prof.cap > 0) {
+    if ((rc = record(g_prof.begin[g_prof.count % g_prof.cap], stream))) return rc;
+  }
+  e = launch_expert(xa, plan.sms, smem, stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "launch expert");
+  if (g_prof.end && g_prof.cap > 0) {
+    if ((rc = record(g_prof.end[g_prof.count % g_prof.cap], stream))) return rc;
+    ++g_prof.count;
+  }
+  return CLOVER_OK;
+}
+
+int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, const float* alpha, float threshold,
+                 int block, int32_t* tokens, uint8_t* masked, int32_t* argmax, float* max_logit, float* lse,
+                 float* max_prob, int32_t* n_committed, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
+                 cudaStream_t stream) {
+  const HeadLayout L = head_layout(d, M);
+  bf16* xn = reinterpret_cast<bf16*>(data + L.xn);
+  NormArgs na;
+  na.x = x;
+  na.xn = xn;
+  na.M = M;
+  na.H = d.hidden;
+  na.eps = d.rms_eps;
+  cudaError_t e = launch_rmsnorm(na, stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "launch rmsnorm");
+
+  HeadArgs ha;
+  memset(&ha, 0, sizeof(ha));
+  int rc;
+  if ((rc = encode_bf16_2d(&ha.tm_w, head_w, d.vocab, d.hidden, 128, "head"))) return rc;
+  if ((rc = encode_bf16_2d(&ha.tm_x, xn, M, d.hidden, 16, "normed positions"))) return rc;
+  ha.alpha = alpha;
+  ha.part_m = reinterpret_cast<float*>(data + L.part_m);
+  ha.part_s = reinterpret_cast<float*>(data + L.part_s);
+  ha.part_a = reinterpret_cast<int*>(data + L.part_a);
+  ha.done_ctr = ctrl + kCtrlHeadDone;
+  ha.tokens = tokens;
+  ha.masked = masked;
+  ha.argmax = argmax;
+  ha.max_logit = max_logit;
+  ha.lse = lse;
+  ha.max_prob = max_prob;
+  ha.n_committed = n_committed ? n_committed : ctrl + kCtrlCommitted;
+  ha.n_masked_left = ctrl + kCtrlMaskedLeft;
+  ha.err = err;
+  ha.M = M;
+  ha.H = d.hidden;
+  ha.V = d.vocab;
+  ha.mask_id = d.mask_id;
+  ha.block = block;
+  ha.n_tiles = (d.vocab + 127) / 128;
+  ha.threshold = threshold;
+  const int nb = (M + 15) & ~15;
+  const size_t fixed = head_smem_bytes(0, nb) + 16 * 2 * 8;
+  ha.stages = static_cast<int>(std::min<size_t>(
+      12, (static_cast<size_t>(kSmemBudget) - fixed) / (kATileBytes + static_cast<size_t>(nb) * 128)));
+  const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
+  e = launch_head(ha, grid, head_smem_bytes(ha.stages, nb), stream, false);
+  if (e != cudaSuccess) return cuda_fail(e, "launch head");
+  return CLOVER_OK;
+}
+
+int check_ws(void* ws, size_t have, size_t need) {
+  if (ws == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(CLOVER_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (have < need) return fail(CLOVER_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", have, need);
+  return CLOVER_OK;
+}
+
+int check_launch_errors(const char* where) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, where);
+  return CLOVER_OK;
+}
+
+int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, int32_t n_layers, const uint16_t* embed,
+                      const float* ctx, const uint16_t* head_w, const float* logit_scale, float threshold,
+                      int32_t block, int32_t* tokens, uint8_t* masked, int32_t M, void* workspace,
+                      size_t workspace_bytes, clover_stream_t stream) {
+  int rc;
+  if ((rc = check_dims(dims))) return rc;
+  if ((rc = check_tokens(M))) return rc;
+  if (n_layers < 0) return fail(CLOVER_ERR_INVALID_ARG, "n_layers < 0");
+  if (n_layers > 0 && layers == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "layers is NULL");
+  if (!embed || !ctx || !head_w || !tokens || !masked)
+    return fail(CLOVER_ERR_INVALID_ARG, "NULL embed/ctx/head_w/tokens/masked");
+  if (!aligned16(embed) || !aligned16(ctx) || !aligned16(head_w))
+    return fail(CLOVER_ERR_INVALID_ARG, "embed/ctx/head_w must be 16-byte aligned");
+  if (block < 1 || M % block != 0) return fail(CLOVER_ERR_INVALID_ARG, "block=%d must divide M=%d", block, M);
+  if (!(threshold == threshold)) return fail(CLOVER_ERR_INVALID_ARG, "threshold is NaN");
+  for (int i = 0; i < n_layers; ++i)
+    if ((rc = check_layer(&layers[i], i))) return rc;
+  const DenoiseLayout L = denoise_layout(*dims, M);
+  if ((rc = check_ws(workspace, workspace_bytes, L.bytes))) return rc;
+  if ((rc = get_encoder())) return rc;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  const Plan plan{di.sms};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* ctrl = reinterpret_cast<int*>(ws);
+  int* err = ctrl + kCtrlErr;
+  float* x = reinterpret_cast<float*>(ws + L.x);
+
+  EmbedArgs ea;
+  ea.tokens = tokens;
+  ea.embed = reinterpret_cast<const bf16*>(embed);
+  ea.ctx = ctx;
+  ea.x = x;
+  ea.err = err;
+  ea.M = M;
+  ea.H = dims->hidden;
+  ea.V = dims->vocab;
+  cudaError_t e = launch_embed(ea, s, false);
+  if (e != cudaSuccess) return cuda_fail(e, "launch embed");
+  for (int l = 0; l < n_layers; ++l) {
+    rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,
+                           reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s);
+    if (rc) return rc;
+  }
+  rc = enqueue_head(*dims, head_w, x, logit_scale, threshold, block, tokens, masked, nullptr, nullptr, nullptr,
+                    nullptr, ctrl + kCtrlCommitted, M, ws + L.head, reinterpret_cast<int*>(ws + L.head_ctrl), err,
+                    plan, s);
+  if (rc) return rc;
+  // The step's masked-count lands in the head control block; mirror it into
+  // the top-level control block for the loop.
+  e = cudaMemcpyAsync(ctrl + kCtrlMaskedLeft, reinterpret_cast<int*>(ws + L.head_ctrl) + kCtrlMaskedLeft, sizeof(int),
+                      cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(masked count)");
+  return check_launch_errors("denoise step");
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t clover_moe_workspace_bytes(const clover_dims* dims, int32_t max_tokens) {
+  if (check_dims(dims) || check_tokens(max_tokens)) return 0;
+  return kCtrlBytes + moe_layout(*dims, max_tokens).bytes;
+}
+
+int clover_moe_block_step(const clover_dims* dims, const clover_moe_layer* layer, const float* x_in, float* x_out,
+                          int32_t* topk_idx, float* topk_w, int32_t M, void* workspace, size_t workspace_bytes,
+                          clover_stream_t stream) {
+  int rc;
+  if ((rc = check_dims(dims))) return rc;
+  if ((rc = check_tokens(M))) return rc;
+  if ((rc = check_layer(layer, 0))) return rc;
+  if (!x_in || !x_out) return fail(CLOVER_ERR_INVALID_ARG, "x_in/x_out is NULL");
+  if (!aligned16(x_in) || !aligned16(x_out)) return fail(CLOVER_ERR_INVALID_ARG, "x_in/x_out not 16-byte aligned");
+  const size_t xb = static_cast<size_t>(M) * dims->hidden * 4;
+  const uint8_t* a0 = reinterpret_cast<const uint8_t*>(x_in);
+  const uint8_t* b0 = reinterpret_cast<const uint8_t*>(x_out);
+  if (a0 != b0 && a0 < b0 + xb && b0 < a0 + xb) return fail(CLOVER_ERR_INVALID_ARG, "x_in and x_out partially overlap");
+  if ((rc = check_ws(workspace, workspace_bytes, kCtrlBytes + moe_layout(*dims, M).bytes))) return rc;
+  if ((rc = get_encoder())) return rc;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* ctrl = reinterpret_cast<int*>(ws);
+  rc = enqueue_moe_layer(*dims, *layer, x_in, x_out, topk_idx, topk_w, M, ws + kCtrlBytes, ctrl, ctrl + kCtrlErr,
+                         Plan{di.sms}, reinterpret_cast<cudaStream_t>(stream));
+  if (rc) return rc;
+  return check_launch_errors("moe block step");
+}
+
+size_t clover_head_workspace_bytes(const clover_dims* dims, int32_t max_tokens) {
+  if (check_dims(dims) || check_tokens(max_tokens)) return 0;
+  return kCtrlBytes + head_layout(*dims, max_tokens).bytes;
+}
+
+int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const float* x, const float* logit_scale,
+                         float threshold, int32_t block, int32_t* tokens, uint8_t* masked, int32_t* argmax,
+                         float* max_logit, float* lse, float* max_prob, int32_t* n_committed, int32_t M,
+                         void* workspace, size_t workspace_bytes, clover_stream_t stream) {
+  int rc;
+  if ((rc = check_dims(dims))) return rc;
+  if ((rc = check_tokens(M))) return rc;
+  if (!head_w || !x || !tokens || !masked) return fail(CLOVER_ERR_INVALID_ARG, "NULL head_w/x/tokens/masked");
+  if (!aligned16(head_w) || !aligned16(x)) return fail(CLOVER_ERR_INVALID_ARG, "head_w/x not 16-byte aligned");
+  if (block < 1) return fail(CLOVER_ERR_INVALID_ARG, "block=%d < 1", block);
+  if (!(threshold == threshold)) return fail(CLOVER_ERR_INVALID_ARG, "threshold is NaN");
+  if ((rc = check_ws(workspace, workspace_bytes, kCtrlBytes + head_layout(*dims, M).bytes))) return rc;
+  if ((rc = get_encoder())) return rc;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* ctrl = reinterpret_cast<int*>(ws);
+  rc = enqueue_head(*dims, head_w, x, logit_scale, threshold, block, tokens, masked, argmax, max_logit, lse, max_prob,
+                    n_committed, M, ws + kCtrlBytes, ctrl, ctrl + kCtrlErr, Plan{di.sms},
+                    reinterpret_cast<cudaStream_t>(stream));
+  if (rc) return rc;
+  return check_launch_errors("lmhead unmask");
+}
+
+size_t clover_denoise_workspace_bytes(const clover_dims* dims, int32_t max_tokens) {
+  if (check_dims(dims) || check_tokens(max_tokens)) return 0;
+  return denoise_layout(*dims, max_tokens).bytes;
+}
+
+int clover_denoise_step(const clover_dims* dims, const clover_moe_layer* layers, int32_t n_layers,
+                        const uint16_t* embed, const float* ctx, const uint16_t* head_w, const float* logit_scale,
+                        float threshold, int32_t block, int32_t* tokens, uint8_t* masked, int32_t M,
+                        void* workspace, size_t workspace_bytes, clover_stream_t stream) {
+  return denoise_step_impl(dims, layers, n_layers, embed, ctx, head_w, logit_scale, threshold, block, tokens, masked,
+                           M, workspace, workspace_bytes, stream);
+}
+
+int clover_denoise_block(const clover_dims* dims, const clover_moe_layer* layers, int32_t n_layers,
+                         const uint16_t* embed, const float* ctx, const uint16_t* head_w, const float* logit_scale,
+                         float threshold, int32_t block, int32_t* tokens, uint8_t* masked, int32_t M,
+                         int32_t max_steps, int32_t* steps_taken, void* workspace, size_t workspace_bytes,
+                         clover_stream_t stream) {
+  if (steps_taken == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "steps_taken is NULL");
+  *steps_taken = 0;
+  if (max_steps < 0) return fail(CLOVER_ERR_INVALID_ARG, "max_steps < 0");
+  int rc;
+  if ((rc = check_tokens(M))) return rc;
+  if (masked == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "masked is NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t host_masked[kMaxTokens];
+  cudaError_t e = cudaMemcpyAsync(host_masked, masked, M, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the mask");
+  int left = 0;
+  for (int i = 0; i < M; ++i) left += host_masked[i] != 0;
+  int steps = 0;
+  while (left > 0 && steps < max_steps) {
+    rc = denoise_step_impl(dims, layers, n_layers, embed, ctx, head_w, logit_scale, threshold, block, tokens, masked,
+                           M, workspace, workspace_bytes, stream);
+    if (rc) return rc;
+    int words[3] = {0, 0, 0};
+    e = cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the step status");
+    ++steps;
+    *steps_taken = steps;
+    if (words[kCtrlErr] != 0)
+      return fail(CLOVER_ERR_DEVICE_TIMEOUT, "kernel status 0x%x after step %d", words[kCtrlErr], steps);
+    left = words[kCtrlMaskedLeft];
+  }
+  if (left > 0) return fail(CLOVER_ERR_NOT_CONVERGED, "%d positions still masked after %d steps", left, steps);
+  return CLOVER_OK;
+}
+
+int clover_workspace_status(void* workspace, size_t workspace_bytes, clover_stream_t stream) {
+  if (workspace == nullptr || workspace_bytes < kCtrlBytes) return fail(CLOVER_ERR_INVALID_ARG, "bad workspace");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
+  if (word == 0) return CLOVER_OK;
+  // Clear the status word and the arrival counters a failed kernel may have
+  // left behind, so the workspace is usable again.
+  e = cudaMemset(workspace, 0, kCtrlBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
+  char what[160] = {0};
+  snprintf(what, sizeof(what), "%s%s%s%s", (word & kErrMbarTimeout) ? "pipeline wait timed out; " : "",
+           (word & kErrDepTimeout) ? "cross-CTA dependency wait timed out; " : "",
+           (word & kErrBadToken) ? "token id out of range (clamped); " : "",
+           (word & kErrBadRoute) ? "expert id out of range; " : "");
+  return fail(CLOVER_ERR_DEVICE_TIMEOUT, "device status 0x%x: %s", word, what);
+}
+
+int32_t clover_profile_expert_events(clover_event_t* begin, clover_event_t* end, int32_t capacity) {
+  const int n = g_prof.count;
+  g_prof.begin = reinterpret_cast<cudaEvent_t*>(begin);
+  g_prof.end = reinterpret_cast<cudaEvent_t*>(end);
+  g_prof.cap = (begin && end) ? capacity : 0;
+  g_prof.count = 0;
+  return n;
+}
+
+int32_t clover_last_error(char* buf, size_t n) {
+  const size_t len = strlen(g_err);
+  if (buf && n > 0) {
+    const size_t c = len < n - 1 ? len : n - 1;
+    memcpy(buf, g_err, c);
+    buf[c] = '\0';
+  }
+  return static_cast<int32_t>(len);
+}
+
+int32_t clover_version(void) { return 100; }
+
+}  // extern "C"

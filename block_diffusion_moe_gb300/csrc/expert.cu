@@ -1,0 +1,529 @@
+// Grouped SwiGLU experts (routed + shared) with the weighted combine, as one
+// persistent tcgen05 kernel per MoE sublayer.
+//
+// Follows "Clover-35B-A3B: how a diffusion model gets to 680 tokens a second,
+// read from its files", section "What Clover is" (one expert = gate and up at
+// 2,048 x 512, down at 512 x 2,048; one always-on shared expert) and section
+// "The expert selection" (a block reads the union of its tokens' experts).
+//
+// Work is cut into equal-sized units that every CTA pulls from a global
+// counter:
+//   gate/up unit (expert a, slice s): A = 64 gate rows + the matching 64 up
+//     rows (128 x H, 512 KB at H = 2048), B = the expert's gathered bf16
+//     inputs; the epilogue forms h = silu(gate) * up, rounds it to bf16 and
+//     stores its 64 columns of h.
+//   down unit (expert a, slice j): A = rows j*128..j*128+127 of W_down
+//     (128 x F, 128 KB), B = the expert's h rows; the epilogue stores the
+//     unweighted expert output rows for those 128 hidden dims.
+// Weights play the M = 128 side of tcgen05.mma and tokens the N side (N = the
+// expert's token count rounded up to 16), so each selected expert's weights
+// stream from HBM exactly once per call while the MMA shape stays legal for
+// one or two tokens. All gate/up units come before all down units in the
+// counter order; a down unit's activation loads wait (bounded) until the 8
+// gate/up slices of its expert have published h, which cannot deadlock
+// because those units were claimed earlier by running CTAs.
+// The last down unit to finish a 128-wide hidden slice sums, for every token,
+// its K weighted expert rows in selection order plus the shared expert row
+// and adds them to the residual stream: a fixed summation order, so results
+// do not depend on scheduling.
+//
+// Warp roles (224 threads): warp 0 lane 0 streams weights (A) with TMA,
+// warp 1 owns TMEM and lane 0 issues the MMAs, warp 2 lane 0 streams
+// activations (B) with TMA, warps 3..6 are the epilogue (each reads the TMEM
+// lane quarter warp % 4). Two TMEM accumulators of 256 columns let the
+// epilogue of one unit overlap the MMAs of the next.
+#include <math.h>
+
+#include "kernels.cuh"
+#include "launch.cuh"
+#include "sm100.cuh"
+
+namespace clover {
+
+namespace {
+
+constexpr int kUnitEnd = -1;
+constexpr int kUnitAbort = -2;
+
+struct Unit {
+  int kind;   // 0 gate/up, 1 down
+  int a;      // active-expert index; 0 is the shared expert
+  int e;      // expert id (E for the shared expert)
+  int slice;  // F/64 slice (gate/up) or H/128 slice (down)
+  int cnt;    // tokens routed to the expert
+  int off;    // first row of the expert in the gathered buffers
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, int n_exp, const ExpertArgs& p) {
+  const int SF = p.F >> 6, SH = p.H >> 7;
+  Unit w;
+  const int n_gu = n_exp * SF;
+  if (u < n_gu) {
+    w.kind = 0;
+    w.a = u / SF;
+    w.slice = u - w.a * SF;
+  } else {
+    const int v = u - n_gu;
+    w.kind = 1;
+    w.a = v / SH;
+    w.slice = v - w.a * SH;
+  }
+  if (w.a == 0) {
+    w.e = p.E;
+    w.cnt = p.M;
+    w.off = p.M * p.K;
+  } else {
+    w.e = p.act[w.a - 1];
+    w.cnt = p.cnt[w.e];
+    w.off = p.off[w.e];
+  }
+  return w;
+}
+
+struct Smem {
+  uint8_t* a_ring;
+  uint8_t* b_ring;
+  float* xch;  // [64][17] up-half exchange for SwiGLU
+  uint64_t *full_a, *empty_a, *full_b, *empty_b, *tfull, *tempty, *ufull, *uempty, *drain;
+  int* unit_ids;  // [4]
+  uint32_t* tmem_slot;
+  volatile uint32_t* abort;
+  volatile int* s_last;
+  volatile int* s_unit;
+  volatile int* s_ok;
+  uint32_t b_stage_bytes;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
+  Smem s;
+  const uint32_t r = smem_u32(raw);
+  uint8_t* base = raw + ((1024u - (r & 1023u)) & 1023u);
+  s.b_stage_bytes = static_cast<uint32_t>(p.nb_max) * 128u;
+  s.a_ring = base;
+  s.b_ring = s.a_ring + static_cast<size_t>(p.stages_a) * kATileBytes;
+  s.xch = reinterpret_cast<float*>(s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 64 * 17);
+  s.full_a = bars;
+  s.empty_a = s.full_a + p.stages_a;
+  s.full_b = s.empty_a + p.stages_a;
+  s.empty_b = s.full_b + p.stages_b;
+  s.tfull = s.empty_b + p.stages_b;
+  s.tempty = s.tfull + 2;
+  s.ufull = s.tempty + 2;
+  s.uempty = s.ufull + kExpertUnitRing;
+  s.drain = s.uempty + kExpertUnitRing;
+  s.unit_ids = reinterpret_cast<int*>(s.drain + 1);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.unit_ids + kExpertUnitRing);
+  s.abort = s.tmem_slot + 1;
+  s.s_last = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
+  s.s_unit = s.s_last + 1;
+  s.s_ok = s.s_last + 2;
+  return s;
+}
+
+__device__ __forceinline__ void raise_abort(const Smem& s, int* err, int code) {
+  atomicOr(err, code);
+  *s.abort = 1u;
+}
+
+// Waits (bounded) for the TMA copies still in flight on a ring after an
+// abort, so that the CTA never exits with copies landing in its memory.
+__device__ void drain_ring(uint64_t* full, int stages, uint32_t issued_mask, uint32_t parity_bits) {
+  for (int i = 0; i < stages; ++i)
+    if (issued_mask & (1u << i)) mbar_wait_for(&full[i], (parity_bits >> i) & 1u, 200000000ull);
+}
+
+__device__ void producer_a(const ExpertArgs& p, const Smem& s, int n_exp, int n_total) {
+  const uint64_t pol = l2_policy_evict_first();
+  const int SA = p.stages_a;
+  int sa = 0;
+  uint32_t pha = 0, issued = 0, parity_bits = 0;
+  for (int it = 0;; ++it) {
+    int u = atomicAdd(p.unit_ctr, 1);
+    if (u >= n_total) u = kUnitEnd;
+    const int us = it & (kExpertUnitRing - 1);
+    const uint32_t upar = (it / kExpertUnitRing) & 1;
+    if (!mbar_wait(&s.uempty[us], upar ^ 1u, s.abort)) {
+      raise_abort(s, p.err, kErrMbarTimeout);
+      break;
+    }
+    s.unit_ids[us] = u;
+    mbar_arrive(&s.ufull[us]);
+    if (u < 0) break;
+    const Unit w = decode_unit(u, n_exp, p);
+    const CUtensorMap* m;
+    int row, nk;
+    if (w.kind == 0) {
+      m = (w.a == 0) ? &p.tm_sgu : &p.tm_gu;
+      row = (w.a == 0 ? 0 : w.e * 2 * p.F) + w.slice * 64;
+      nk = p.H >> 6;
+    } else {
+      m = (w.a == 0) ? &p.tm_sdn : &p.tm_dn;
+      row = (w.a == 0 ? 0 : w.e * p.H) + w.slice * 128;
+      nk = p.F >> 6;
+    }
+    bool ok = true;
+    for (int kc = 0; kc < nk; ++kc) {
+      if (!mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
+        raise_abort(s, p.err, kErrMbarTimeout);
+        ok = false;
+        break;
+      }
+      const uint32_t dst = smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes);
+      mbar_arrive_expect_tx(&s.full_a[sa], kATileBytes);
+      if (w.kind == 0) {
+        tma_load_2d(dst, m, &s.full_a[sa], kc * 64, row, pol);           // 64 gate rows
+        tma_load_2d(dst + 8192, m, &s.full_a[sa], kc * 64, row + p.F, pol);  // 64 up rows
+      } else {
+        tma_load_2d(dst, m, &s.full_a[sa], kc * 64, row, pol);  // 128 down rows
+      }
+      issued |= 1u << sa;
+      parity_bits = (parity_bits & ~(1u << sa)) | (pha << sa);
+      if (++sa == SA) {
+        sa = 0;
+        pha ^= 1u;
+      }
+    }
+    if (!ok) break;
+  }
+  if (*s.abort) drain_ring(s.full_a, SA, issued, parity_bits);
+}
+
+__device__ void producer_b(const ExpertArgs& p, const Smem& s, int n_exp) {
+  const uint64_t pol = l2_policy_evict_last();
+  const int SB = p.stages_b;
+  const int SF = p.F >> 6;
+  int sb = 0;
+  uint32_t phb = 0, issued = 0, parity_bits = 0;
+  for (int it = 0;; ++it) {
+    const int us = it & (kExpertUnitRing - 1);
+    const uint32_t upar = (it / kExpertUnitRing) & 1;
+    if (!mbar_wait(&s.ufull[us], upar, s.abort)) {
+      raise_abort(s, p.err, kErrMbarTimeout);
+      break;
+    }
+    const int u = s.unit_ids[us];
+    mbar_arrive(&s.uempty[us]);
+    if (u < 0) break;
+    const Unit w = decode_unit(u, n_exp, p);
+    const int nrows = (w.cnt + 15) & ~15;
+    const CUtensorMap* m;
+    int nk;
+    if (w.kind == 0) {
+      m = &p.tm_xg;
+      nk = p.H >> 6;
+    } else {
+      m = &p.tm_h;
+      nk = p.F >> 6;
+      // The expert's SwiGLU rows must be complete before they are loaded.
+      const unsigned long long t0 = global_ns();
+      bool ok = true;
+      while (ld_acquire_gpu(&p.gu_done[w.a]) < SF) {
+        if (*s.abort) {
+          ok = false;
+          break;
+        }
+        if (global_ns() - t0 > kWaitLimitNs) {
+          raise_abort(s, p.err, kErrDepTimeout);
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+      if (!ok) break;
+      fence_proxy_async_global();
+    }
+    bool ok = true;
+    for (int kc = 0; kc < nk; ++kc) {
+      if (!mbar_wait(&s.empty_b[sb], phb ^ 1u, s.abort)) {
+        raise_abort(s, p.err, kErrMbarTimeout);
+        ok = false;
+        break;
+      }
+      const uint32_t dst = smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes);
+      mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(nrows) * 128u);
+      for (int i = 0; i < nrows; i += 16) tma_load_2d(dst + i * 128, m, &s.full_b[sb], kc * 64, w.off + i, pol);
+      issued |= 1u << sb;
+      parity_bits = (parity_bits & ~(1u << sb)) | (phb << sb);
+      if (++sb == SB) {
+        sb = 0;
+        phb ^= 1u;
+      }
+    }
+    if (!ok) break;
+  }
+  if (*s.abort) drain_ring(s.full_b, SB, issued, parity_bits);
+}
+
+__device__ void mma_issuer(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t tmem_base) {
+  const int SA = p.stages_a, SB = p.stages_b;
+  int sa = 0, sb = 0;
+  uint32_t pha = 0, phb = 0;
+  for (int it = 0;; ++it) {
+    const int us = it & (kExpertUnitRing - 1);
+    const uint32_t upar = (it / kExpertUnitRing) & 1;
+    if (!mbar_wait(&s.ufull[us], upar, s.abort)) {
+      raise_abort(s, p.err, kErrMbarTimeout);
+      break;
+    }
+    const int u = s.unit_ids[us];
+    mbar_arrive(&s.uempty[us]);
+    if (u < 0) break;
+    const Unit w = decode_unit(u, n_exp, p);
+    const int n = (w.cnt + 15) & ~15;
+    const int nk = (w.kind == 0) ? (p.H >> 6) : (p.F >> 6);
+    const uint32_t idesc = umma_idesc_bf16(128, n);
+    const int acc = it & 1;
+    const uint32_t apar = (it >> 1) & 1;
+    if (!mbar_wait(&s.tempty[acc], apar ^ 1u, s.abort)) {
+      raise_abort(s, p.err, kErrMbarTimeout);
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * 256u;
+    bool ok = true;
+    for (int kc = 0; kc < nk; ++kc) {
+      if (!mbar_wait(&s.full_a[sa], pha, s.abort) || !mbar_wait(&s.full_b[sb], phb, s.abort)) {
+        raise_abort(s, p.err, kErrMbarTimeout);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint64_t ad = umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes));
+      const uint64_t bd = umma_desc_sw128(smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes));
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                  (kc | k) != 0 ? 1u : 0u);
+      umma_commit(&s.empty_a[sa]);
+      umma_commit(&s.empty_b[sb]);
+      if (++sa == SA) {
+        sa = 0;
+        pha ^= 1u;
+      }
+      if (++sb == SB) {
+        sb = 0;
+        phb ^= 1u;
+      }
+    }
+    if (!ok) break;
+    umma_commit(&s.tfull[acc]);
+  }
+  // Every MMA this thread issued must be complete before TMEM is released.
+  umma_commit(s.drain);
+  mbar_wait_for(s.drain, 0, 200000000ull);
+}
+
+// Sums the weighted expert rows of one 128-wide hidden slice into the
+// residual stream: x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t).
+__device__ void combine_slice(const ExpertArgs& p, int j, int etid) {
+  const int c4 = (etid & 31) * 4;
+  const int g = etid >> 5;
+  const size_t H = p.H;
+  const size_t col = static_cast<size_t>(j) * 128 + c4;
+  const int MK = p.M * p.K;
+  for (int t = g; t < p.M; t += 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < p.K; ++k) {
+      const int r = p.tok_slot[t * p.K + k];
+      const float wk = p.topk_w[t * p.K + k];
+      const float4 y = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(r) * H + col));
+      acc.x = fmaf(wk, y.x, acc.x);
+      acc.y = fmaf(wk, y.y, acc.y);
+      acc.z = fmaf(wk, y.z, acc.z);
+      acc.w = fmaf(wk, y.w, acc.w);
+    }
+    const float4 ys = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t) * H + col));
+    acc.x += ys.x;
+    acc.y += ys.y;
+    acc.z += ys.z;
+    acc.w += ys.w;
+    const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * H + col);
+    float4 o;
+    o.x = xi.x + acc.x;
+    o.y = xi.y + acc.y;
+    o.z = xi.z + acc.z;
+    o.w = xi.w + acc.w;
+    *reinterpret_cast<float4*>(p.x_out + static_cast<size_t>(t) * H + col) = o;
+  }
+}
+
+__device__ void epilogue(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t tmem_base) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;             // TMEM lane quarter this warp may read
+  const int row = q * 32 + lane;      // accumulator row
+  const int etid = threadIdx.x - 96;  // 0..127
+  const int SF = p.F >> 6;
+  for (int it = 0;; ++it) {
+    const int us = it & (kExpertUnitRing - 1);
+    const uint32_t upar = (it / kExpertUnitRing) & 1;
+    if (etid == 0) {
+      int u = kUnitAbort;
+      if (mbar_wait(&s.ufull[us], upar, s.abort)) {
+        u = s.unit_ids[us];
+        mbar_arrive(&s.uempty[us]);
+      } else {
+        raise_abort(s, p.err, kErrMbarTimeout);
+      }
+      *s.s_unit = u;
+    }
+    named_bar_sync(1, 128);
+    const int u = *s.s_unit;
+    if (u < 0) break;
+    const Unit w = decode_unit(u, n_exp, p);
+    const int n = (w.cnt + 15) & ~15;
+    const int acc = it & 1;
+    const uint32_t apar = (it >> 1) & 1;
+    if (etid == 0) {
+      const bool ok = mbar_wait(&s.tfull[acc], apar, s.abort);
+      if (!ok) raise_abort(s, p.err, kErrMbarTimeout);
+      *s.s_ok = ok ? 1 : 0;
+    }
+    named_bar_sync(1, 128);
+    if (!*s.s_ok) break;
+    tc_fence_after();
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * 256u;
+    if (w.kind == 0) {
+      const int f = w.slice * 64 + row;  // meaningful for the gate half (q < 2)
+      bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + f;
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        float v[16];
+        __syncwarp();
+        tmem_ld16(tb + c0, v);
+        if (q >= 2) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) s.xch[(row - 64) * 17 + j] = v[j];
+        }
+        named_bar_sync(1, 128);
+        if (q < 2) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = c0 + j;
+            if (c < w.cnt) {
+              const float g = v[j];
+              const float up = s.xch[row * 17 + j];
+              const float h = g / (1.0f + expf(-g)) * up;
+              hrow[static_cast<size_t>(c) * p.F] = __float2bfloat16_rn(h);
+            }
+          }
+        }
+        named_bar_sync(1, 128);
+      }
+      tc_fence_before();
+      fence_proxy_async_global();
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (etid == 0) {
+        mbar_arrive(&s.tempty[acc]);
+        red_release_gpu_add(&p.gu_done[w.a], 1);
+      }
+    } else {
+      float* ycol = p.yslot + static_cast<size_t>(w.off) * p.H + static_cast<size_t>(w.slice) * 128 + row;
+      for (int c0 = 0; c0 < n; c0 += 16) {
+        float v[16];
+        __syncwarp();
+        tmem_ld16(tb + c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          if (c < w.cnt) ycol[static_cast<size_t>(c) * p.H] = v[j];
+        }
+      }
+      tc_fence_before();
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (etid == 0) {
+        mbar_arrive(&s.tempty[acc]);
+        const int old = atomicAdd(&p.dn_done[w.slice], 1);
+        *s.s_last = (old == n_exp - 1) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (*s.s_last) {
+        __threadfence();
+        combine_slice(p, w.slice, etid);
+      }
+    }
+    (void)SF;
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_constant__ ExpertArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem s = carve(smem_raw, p);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages_a; ++i) {
+      mbar_init(&s.full_a[i], 1);
+      mbar_init(&s.empty_a[i], 1);
+    }
+    for (int i = 0; i < p.stages_b; ++i) {
+      mbar_init(&s.full_b[i], 1);
+      mbar_init(&s.empty_b[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 1);
+    }
+    for (int i = 0; i < kExpertUnitRing; ++i) {
+      mbar_init(&s.ufull[i], 1);
+      mbar_init(&s.uempty[i], 3);  // B loader, MMA issuer, epilogue leader
+    }
+    mbar_init(s.drain, 1);
+    *s.abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_gu);
+    tma_prefetch_desc(&p.tm_sgu);
+    tma_prefetch_desc(&p.tm_dn);
+    tma_prefetch_desc(&p.tm_sdn);
+  }
+  if (warp == 1) {
+    tmem_alloc(s.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s.tmem_slot;
+
+  pdl_wait();
+  const int n_exp = *p.n_active + 1;
+  const int n_total = n_exp * ((p.F >> 6) + (p.H >> 7));
+
+  if (warp == 0) {
+    if (lane == 0) producer_a(p, s, n_exp, n_total);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(p, s, n_exp, tmem_base);
+  } else if (warp == 2) {
+    if (lane == 0) producer_b(p, s, n_exp);
+  } else {
+    epilogue(p, s, n_exp, tmem_base);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+  pdl_trigger();
+}
+
+size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {
+  return 1024 + static_cast<size_t>(stages_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
+         64 * 17 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
+         128;
+}
+
+cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(k_expert, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k_expert, dim3(grid), dim3(kExpertThreads), smem, s, pdl, a);
+}
+
+}  // namespace clover

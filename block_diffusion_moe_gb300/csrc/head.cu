@@ -1,0 +1,376 @@
+// Untied output head fused with the per-position statistics and the
+// low-confidence unmask rule.
+//
+// Follows "Clover-35B-A3B: how a diffusion model gets to 680 tokens a second,
+// read from its files": section "What Clover is" (the 248,320 x 2,048 head is
+// untied and read in full at every step; mask token 151669; low-confidence
+// threshold 0.95) and section "How it writes", steps 2-3 (the mask token's
+// logit is minus infinity; every still-masked slot above the threshold is
+// committed, else the single most confident one).
+//
+// Each CTA owns vocabulary tiles blockIdx.x, blockIdx.x + G, ...; a tile is
+// 128 head rows (the M = 128 side of tcgen05.mma) against all positions (the
+// N side). The epilogue turns each 128 x N accumulator into per-position
+// (max, sum of exp relative to the max, argmax) and folds it into a running
+// per-CTA state, so the logits never leave the SM. The last CTA to finish
+// merges the G partial states in CTA order, derives log-sum-exp and the
+// maximum probability, and applies the unmask rule to every block of
+// positions. Ties in the argmax go to the lowest vocabulary id at every level.
+#include <math.h>
+
+#include "kernels.cuh"
+#include "launch.cuh"
+#include "sm100.cuh"
+
+namespace clover {
+
+namespace {
+
+struct HeadSmem {
+  uint8_t* ring;  // stages x (A tile 16 KB + B tile nb x 128 B)
+  float* wp_m;    // [4][nb]
+  float* wp_s;    // [4][nb]
+  int* wp_a;      // [4][nb]
+  float* run_m;   // [nb]
+  float* run_s;   // [nb]
+  int* run_a;     // [nb]
+  float* alpha;   // [nb]
+  uint64_t *full, *empty, *tfull, *tempty, *drain;
+  uint32_t* tmem_slot;
+  volatile uint32_t* abort;
+  volatile int* s_ok;
+  volatile int* s_last;
+  int* s_counts;  // [2]: committed, still masked
+  uint32_t stage_bytes;
+};
+
+__device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int nb) {
+  HeadSmem s;
+  const uint32_t r = smem_u32(raw);
+  uint8_t* base = raw + ((1024u - (r & 1023u)) & 1023u);
+  s.stage_bytes = kATileBytes + static_cast<uint32_t>(nb) * 128u;
+  s.ring = base;
+  float* f = reinterpret_cast<float*>(base + static_cast<size_t>(p.stages) * s.stage_bytes);
+  s.wp_m = f;
+  s.wp_s = s.wp_m + 4 * nb;
+  s.wp_a = reinterpret_cast<int*>(s.wp_s + 4 * nb);
+  s.run_m = reinterpret_cast<float*>(s.wp_a + 4 * nb);
+  s.run_s = s.run_m + nb;
+  s.run_a = reinterpret_cast<int*>(s.run_s + nb);
+  s.alpha = reinterpret_cast<float*>(s.run_a + nb);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.alpha + nb);  // nb % 16 == 0 keeps 8-byte alignment
+  s.full = bars;
+  s.empty = s.full + p.stages;
+  s.tfull = s.empty + p.stages;
+  s.tempty = s.tfull + 2;
+  s.drain = s.tempty + 2;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+  s.abort = s.tmem_slot + 1;
+  s.s_ok = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
+  s.s_last = s.s_ok + 1;
+  s.s_counts = const_cast<int*>(s.s_last + 1);
+  return s;
+}
+
+// Folds the partial (m2, s2, a2) into (m, s, a): m = max, s rescaled to the
+// new max, a = lowest id attaining the max.
+__device__ __forceinline__ void lse_merge(float& m, float& s, int& a, float m2, float s2, int a2) {
+  if (m2 > m) {
+    s = s * expf(m - m2) + s2;  // expf(-inf) = 0 covers an empty (m = -inf) state
+    m = m2;
+    a = a2;
+  } else if (m2 == m) {
+    s += s2;
+    a = min(a, a2);
+  } else {
+    s += s2 * expf(m2 - m);
+  }
+}
+
+__device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
+  const uint64_t pol_w = l2_policy_evict_first();
+  const uint64_t pol_x = l2_policy_evict_last();
+  const int nk = p.H >> 6;
+  int st = 0;
+  uint32_t ph = 0, issued = 0, parity_bits = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
+    for (int kc = 0; kc < nk; ++kc) {
+      if (!mbar_wait(&s.empty[st], ph ^ 1u, s.abort)) {
+        atomicOr(p.err, kErrMbarTimeout);
+        *s.abort = 1u;
+        ok = false;
+        break;
+      }
+      const uint32_t dst = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
+      mbar_arrive_expect_tx(&s.full[st], s.stage_bytes);
+      tma_load_2d(dst, &p.tm_w, &s.full[st], kc * 64, tile * 128, pol_w);
+      for (int i = 0; i < nb; i += 16) tma_load_2d(dst + kATileBytes + i * 128, &p.tm_x, &s.full[st], kc * 64, i, pol_x);
+      issued |= 1u << st;
+      parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+      if (++st == p.stages) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+  }
+  if (*s.abort) {
+    for (int i = 0; i < p.stages; ++i)
+      if (issued & (1u << i)) mbar_wait_for(&s.full[i], (parity_bits >> i) & 1u, 200000000ull);
+  }
+}
+
+__device__ void head_mma(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t tmem_base) {
+  const int nk = p.H >> 6;
+  const uint32_t idesc = umma_idesc_bf16(128, nb);
+  int st = 0;
+  uint32_t ph = 0;
+  int it = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x, ++it) {
+    const int acc = it & 1;
+    const uint32_t apar = (it >> 1) & 1;
+    if (!mbar_wait(&s.tempty[acc], apar ^ 1u, s.abort)) {
+      atomicOr(p.err, kErrMbarTimeout);
+      *s.abort = 1u;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * 256u;
+    for (int kc = 0; kc < nk; ++kc) {
+      if (!mbar_wait(&s.full[st], ph, s.abort)) {
+        atomicOr(p.err, kErrMbarTimeout);
+        *s.abort = 1u;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
+      const uint64_t ad = umma_desc_sw128(a_addr);
+      const uint64_t bd = umma_desc_sw128(a_addr + kATileBytes);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                  (kc | k) != 0 ? 1u : 0u);
+      umma_commit(&s.empty[st]);
+      if (++st == p.stages) {
+        st = 0;
+        ph ^= 1u;
+      }
+    }
+    if (ok) umma_commit(&s.tfull[acc]);
+  }
+  umma_commit(s.drain);
+  mbar_wait_for(s.drain, 0, 200000000ull);
+}
+
+__device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t tmem_base) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;
+  const int row = q * 32 + lane;
+  const int etid = threadIdx.x - 64;  // 0..127
+  for (int n = etid; n < nb; n += 128) {
+    s.run_m[n] = -INFINITY;
+    s.run_s[n] = 0.f;
+    s.run_a[n] = 0x7fffffff;
+    s.alpha[n] = (n < p.M && p.alpha != nullptr) ? p.alpha[n] : 1.0f;
+  }
+  named_bar_sync(1, 128);
+  int it = 0;
+  for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++it) {
+    const int acc = it & 1;
+    const uint32_t apar = (it >> 1) & 1;
+    if (etid == 0) {
+      const bool ok = mbar_wait(&s.tfull[acc], apar, s.abort);
+      if (!ok) {
+        atomicOr(p.err, kErrMbarTimeout);
+        *s.abort = 1u;
+      }
+      *s.s_ok = ok ? 1 : 0;
+    }
+    named_bar_sync(1, 128);
+    if (!*s.s_ok) break;
+    tc_fence_after();
+    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * 256u;
+    const int vid = tile * 128 + row;
+    const bool valid_row = (vid < p.V) && (vid != p.mask_id);
+    for (int c0 = 0; c0 < nb; c0 += 16) {
+      float v[16];
+      __syncwarp();
+      tmem_ld16(tb + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int c = c0 + j;
+        const float z = valid_row ? v[j] * s.alpha[c] : -INFINITY;
+        const float m = warp_max_f(z);
+        const unsigned bal = __ballot_sync(0xffffffffu, z == m && m != -INFINITY);
+        const float e = (m == -INFINITY) ? 0.f : expf(z - m);
+        const float sum = warp_sum_f(e);
+        if (lane == 0) {
+          s.wp_m[q * nb + c] = m;
+          s.wp_s[q * nb + c] = sum;
+          s.wp_a[q * nb + c] = bal ? tile * 128 + q * 32 + (__ffs(bal) - 1) : 0x7fffffff;
+        }
+      }
+      if (c0 + 16 >= nb) {
+        // all TMEM reads of this accumulator are done
+        tc_fence_before();
+      }
+      named_bar_sync(1, 128);
+      if (etid < 16) {
+        const int c = c0 + etid;
+        float m = s.run_m[c], sm = s.run_s[c];
+        int a = s.run_a[c];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) lse_merge(m, sm, a, s.wp_m[w * nb + c], s.wp_s[w * nb + c], s.wp_a[w * nb + c]);
+        s.run_m[c] = m;
+        s.run_s[c] = sm;
+        s.run_a[c] = a;
+      }
+      named_bar_sync(1, 128);
+    }
+    if (etid == 0) mbar_arrive(&s.tempty[acc]);
+  }
+  // Leave together if any role gave up (the decision is broadcast so that no
+  // epilogue thread is left waiting on the named barrier).
+  named_bar_sync(1, 128);
+  if (etid == 0) *s.s_ok = (*s.abort == 0u) ? 1 : 0;
+  named_bar_sync(1, 128);
+  if (!*s.s_ok) return;
+
+  // Publish this CTA's partial state, then let the last CTA merge all of them.
+  const int G = gridDim.x;
+  for (int n = etid; n < p.M; n += 128) {
+    p.part_m[static_cast<size_t>(blockIdx.x) * p.M + n] = s.run_m[n];
+    p.part_s[static_cast<size_t>(blockIdx.x) * p.M + n] = s.run_s[n];
+    p.part_a[static_cast<size_t>(blockIdx.x) * p.M + n] = s.run_a[n];
+  }
+  __threadfence();
+  named_bar_sync(1, 128);
+  if (etid == 0) {
+    const int old = atomicAdd(p.done_ctr, 1);
+    *s.s_last = (old == G - 1) ? 1 : 0;
+    s.s_counts[0] = 0;
+    s.s_counts[1] = 0;
+  }
+  named_bar_sync(1, 128);
+  if (!*s.s_last) return;
+  __threadfence();
+  for (int n = etid; n < p.M; n += 128) {
+    float m = -INFINITY, sm = 0.f;
+    int a = 0x7fffffff;
+    for (int b = 0; b < G; ++b) {
+      const size_t i = static_cast<size_t>(b) * p.M + n;
+      lse_merge(m, sm, a, __ldcg(p.part_m + i), __ldcg(p.part_s + i), __ldcg(p.part_a + i));
+    }
+    const float lse = m + logf(sm);
+    const float pmax = 1.0f / sm;  // = exp(m - lse)
+    if (p.argmax) p.argmax[n] = a;
+    if (p.max_logit) p.max_logit[n] = m;
+    if (p.lse) p.lse[n] = lse;
+    if (p.max_prob) p.max_prob[n] = pmax;
+    s.run_m[n] = pmax;  // reuse: per-position max probability
+    s.run_a[n] = a;
+  }
+  named_bar_sync(1, 128);
+  // Unmask rule, one thread per block of positions.
+  const int nblk = (p.M + p.block - 1) / p.block;
+  for (int b = etid; b < nblk; b += 128) {
+    const int p0 = b * p.block, p1 = min(p.M, p0 + p.block);
+    int n_commit = 0, best = -1;
+    float best_p = 0.f;
+    for (int i = p0; i < p1; ++i) {
+      if (!p.masked[i]) continue;
+      const float pm = s.run_m[i];
+      if (pm > p.threshold) ++n_commit;
+      if (best < 0 || pm > best_p) {
+        best = i;
+        best_p = pm;
+      }
+    }
+    int still = 0, done = 0;
+    for (int i = p0; i < p1; ++i) {
+      if (!p.masked[i]) continue;
+      const bool c = (n_commit > 0) ? (s.run_m[i] > p.threshold) : (i == best);
+      if (c) {
+        p.tokens[i] = s.run_a[i];
+        p.masked[i] = 0;
+        ++done;
+      } else {
+        ++still;
+      }
+    }
+    atomicAdd(&s.s_counts[0], done);
+    atomicAdd(&s.s_counts[1], still);
+  }
+  named_bar_sync(1, 128);
+  if (etid == 0) {
+    if (p.n_committed) *p.n_committed = s.s_counts[0];
+    if (p.n_masked_left) *p.n_masked_left = s.s_counts[1];
+    *p.done_ctr = 0;
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant__ HeadArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const int nb = (p.M + 15) & ~15;
+  const HeadSmem s = carve(smem_raw, p, nb);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&s.full[i], 1);
+      mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s.tfull[i], 1);
+      mbar_init(&s.tempty[i], 1);
+    }
+    mbar_init(s.drain, 1);
+    *s.abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tm_w);
+    tma_prefetch_desc(&p.tm_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(s.tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s.tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) head_producer(p, s, nb);
+  } else if (warp == 1) {
+    if (lane == 0) head_mma(p, s, nb, tmem_base);
+  } else {
+    head_epilogue(p, s, nb, tmem_base);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+  pdl_trigger();
+}
+
+size_t head_smem_bytes(int stages, int nb) {
+  return 1024 + static_cast<size_t>(stages) * (kATileBytes + static_cast<size_t>(nb) * 128) +
+         static_cast<size_t>(nb) * (4 * 12 + 12 + 4) + static_cast<size_t>(2 * stages + 5) * 8 + 64;
+}
+
+cudaError_t launch_head(const HeadArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(k_head, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k_head, dim3(grid), dim3(kHeadThreads), smem, s, pdl, a);
+}
+
+}  // namespace clover

@@ -1,0 +1,134 @@
+// Kernel argument blocks and launch wrappers shared by the host API and the
+// kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace clover {
+
+using bf16 = __nv_bfloat16;
+
+// Routing kernel tiling: 8 experts x 32 tokens per CTA.
+constexpr int kRouteExperts = 8;
+constexpr int kRouteTokens = 32;
+constexpr int kMaxTokens = 256;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+
+// Expert kernel: 7 warps (A loads, MMA, B loads, 4 epilogue warps).
+constexpr int kExpertThreads = 224;
+constexpr int kExpertUnitRing = 4;
+// Head kernel: 6 warps (loads, MMA, 4 epilogue warps).
+constexpr int kHeadThreads = 192;
+constexpr int kHeadMaxCtas = 512;
+
+constexpr int kATileBytes = 128 * 64 * 2;  // 128 rows x 64 bf16
+constexpr int kSmemBudget = 227 * 1024;
+
+struct EmbedArgs {
+  const int32_t* tokens;
+  const bf16* embed;  // [V][H]
+  const float* ctx;   // [M][H]
+  float* x;           // [M][H]
+  int* err;
+  int M, H, V;
+};
+
+struct NormArgs {
+  const float* x;  // [M][H]
+  bf16* xn;        // [M][H]
+  int M, H;
+  float eps;
+};
+
+struct RouteArgs {
+  const float* x;       // [M][H] residual stream
+  const bf16* wr;       // [E][H]
+  const float* bias;    // [E] or null
+  float* logits;        // [M][E]
+  bf16* xn_rows;        // [M][H] normed input (the shared expert's rows of the gathered buffer)
+  int* tg_ctr;          // [ceil(M/32)] arrival counters, zero between launches
+  int32_t* topk_idx;    // [M][K]
+  float* topk_w;        // [M][K]
+  int M, H, E, K;
+  float eps;
+};
+
+struct PermArgs {
+  const int32_t* topk_idx;  // [M][K]
+  const float* topk_w;      // [M][K]
+  int32_t* tok_slot;        // [M][K] -> row of the gathered buffer
+  int* cnt;                 // [E]
+  int* off;                 // [E]
+  int* act;                 // [E] active expert ids, ascending
+  int* n_active;            // scalar
+  int* unit_ctr;            // scalar, reset to 0
+  int* gu_done;             // [E+1], reset to 0
+  int* dn_done;             // [H/128], reset to 0
+  bf16* xg;                 // [M*K + M][H] gathered normed inputs
+  int32_t* out_idx;         // optional copies for the caller
+  float* out_w;
+  int M, H, E, K;
+};
+
+struct ExpertArgs {
+  CUtensorMap tm_gu;   // routed gate/up  [E*2F][H]
+  CUtensorMap tm_sgu;  // shared gate/up  [2F][H]
+  CUtensorMap tm_dn;   // routed down     [E*H][F]
+  CUtensorMap tm_sdn;  // shared down     [H][F]
+  CUtensorMap tm_xg;   // gathered inputs [M*K+M][H]
+  CUtensorMap tm_h;    // SwiGLU outputs  [M*K+M][F]
+  const float* x_in;
+  float* x_out;
+  bf16* hbuf;          // [M*K+M][F]
+  float* yslot;        // [M*K+M][H]
+  const int* n_active;
+  const int* act;
+  const int* cnt;
+  const int* off;
+  const int32_t* tok_slot;
+  const float* topk_w;
+  int* unit_ctr;
+  int* gu_done;
+  int* dn_done;
+  int* err;
+  int M, H, F, E, K;
+  int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
+};
+
+struct HeadArgs {
+  CUtensorMap tm_w;  // head [V][H]
+  CUtensorMap tm_x;  // normed positions [M][H]
+  const float* alpha;  // [M] or null
+  float* part_m;       // [G][M]
+  float* part_s;       // [G][M]
+  int* part_a;         // [G][M]
+  int* done_ctr;       // scalar, zero between launches
+  int32_t* tokens;     // [M] in/out
+  uint8_t* masked;     // [M] in/out
+  int32_t* argmax;     // [M] out (nullable)
+  float* max_logit;    // [M] out (nullable)
+  float* lse;          // [M] out (nullable)
+  float* max_prob;     // [M] out (nullable)
+  int* n_committed;    // scalar out (nullable)
+  int* n_masked_left;  // scalar out (nullable)
+  int* err;
+  int M, H, V, mask_id, block, n_tiles, stages;
+  float threshold;
+};
+
+// Launch wrappers (return the cudaError_t of the launch).
+cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_perm(const PermArgs& a, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
+cudaError_t launch_head(const HeadArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
+
+size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max);
+size_t head_smem_bytes(int stages, int nb);
+
+}  // namespace clover

@@ -1,0 +1,192 @@
+"""GPU vs oracle on the tiny configuration (1 MoE layer, hidden 256, 16
+experts top-2 + shared, SwiGLU 256->64->256, vocabulary 1,024, blocks of 8),
+plus ragged shapes and edge cases. Every call goes through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_diffusion_moe_gb300 import clover, synth
+from tests.helpers import (bits, calibrate_alpha, compare_head, compare_routing, decisions_clear, hidden_close,
+                           layer_to_oracle)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _dims(**kw):
+    import dataclasses
+    return dataclasses.replace(synth.TINY, **kw)
+
+
+@pytest.mark.parametrize("M", [8, 1, 5, 16, 37, 256])
+def test_moe_layer_matches_oracle(M):
+    d = synth.TINY
+    layer = synth.make_layer(d, 0, 0, DEV)
+    x = synth.make_x(d, M, 3, DEV)
+    x_out, idx, w = clover.moe_block_step(d, layer, x)
+    torch.cuda.synchronize()
+    L = layer_to_oracle(layer)
+    xh = x.cpu().numpy()
+    ref = O.moe_layer(xh, L, d.top_k, d.rms_eps)
+    compare_routing(idx.cpu().numpy(), w.cpu().numpy(), ref, d.top_k)
+    forced = O.moe_layer(xh, L, d.top_k, d.rms_eps, force_idx=idx.cpu().numpy())
+    g = x_out.cpu().numpy()
+    ok, worst = hidden_close(g, forced["x_out"])
+    assert ok, worst
+    ok, worst = hidden_close(g - xh, forced["x_out"] - xh)   # the MoE update alone
+    assert ok, worst
+
+
+def test_moe_layer_in_place_and_deterministic():
+    d = synth.TINY
+    layer = synth.make_layer(d, 1, 0, DEV, zipf_s=1.2)
+    x = synth.make_x(d, 64, 4, DEV)
+    a, ia, wa = clover.moe_block_step(d, layer, x)
+    b, ib, wb = clover.moe_block_step(d, layer, x)
+    xi = x.clone()
+    c, _, _ = clover.moe_block_step(d, layer, xi, x_out=xi)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(ia, ib) and torch.equal(wa, wb)
+    assert torch.equal(a, c)
+
+
+def test_zipf_bias_routes_like_oracle():
+    d = synth.TINY
+    layer = synth.make_layer(d, 2, 0, DEV, zipf_s=1.2)
+    x = synth.make_x(d, 128, 5, DEV)
+    x_out, idx, w = clover.moe_block_step(d, layer, x)
+    torch.cuda.synchronize()
+    L = layer_to_oracle(layer)
+    ref = O.moe_layer(x.cpu().numpy(), L, d.top_k, d.rms_eps)
+    compare_routing(idx.cpu().numpy(), w.cpu().numpy(), ref, d.top_k)
+    # the bias makes the popular experts popular
+    counts = np.bincount(idx.cpu().numpy().ravel(), minlength=d.n_experts)
+    top = int(np.argmax(layer.router_bias.cpu().numpy()))
+    assert counts[top] == counts.max()
+
+
+def _head_ref(d, head, x, alpha):
+    z = O.head_logits(x, bits(head), d.rms_eps, alpha)
+    st = O.head_stats(z, d.mask_id)
+    z = z.copy()
+    z[:, d.mask_id] = -np.inf
+    st["z"] = z
+    return st
+
+
+@pytest.mark.parametrize("V,M", [(1024, 8), (1000, 37), (1024, 256)])
+def test_head_unmask_matches_oracle(V, M):
+    d = _dims(vocab=V, mask_id=V - 1)
+    head = synth.make_head(d, 7, DEV)
+    x = synth.make_x(d, M, 8, DEV)
+    xh = x.cpu().numpy()
+    z_raw = O.head_logits(xh, bits(head), d.rms_eps)
+    alpha = calibrate_alpha(z_raw, d.mask_id, synth.confidence_targets(M, 9).numpy(), O)
+    tokens, masked = synth.masked_block(d, M, DEV)
+    masked[::3] = 0                       # some slots already committed
+    tokens[::3] = 5
+    t0, m0 = tokens.cpu().numpy(), masked.cpu().numpy()
+    a = torch.from_numpy(alpha).to(DEV)
+    out = clover.lmhead_unmask(d, head, x, tokens, masked, logit_scale=a, threshold=0.95, block=d.block)
+    torch.cuda.synchronize()
+    ref = _head_ref(d, head, xh, alpha)
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    compare_head(got, ref)
+    assert not np.any(got["argmax"] == d.mask_id)
+    if decisions_clear(ref["max_prob"], m0, 0.95, d.block):
+        rt, rm, rc = O.unmask(t0, m0, ref["argmax"], ref["max_prob"], 0.95, d.block)
+        assert np.array_equal(tokens.cpu().numpy(), rt)
+        assert np.array_equal(masked.cpu().numpy(), rm)
+        assert int(got["n_committed"][0]) == int(rc.sum())
+
+
+def test_head_mask_token_never_predicted():
+    d = synth.TINY
+    M = 16
+    x = synth.make_x(d, M, 10, DEV)
+    xh = x.cpu().numpy()
+    xb = O.round_to_bf16(O.rms_norm(xh, d.rms_eps))
+    head = synth.make_head(d, 11, DEV)
+    hh = head.float().cpu().numpy()
+    hh[d.mask_id] = xb[0] * 0.2          # the mask row would win position 0 by far
+    head = torch.from_numpy(hh).to(torch.bfloat16).to(DEV)
+    tokens, masked = synth.masked_block(d, M, DEV)
+    out = clover.lmhead_unmask(d, head, x, tokens, masked, block=M)
+    torch.cuda.synchronize()
+    assert int(out["argmax"][0]) != d.mask_id
+    ref = _head_ref(d, head, xh, None)
+    compare_head({k: v.cpu().numpy() for k, v in out.items()}, ref)
+
+
+def test_tiny_denoise_four_steps():
+    """Tiny configuration: 4 denoising steps with the 0.95 rule, against the
+    oracle's loop, step by step."""
+    d = synth.TINY
+    n = 8
+    layer = synth.make_layer(d, 0, 0, DEV)
+    embed = synth.make_embed(d, 0, DEV)
+    head = synth.make_head(d, 0, DEV)
+    ctx = synth.make_ctx(d, n, 0, DEV)
+    model = clover.Model(d, [layer], embed, head)
+    ref_model = {"dims": {"top_k": d.top_k, "rms_eps": d.rms_eps, "mask_id": d.mask_id},
+                 "layers": [layer_to_oracle(layer)], "embed": bits(embed), "head": bits(head),
+                 "ctx": ctx.cpu().numpy()}
+    # logit scales so that a few slots clear the threshold at step 1
+    t0, m0 = synth.masked_block(d, n)
+    x1 = O.embed(t0.numpy(), ref_model["embed"], ref_model["ctx"])
+    x1 = O.moe_layer(x1, ref_model["layers"][0], d.top_k, d.rms_eps)["x_out"]
+    alpha = calibrate_alpha(O.head_logits(x1, ref_model["head"], d.rms_eps), d.mask_id,
+                            synth.confidence_targets(n, 1).numpy(), O)
+    tokens, masked = synth.masked_block(d, n, DEV)
+    a = torch.from_numpy(alpha).to(DEV)
+    rt, rm = t0.numpy(), m0.numpy()
+    ws = clover.workspace(clover.denoise_workspace_bytes(d, n))
+    for step in range(4):
+        ref = O.denoise_step(rt, rm, ref_model, 0.95, d.block, alpha)
+        clover.denoise_step(model, ctx, tokens, masked, logit_scale=a, block=d.block, ws=ws)
+        torch.cuda.synchronize()
+        assert decisions_clear(ref["max_prob"], rm, 0.95, d.block), step
+        rt, rm = ref["tokens"], ref["masked"]
+        assert np.array_equal(tokens.cpu().numpy(), rt), step
+        assert np.array_equal(masked.cpu().numpy(), rm), step
+    clover.workspace_status(ws)
+
+
+def test_denoise_block_runs_to_completion_and_reports():
+    d = synth.TINY
+    n = 16
+    layer = synth.make_layer(d, 3, 0, DEV)
+    model = clover.Model(d, [layer], synth.make_embed(d, 3, DEV), synth.make_head(d, 3, DEV))
+    ctx = synth.make_ctx(d, n, 3, DEV)
+    tokens, masked = synth.masked_block(d, n, DEV)
+    steps = clover.denoise_block(model, ctx, tokens, masked, block=d.block, max_steps=n)
+    torch.cuda.synchronize()
+    assert 1 <= steps <= d.block
+    assert int(masked.sum()) == 0
+    assert not bool((tokens == d.mask_id).any())
+    # too few steps -> not converged, with the steps taken reported
+    tokens, masked = synth.masked_block(d, n, DEV)
+    with pytest.raises(clover.CloverError) as ei:
+        clover.denoise_block(model, ctx, tokens, masked, block=d.block, max_steps=2)
+    assert ei.value.code == clover.ERR_NOT_CONVERGED
+    assert int(masked.sum()) == n - 4            # one commit per step per block of 8
+    # nothing masked -> zero steps
+    steps = clover.denoise_block(model, ctx, tokens, torch.zeros_like(masked), block=d.block, max_steps=4)
+    assert steps == 0
+
+
+def test_bad_token_id_is_clamped_and_reported():
+    d = synth.TINY
+    n = 8
+    layer = synth.make_layer(d, 4, 0, DEV)
+    model = clover.Model(d, [layer], synth.make_embed(d, 4, DEV), synth.make_head(d, 4, DEV))
+    ctx = synth.make_ctx(d, n, 4, DEV)
+    tokens, masked = synth.masked_block(d, n, DEV)
+    tokens[2] = d.vocab + 5
+    masked[2] = 0
+    ws = clover.denoise_step(model, ctx, tokens, masked, block=d.block)
+    with pytest.raises(clover.CloverError) as ei:
+        clover.workspace_status(ws)
+    assert ei.value.code == clover.ERR_DEVICE_TIMEOUT and "token id" in str(ei.value)
+    clover.workspace_status(ws)    # the status word was cleared
