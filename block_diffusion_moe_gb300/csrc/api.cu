@@ -119,8 +119,8 @@ int check_dims(const clover_dims* d) {
   if (d->hidden <= 0 || d->n_experts <= 0 || d->top_k <= 0 || d->d_ff <= 0 || d->vocab <= 0)
     return fail(CLOVER_ERR_INVALID_ARG, "dims must be positive");
   if (!(d->rms_eps >= 0.f) || d->rms_eps > 1.f) return fail(CLOVER_ERR_INVALID_ARG, "rms_eps out of range");
-  if (d->hidden % 128 != 0 || d->hidden > 16384)
-    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "hidden=%d: must be a multiple of 128, at most 16384", d->hidden);
+  if (d->hidden % 128 != 0 || d->hidden > 8192)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "hidden=%d: must be a multiple of 128, at most 8192", d->hidden);
   if (d->d_ff % 64 != 0 || d->d_ff > 16384)
     return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "d_ff=%d: must be a multiple of 64, at most 16384", d->d_ff);
   if (d->n_experts > kMaxExperts) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "n_experts=%d > %d", d->n_experts, kMaxExperts);

@@ -28,7 +28,7 @@
  *     records a flag in the workspace and the kernel returns;
  *     clover_workspace_status() reports it as CLOVER_ERR_DEVICE_TIMEOUT.
  *   - Shapes: hidden % 128 == 0, d_ff % 64 == 0, 1 <= top_k <= 32,
- *     top_k <= n_experts <= 256, 1 <= tokens <= 256, vocab >= 2,
+ *     top_k <= n_experts <= 256, hidden <= 8192, 1 <= tokens <= 256, vocab >= 2,
  *     0 <= mask_id < vocab. Other shapes return CLOVER_ERR_UNSUPPORTED_SHAPE;
  *     there is no fallback path.
  */
