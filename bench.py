@@ -269,6 +269,9 @@ def run_ours(args):
     n_exp = args.steps * D.n_layers
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_exp)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_exp)]
+    for e in ev_b + ev_e:          # torch creates the CUDA event on first record
+        e.record(stream)
+    torch.cuda.synchronize()
     arr_b = (clover.ctypes.c_void_p * n_exp)(*[e.cuda_event for e in ev_b])
     arr_e = (clover.ctypes.c_void_p * n_exp)(*[e.cuda_event for e in ev_e])
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
