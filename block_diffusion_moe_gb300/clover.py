@@ -53,6 +53,11 @@ EXPORTS = {
                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                             ctypes.c_size_t, ctypes.c_void_p]),
+    "clover_lmhead_unmask_static": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_float, ctypes.c_int32, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_int32, ctypes.c_void_p]),
     "clover_denoise_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),
     "clover_denoise_step": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.POINTER(MoeLayer), ctypes.c_int32,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,

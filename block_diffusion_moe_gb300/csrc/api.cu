@@ -455,6 +455,12 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
 
 }  // namespace
 
+namespace clover {
+// Lets other translation units of the library report through
+// clover_last_error().
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace clover
+
 extern "C" {
 
 size_t clover_moe_workspace_bytes(const clover_dims* dims, int32_t max_tokens) {

@@ -171,6 +171,26 @@ int32_t clover_profile_expert_events(clover_event_t* begin, clover_event_t* end,
  * bytes, NUL-terminated). Returns its full length. */
 int32_t clover_last_error(char* buf, size_t n);
 
+/* Same operation and arguments as clover_lmhead_unmask, without the
+ * workspace. (The pages have no counterpart: this is a library convenience.)
+ * For callers that cannot allocate device memory -- a plug-in inside an
+ * application that owns all GPU memory, code running during CUDA graph
+ * capture, a latency-critical loop that must not synchronise on an
+ * allocation. The scratch lives in a 1 MiB array inside the library that
+ * every GPU loading the library keeps until the process exits; it fits up to
+ * 102 positions at hidden 2048 (the rule: clover_head_workspace_bytes(dims, M)
+ * <= 1 MiB). Larger sizes return CLOVER_ERR_WORKSPACE_TOO_SMALL and nothing
+ * runs. The first call on each device looks up the array's device address;
+ * make that first call before any stream capture. The call allocates nothing
+ * and clears the array's control words itself. All calls share the one
+ * array: calls that may overlap on the GPU (other streams, other threads)
+ * race and must be serialised by the caller. */
+int clover_lmhead_unmask_static(const clover_dims* dims, const uint16_t* head_w, const float* x,
+                                const float* logit_scale, float threshold, int32_t block,
+                                int32_t* tokens, uint8_t* masked,
+                                int32_t* argmax, float* max_logit, float* lse, float* max_prob,
+                                int32_t* n_committed, int32_t M, clover_stream_t stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t clover_version(void);
 
