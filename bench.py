@@ -197,11 +197,12 @@ def cpu_baseline(layers=None, n_layers: int = 8, head_rows: int = 8192, seed: in
     z = O.head_logits(x, synth.bf16_bits(head), D.rms_eps)
     O.head_stats(z, 0)
     th = time.perf_counter() - a
-    per_step = tl / len(layers) * D.n_layers + th * (D.vocab / head_rows)
+    per_layer = tl / len(layers)
+    head_full = th * (D.vocab / head_rows)
     desc = (f"oracle (numpy float64, BLAS threads = host cores) on {len(layers)} MoE layers of the 32-position "
             f"block ({tl:.1f} s) and {head_rows} of {D.vocab} head rows ({th:.1f} s), scaled to 40 layers + "
             f"full head")
-    return per_step, desc, os.cpu_count()
+    return per_layer, head_full, desc, os.cpu_count()
 
 
 # ------------------------------------------------------------------- arms
@@ -216,9 +217,9 @@ def run_reference(args):
     cores = os.cpu_count()
     ref_layers = [synth.make_layer(D, 0, 0, "cpu")]
     for i in range(args.warmup + args.steps):
-        s, desc, cores = cpu_baseline(layers=ref_layers, n_layers=1, head_rows=4096, seed=i)
+        pl, hf, desc, cores = cpu_baseline(layers=ref_layers, n_layers=1, head_rows=4096, seed=i)
         if i >= args.warmup:
-            per.append(s)
+            per.append(pl * D.n_layers + hf)
     sec = float(np.mean(per))
     value = M / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
@@ -230,6 +231,16 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+WORKLOADS = {
+    "step": WORKLOAD,
+    "layer": "one Clover-shaped MoE layer (256 experts top-8 + shared, hidden 2,048, SwiGLU 512) on a "
+             "32-position block, uniform routing",
+    "head": "LM head + low-confidence unmask: 32 positions x hidden 2,048 into the untied 248,320-row head",
+    "zipf": "batched and skewed routing: 8 blocks x 32 positions (256 tokens) through 40 Clover-shaped MoE "
+            "layers + head, router biased to Zipf(1.2) expert popularity",
+}
+
+
 def run_ours(args):
     from block_diffusion_moe_gb300 import clover
 
@@ -238,12 +249,25 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     clover.lib()
     seed = 1000 + rank
-    layers = [synth.make_layer(D, seed, l, dev) for l in range(D.n_layers)]
-    model = clover.Model(D, layers, synth.make_embed(D, seed, dev), synth.make_head(D, seed, dev))
-    ctx = synth.make_ctx(D, M, seed, dev)
-    tokens, masked = synth.masked_block(D, M, dev)
-    ws = clover.workspace(clover.denoise_workspace_bytes(D, M), dev)
+    kind = args.workload
+    n_pos = 256 if kind == "zipf" else M
+    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "layer": 1, "head": 0}[kind]
+    zipf = 1.2 if kind == "zipf" else None
+    layers = [synth.make_layer(D, seed, l, dev, zipf_s=zipf) for l in range(n_layers)]
+    head_w = synth.make_head(D, seed, dev) if kind != "layer" else None
+    embed = synth.make_embed(D, seed, dev) if kind in ("step", "zipf") else None
+    model = clover.Model(D, layers, embed, head_w) if kind in ("step", "zipf") else None
+    ctx = synth.make_ctx(D, n_pos, seed, dev)
+    tokens, masked = synth.masked_block(D, n_pos, dev)
     stream = torch.cuda.current_stream(dev)
+    x_fixed = synth.make_x(D, n_pos, seed, dev)
+    x_out = torch.empty_like(x_fixed)
+    if kind in ("step", "zipf"):
+        ws = clover.workspace(clover.denoise_workspace_bytes(D, n_pos), dev)
+    elif kind == "layer":
+        ws = clover.workspace(clover.moe_workspace_bytes(D, n_pos), dev)
+    else:
+        ws = clover.workspace(clover.head_workspace_bytes(D, n_pos), dev)
 
     def reset():
         tokens.fill_(D.mask_id)
@@ -252,11 +276,16 @@ def run_ours(args):
     steps_in_block = [0]
 
     def step():
-        if steps_in_block[0] == M:
-            reset()
-            steps_in_block[0] = 0
-        clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
-        steps_in_block[0] += 1
+        if kind in ("step", "zipf"):
+            if steps_in_block[0] == M:
+                reset()
+                steps_in_block[0] = 0
+            clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
+            steps_in_block[0] += 1
+        elif kind == "layer":
+            clover.moe_block_step(D, layers[0], x_fixed, x_out=x_out, ws=ws, with_topk=False)
+        else:
+            clover.lmhead_unmask(D, head_w, x_fixed, tokens, masked, block=M, ws=ws)
 
     for _ in range(args.warmup):
         step()
@@ -265,116 +294,142 @@ def run_ours(args):
     torch.cuda.synchronize()
     clover.workspace_status(ws)
 
-    # ---- timed region: device time of K steps, expert-kernel events inside
-    n_exp = args.steps * D.n_layers
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_exp)]
-    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_exp)]
+    # ---- timed region: device time of K steps; per-launch events around the
+    # dominant kernel (the expert kernel, or the whole head call)
+    per_step_launches = n_layers if kind != "head" else 1
+    n_ev = args.steps * per_step_launches
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     for e in ev_b + ev_e:          # torch creates the CUDA event on first record
         e.record(stream)
     torch.cuda.synchronize()
-    arr_b = (clover.ctypes.c_void_p * n_exp)(*[e.cuda_event for e in ev_b])
-    arr_e = (clover.ctypes.c_void_p * n_exp)(*[e.cuda_event for e in ev_e])
+    arr_b = (clover.ctypes.c_void_p * n_ev)(*[e.cuda_event for e in ev_b])
+    arr_e = (clover.ctypes.c_void_p * n_ev)(*[e.cuda_event for e in ev_e])
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     _barrier(dist)
     with Clocks(local) as clk:
-        clover.lib().clover_profile_expert_events(arr_b, arr_e, n_exp)
+        if kind != "head":
+            clover.lib().clover_profile_expert_events(arr_b, arr_e, n_ev)
         start.record(stream)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            if kind == "head":
+                ev_b[i].record(stream)
             step()
+            if kind == "head":
+                ev_e[i].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
-        recorded = clover.lib().clover_profile_expert_events(None, None, 0)
+        recorded = clover.lib().clover_profile_expert_events(None, None, 0) if kind != "head" else n_ev
     _barrier(dist)
     clover.workspace_status(ws)
     ms = start.elapsed_time(end)
     ms = _max_over_ranks(ms, dist)
-    assert recorded == n_exp, (recorded, n_exp)
+    assert recorded == n_ev, (recorded, n_ev)
     durs = [b.elapsed_time(e) for b, e in zip(ev_b, ev_e)]
 
-    # ---- algorithmic bytes per expert launch: replay the same steps layer by
-    # layer (the kernels are deterministic) and count the experts touched.
-    reset()
-    u_per_launch = []
-    t_r, m_r = tokens, masked
-    x = torch.empty((M, D.hidden), dtype=torch.float32, device=dev)
-    moe_ws = clover.workspace(clover.moe_workspace_bytes(D, M), dev)
-    head_ws = clover.workspace(clover.head_workspace_bytes(D, M), dev)
-    for s in range(args.steps):
-        if s > 0 and s % M == 0:
-            reset()
-        x.copy_(model.embed[t_r.long()].float() + ctx)
-        for L in layers:
-            x, idx, _ = clover.moe_block_step(D, L, x, x_out=x, ws=moe_ws)
-            u_per_launch.append(int(torch.unique(idx).numel()))
-        clover.lmhead_unmask(D, model.head_w, x, t_r, m_r, block=M, ws=head_ws)
-    torch.cuda.synchronize()
+    # ---- algorithmic bytes: replay the same steps layer by layer (the kernels
+    # are deterministic) and count the experts each launch touched.
     ebytes = D.expert_bytes
-    alg = [(u + 1) * ebytes for u in u_per_launch]
+    u_per_launch = []
+    if kind == "head":
+        alg = [D.head_bytes] * n_ev
+    else:
+        reset()
+        x = torch.empty((n_pos, D.hidden), dtype=torch.float32, device=dev)
+        moe_ws = clover.workspace(clover.moe_workspace_bytes(D, n_pos), dev)
+        head_ws = clover.workspace(clover.head_workspace_bytes(D, n_pos), dev)
+        for s_ in range(args.steps):
+            if kind == "layer":
+                _, idx, _ = clover.moe_block_step(D, layers[0], x_fixed, x_out=x, ws=moe_ws)
+                u_per_launch.append(int(torch.unique(idx).numel()))
+                continue
+            if s_ > 0 and s_ % M == 0:
+                reset()
+            x.copy_(model.embed[tokens.long()].float() + ctx)
+            for L in layers:
+                x, idx, _ = clover.moe_block_step(D, L, x, x_out=x, ws=moe_ws)
+                u_per_launch.append(int(torch.unique(idx).numel()))
+            clover.lmhead_unmask(D, head_w, x, tokens, masked, block=M, ws=head_ws)
+        torch.cuda.synchronize()
+        alg = [(u + 1) * ebytes for u in u_per_launch]
     achieved = sum(alg) / (sum(durs) * 1e-3) / 1e9          # GB/s
     peak, peak_kind = _peaks()
-    u_mean = float(np.mean(u_per_launch))
-    step_bytes = sum(alg) / args.steps + D.n_layers * D.router_bytes + D.head_bytes
-    # share of the step spent in the expert kernel
-    expert_share = sum(durs) / ms
+    u_mean = float(np.mean(u_per_launch)) if u_per_launch else None
+    step_bytes = sum(alg) / args.steps + n_layers * D.router_bytes + (D.head_bytes if kind != "layer" else 0)
+    share = sum(durs) / ms
 
     # ---- end to end through the C ABI with host buffers
-    h_tokens = torch.empty(M, dtype=torch.int32).pin_memory()
-    h_masked = torch.empty(M, dtype=torch.uint8).pin_memory()
-    h_ctx = ctx.cpu().pin_memory()
-    o_tokens = torch.empty(M, dtype=torch.int32).pin_memory()
-    o_masked = torch.empty(M, dtype=torch.uint8).pin_memory()
+    h_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
+    h_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
+    h_in = (x_fixed if kind in ("layer", "head") else ctx).cpu().pin_memory()
+    d_in = x_fixed if kind in ("layer", "head") else ctx
+    o_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
+    o_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
+    o_x = torch.empty((n_pos, D.hidden), dtype=torch.float32).pin_memory()
     h_tokens.fill_(D.mask_id)
     h_masked.fill_(1)
-    e2e_steps = args.steps
+    steps_in_block[0] = 0
     _barrier(dist)
     t0 = time.perf_counter()
-    for s in range(e2e_steps):
-        if s > 0 and s % M == 0:
+    for s_ in range(args.steps):
+        if kind in ("step", "zipf") and s_ > 0 and s_ % M == 0:
             h_tokens.fill_(D.mask_id)
             h_masked.fill_(1)
-        tokens.copy_(h_tokens, non_blocking=True)
-        masked.copy_(h_masked, non_blocking=True)
-        ctx.copy_(h_ctx, non_blocking=True)
-        clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
-        o_tokens.copy_(tokens, non_blocking=True)
-        o_masked.copy_(masked, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        if kind != "layer":
+            tokens.copy_(h_tokens, non_blocking=True)
+            masked.copy_(h_masked, non_blocking=True)
+        if kind in ("step", "zipf"):
+            clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
+        else:
+            step()
+        if kind == "layer":
+            o_x.copy_(x_out, non_blocking=True)
+        else:
+            o_tokens.copy_(tokens, non_blocking=True)
+            o_masked.copy_(masked, non_blocking=True)
         torch.cuda.synchronize()
-        h_tokens.copy_(o_tokens)
-        h_masked.copy_(o_masked)
+        if kind in ("step", "zipf"):
+            h_tokens.copy_(o_tokens)
+            h_masked.copy_(o_masked)
     e2e_s = time.perf_counter() - t0
     e2e_s = _max_over_ranks(e2e_s, dist)
-    h2d = M * 4 + M + M * D.hidden * 4
-    d2h = M * 4 + M
+    if kind == "layer":
+        h2d, d2h = n_pos * D.hidden * 4, n_pos * D.hidden * 4
+    else:
+        h2d = n_pos * 4 + n_pos + n_pos * D.hidden * 4
+        d2h = n_pos * 4 + n_pos
 
-    value = _sum_over_ranks(M * args.steps, dist) / (ms * 1e-3)
-    e2e_value = _sum_over_ranks(M * e2e_steps, dist) / e2e_s
+    value = _sum_over_ranks(n_pos * args.steps, dist) / (ms * 1e-3)
+    e2e_value = _sum_over_ranks(n_pos * args.steps, dist) / e2e_s
     if rank != 0:
         return
     csum = clk.summary()
-    traffic = _expert_traffic()
+    launches_per_step = {"step": 1 + 3 * n_layers + 2, "zipf": 1 + 3 * n_layers + 2, "layer": 3, "head": 2}[kind]
+    roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
+                   else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded random-init bf16 weights of the Clover shapes)",
-        "config": {"workload": WORKLOAD, "global_batch": M * ws_n, "seq_len": M,
+        "config": {"workload": WORKLOADS[kind], "global_batch": n_pos * ws_n, "seq_len": M,
                    "parallelism": "replicas" if ws_n > 1 else "single",
-                   "l2": "inputs larger than L2 (each step streams ~42 GB of weights)",
+                   "l2": "inputs larger than L2 (every step streams >= 1 GB of weights)",
                    "mean_unique_experts_per_layer": u_mean,
                    "algorithmic_bytes_per_step": step_bytes,
                    "step_hbm_gbs": step_bytes / (ms / args.steps * 1e-3) / 1e9,
                    "step_roofline_frac": step_bytes / (ms / args.steps * 1e-3) / 1e9 / peak},
-        "roofline": {"kernel": "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)",
-                     "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"kernel": roof_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": traffic, "launches": len(durs),
-                     "mean_launch_us": float(np.mean(durs)) * 1e3,
-                     "share_of_step": expert_share},
+                     "traffic": _expert_traffic() if kind != "head" else None, "launches": len(durs),
+                     "mean_launch_us": float(np.mean(durs)) * 1e3, "share_of_step": share},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (1 + 3 * D.n_layers + 2),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": csum,
     }
-    if not args.no_cpu_baseline:
-        sec, desc, cores = cpu_baseline(layers=layers)
+    if not args.no_cpu_baseline and kind in ("step", "layer"):
+        pl, hf, desc, cores = cpu_baseline(layers=layers)
+        sec = pl * D.n_layers + hf if kind == "step" else pl
         line["cpu_baseline"] = {"value": M / sec, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
     print(json.dumps(line), flush=True)
 
@@ -386,6 +441,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="step", choices=sorted(WORKLOADS),
+                    help="step (default, the headline): full 40-layer block step; layer / head / zipf: the other "
+                         "configurations")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
