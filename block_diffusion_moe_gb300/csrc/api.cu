@@ -30,6 +30,10 @@ int cuda_fail(cudaError_t e, const char* where) {
   return fail(CLOVER_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+// Every kernel waits for its predecessor's results with griddepcontrol.wait,
+// so all launches may use programmatic dependent launch.
+constexpr bool kPdl = true;
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -44,7 +48,7 @@ enum CtrlWord : int {
   kCtrlMaskedLeft = 2,   // positions still masked after the last head call
   kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
   kCtrlCommitted = 4,    // positions committed by the last head call
-  kCtrlTokenGroups = 8,  // [8] routing arrival counters (reset by their last CTA)
+  kCtrlTokenGroups = 8,  // [32] routing arrival counters (reset by their last CTA)
 };
 
 struct MoeLayout {
@@ -253,7 +257,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   ra.E = E;
   ra.K = K;
   ra.eps = d.rms_eps;
-  cudaError_t e = launch_route(ra, stream, false);
+  cudaError_t e = launch_route(ra, stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch route");
 
   PermArgs pa;
@@ -274,7 +278,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   pa.H = H;
   pa.E = E;
   pa.K = K;
-  e = launch_perm(pa, std::max(1, std::min(MK, plan.sms)), stream, false);
+  e = launch_perm(pa, std::max(1, std::min(MK, plan.sms)), stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch perm");
 
   ExpertArgs xa;
@@ -323,7 +327,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   if (g_prof.begin && g_prof.cap > 0) {
     if ((rc = record(g_prof.begin[g_prof.count % g_prof.cap], stream))) return rc;
   }
-  e = launch_expert(xa, plan.sms, smem, stream, false);
+  e = launch_expert(xa, plan.sms, smem, stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch expert");
   if (g_prof.end && g_prof.cap > 0) {
     if ((rc = record(g_prof.end[g_prof.count % g_prof.cap], stream))) return rc;
@@ -344,7 +348,7 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
   na.M = M;
   na.H = d.hidden;
   na.eps = d.rms_eps;
-  cudaError_t e = launch_rmsnorm(na, stream, false);
+  cudaError_t e = launch_rmsnorm(na, stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch rmsnorm");
 
   HeadArgs ha;
@@ -378,7 +382,7 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
   ha.stages = static_cast<int>(std::min<size_t>(
       12, (static_cast<size_t>(kSmemBudget) - fixed) / (kATileBytes + static_cast<size_t>(nb) * 128)));
   const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
-  e = launch_head(ha, grid, head_smem_bytes(ha.stages, nb), stream, false);
+  e = launch_head(ha, grid, head_smem_bytes(ha.stages, nb), stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch head");
   return CLOVER_OK;
 }
@@ -434,7 +438,7 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
   ea.M = M;
   ea.H = dims->hidden;
   ea.V = dims->vocab;
-  cudaError_t e = launch_embed(ea, s, false);
+  cudaError_t e = launch_embed(ea, s, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch embed");
   for (int l = 0; l < n_layers; ++l) {
     rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,

@@ -491,6 +491,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_const
   const uint32_t tmem_base = *s.tmem_slot;
 
   pdl_wait();
+  pdl_trigger();
   const int n_exp = *p.n_active + 1;
   const int n_total = n_exp * ((p.F >> 6) + (p.H >> 7));
 
@@ -511,7 +512,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_const
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
-  pdl_trigger();
 }
 
 size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {

@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
   pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) head_producer(p, s, nb);
@@ -359,7 +360,6 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
-  pdl_trigger();
 }
 
 size_t head_smem_bytes(int stages, int nb) {

@@ -11,9 +11,9 @@ namespace clover {
 
 using bf16 = __nv_bfloat16;
 
-// Routing kernel tiling: 8 experts x 32 tokens per CTA.
+// Routing kernel tiling: 8 experts x 8 tokens (one per warp) per CTA.
 constexpr int kRouteExperts = 8;
-constexpr int kRouteTokens = 32;
+constexpr int kRouteTokens = 8;
 constexpr int kMaxTokens = 256;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
@@ -50,7 +50,7 @@ struct RouteArgs {
   const float* bias;    // [E] or null
   float* logits;        // [M][E]
   bf16* xn_rows;        // [M][H] normed input (the shared expert's rows of the gathered buffer)
-  int* tg_ctr;          // [ceil(M/32)] arrival counters, zero between launches
+  int* tg_ctr;          // [ceil(M/8)] arrival counters, zero between launches
   int32_t* topk_idx;    // [M][K]
   float* topk_w;        // [M][K]
   int M, H, E, K;

@@ -18,6 +18,7 @@ namespace clover {
 // x_p = E[t_p] + c_p. One CTA per position.
 __global__ void __launch_bounds__(256) k_embed(EmbedArgs a) {
   pdl_wait();
+  pdl_trigger();
   const int p = blockIdx.x;
   int t = a.tokens[p];
   if (t < 0 || t >= a.V) {
@@ -39,12 +40,13 @@ __global__ void __launch_bounds__(256) k_embed(EmbedArgs a) {
     o.w = __high2float(e23) + cv.w;
     *reinterpret_cast<float4*>(xr + c) = o;
   }
-  pdl_trigger();
 }
 
 // Reciprocal RMS of one row, computed by one warp: 1 / sqrt(mean(x^2) + eps).
+// Loads are unrolled so that several are in flight per lane.
 __device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int lane) {
   float ss = 0.f;
+#pragma unroll 8
   for (int c = lane * 4; c < H; c += 128) {
     const float4 v = *reinterpret_cast<const float4*>(xr + c);
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
@@ -57,6 +59,7 @@ __device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int
 // xn = bf16(x * rstd). One warp per row.
 __global__ void __launch_bounds__(256) k_rmsnorm(NormArgs a) {
   pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t < a.M) {
@@ -73,11 +76,10 @@ __global__ void __launch_bounds__(256) k_rmsnorm(NormArgs a) {
       *reinterpret_cast<uint2*>(out + c) = pk;
     }
   }
-  pdl_trigger();
 }
 
 // ------------------------------------------------------------------ route
-// Grid (ceil(E/8), ceil(M/32)). Each CTA normalises its 32 tokens (one warp
+// Grid (ceil(E/8), ceil(M/8)). Each CTA normalises its 8 tokens (one warp
 // per token), writes the bf16 normed rows (expert group 0 only) and the
 // router logits of its 8 experts. The last CTA to finish a token group then
 // takes softmax top-k for those tokens: selection by descending logit with
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
   const int e0 = blockIdx.x * kRouteExperts;
   const int ne = min(kRouteExperts, a.E - e0);
   const int t0 = blockIdx.y * kRouteTokens;
-  const int t1 = min(a.M, t0 + kRouteTokens);
+  const int t1 = min(a.M, t0 + kRouteTokens);  // one token per warp
   const int H = a.H;
 
   // Router rows do not depend on earlier kernels: stage them before waiting.
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     for (int i = tid; i < n16; i += blockDim.x) dst[i] = src[i];
   }
   pdl_wait();
+  pdl_trigger();
   __syncthreads();
 
   for (int t = t0 + warp; t < t1; t += 8) {
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     float acc[kRouteExperts];
 #pragma unroll
     for (int e = 0; e < kRouteExperts; ++e) acc[e] = 0.f;
+#pragma unroll 4
     for (int c = lane * 4; c < H; c += 128) {
       const float4 v = *reinterpret_cast<const float4*>(xr + c);
       __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * rstd, v.y * rstd);
@@ -153,10 +157,7 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     s_last = (old == static_cast<int>(gridDim.x) - 1);
   }
   __syncthreads();
-  if (!s_last) {
-    pdl_trigger();
-    return;
-  }
+  if (!s_last) return;
   __threadfence();
 
   // Top-k for this token group (one warp per token; lane l holds experts
@@ -209,7 +210,6 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
     }
   }
   if (tid == 0) a.tg_ctr[blockIdx.y] = 0;
-  pdl_trigger();
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x == 256).
@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
   const int nw = (a.M + 31) >> 5;
 
   pdl_wait();
+  pdl_trigger();
   for (int i = tid; i < MK; i += blockDim.x) {
     const int e = a.topk_idx[i];
     s_idx[i] = e < 0 ? 0 : (e >= a.E ? a.E - 1 : e);  // ids come from k_route; clamp keeps smem indexing safe
@@ -314,7 +315,6 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
     uint4* dst = reinterpret_cast<uint4*>(a.xg + static_cast<size_t>(r) * H);
     for (int i = tid; i < static_cast<int>(H / 8); i += blockDim.x) dst[i] = src[i];
   }
-  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- launches
