@@ -379,9 +379,14 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
   ha.threshold = threshold;
   const int nb = (M + 15) & ~15;
   const size_t fixed = head_smem_bytes(0, nb) + 16 * 2 * 8;
+  // 8 stages (128 KB of weights in flight per SM) streamed best on GB300.
   ha.stages = static_cast<int>(std::min<size_t>(
-      12, (static_cast<size_t>(kSmemBudget) - fixed) / (kATileBytes + static_cast<size_t>(nb) * 128)));
+      8, (static_cast<size_t>(kSmemBudget) - fixed) / (kATileBytes + static_cast<size_t>(nb) * 128)));
   const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
+  // The final merge reuses the ring for 12 bytes x 32 positions x grid.
+  if (static_cast<size_t>(ha.stages) * (kATileBytes + static_cast<size_t>(nb) * 128) <
+      static_cast<size_t>(grid) * 32 * 12)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
   e = launch_head(ha, grid, head_smem_bytes(ha.stages, nb), stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch head");
   return CLOVER_OK;

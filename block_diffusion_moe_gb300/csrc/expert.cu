@@ -162,8 +162,14 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, int n_exp, int n_
       row = (w.a == 0 ? 0 : w.e * p.H) + w.slice * 128;
       nk = p.F >> 6;
     }
+    // Start each unit's K walk at an offset fixed by (expert, slice), so that
+    // concurrent units request different offsets within the weight rows; the
+    // offset does not depend on scheduling, so results stay reproducible.
+    const int rot = static_cast<int>((static_cast<unsigned>(w.e) * 5u + static_cast<unsigned>(w.slice) * 3u) %
+                                     static_cast<unsigned>(nk));
     bool ok = true;
-    for (int kc = 0; kc < nk; ++kc) {
+    for (int kc0 = 0; kc0 < nk; ++kc0) {
+      const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
       if (!mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
         ok = false;
@@ -233,8 +239,11 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, int n_exp) {
       if (!ok) break;
       fence_proxy_async_global();
     }
+    const int rot = static_cast<int>((static_cast<unsigned>(w.e) * 5u + static_cast<unsigned>(w.slice) * 3u) %
+                                     static_cast<unsigned>(nk));
     bool ok = true;
-    for (int kc = 0; kc < nk; ++kc) {
+    for (int kc0 = 0; kc0 < nk; ++kc0) {
+      const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
       if (!mbar_wait(&s.empty_b[sb], phb ^ 1u, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
         ok = false;
@@ -322,23 +331,40 @@ __device__ void combine_slice(const ExpertArgs& p, int j, int etid) {
   const size_t H = p.H;
   const size_t col = static_cast<size_t>(j) * 128 + c4;
   const int MK = p.M * p.K;
+  const int K = p.K;
   for (int t = g; t < p.M; t += 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < p.K; ++k) {
-      const int r = p.tok_slot[t * p.K + k];
-      const float wk = p.topk_w[t * p.K + k];
-      const float4 y = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(r) * H + col));
-      acc.x = fmaf(wk, y.x, acc.x);
-      acc.y = fmaf(wk, y.y, acc.y);
-      acc.z = fmaf(wk, y.z, acc.z);
-      acc.w = fmaf(wk, y.w, acc.w);
-    }
     const float4 ys = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t) * H + col));
+    const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * H + col);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // Selections in groups of 8: every load of a group is issued before any
+    // is used (the sum still runs in selection order).
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      int r[8];
+      float wk[8];
+      float4 y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool v = k0 + i < K;
+        r[i] = v ? p.tok_slot[t * K + k0 + i] : MK + t;
+        wk[i] = v ? p.topk_w[t * K + k0 + i] : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        y[i] = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(r[i]) * H + col));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (k0 + i < K) {
+          acc.x = fmaf(wk[i], y[i].x, acc.x);
+          acc.y = fmaf(wk[i], y[i].y, acc.y);
+          acc.z = fmaf(wk[i], y[i].z, acc.z);
+          acc.w = fmaf(wk[i], y[i].w, acc.w);
+        }
+      }
+    }
     acc.x += ys.x;
     acc.y += ys.y;
     acc.z += ys.z;
     acc.w += ys.w;
-    const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * H + col);
     float4 o;
     o.x = xi.x + acc.x;
     o.y = xi.y + acc.y;

@@ -35,6 +35,7 @@ struct HeadSmem {
   float* run_s;   // [nb]
   int* run_a;     // [nb]
   float* alpha;   // [nb]
+  float* tr;      // [4][32][33] per-warp transpose tiles
   uint64_t *full, *empty, *tfull, *tempty, *drain;
   uint32_t* tmem_slot;
   volatile uint32_t* abort;
@@ -58,7 +59,8 @@ __device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int n
   s.run_s = s.run_m + nb;
   s.run_a = reinterpret_cast<int*>(s.run_s + nb);
   s.alpha = reinterpret_cast<float*>(s.run_a + nb);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.alpha + nb);  // nb % 16 == 0 keeps 8-byte alignment
+  s.tr = s.alpha + nb;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.tr + 4 * 32 * 33);  // nb % 16 == 0 keeps 8-byte alignment
   s.full = bars;
   s.empty = s.full + p.stages;
   s.tfull = s.empty + p.stages;
@@ -91,11 +93,17 @@ __device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
   const uint64_t pol_w = l2_policy_evict_first();
   const uint64_t pol_x = l2_policy_evict_last();
   const int nk = p.H >> 6;
+  // Each CTA walks the K chunks from its own starting point, so that the
+  // CTAs' simultaneous requests do not all share the same offset within the
+  // head rows (which would concentrate them on few DRAM channels). The MMA
+  // consumes stages in issue order; only the accumulation order changes.
+  const int rot = static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(nk));
   int st = 0;
   uint32_t ph = 0, issued = 0, parity_bits = 0;
   bool ok = true;
   for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
-    for (int kc = 0; kc < nk; ++kc) {
+    for (int kc0 = 0; kc0 < nk; ++kc0) {
+      const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
       if (!mbar_wait(&s.empty[st], ph ^ 1u, s.abort)) {
         atomicOr(p.err, kErrMbarTimeout);
         *s.abort = 1u;
@@ -164,73 +172,116 @@ __device__ void head_mma(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t 
   mbar_wait_for(s.drain, 0, 200000000ull);
 }
 
+// Per tile, each epilogue warp owns 32 vocabulary rows (its TMEM lane
+// quarter) of the 128 x nb accumulator. It moves them 32 token columns at a
+// time through a padded shared-memory tile so that lane j then walks column j
+// serially: tile max, first row reaching it, and the sum of exp(z - max).
+// That folds into a running (max, sum, argmax) per column held in the lane's
+// registers across all of the CTA's tiles; warps never wait on each other
+// until the end.
 __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t tmem_base) {
+  constexpr int kMaxChunks = kMaxTokens / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int row = q * 32 + lane;
   const int etid = threadIdx.x - 64;  // 0..127
-  for (int n = etid; n < nb; n += 128) {
-    s.run_m[n] = -INFINITY;
-    s.run_s[n] = 0.f;
-    s.run_a[n] = 0x7fffffff;
-    s.alpha[n] = (n < p.M && p.alpha != nullptr) ? p.alpha[n] : 1.0f;
+  const int nch = (nb + 31) >> 5;
+  float* tr = s.tr + q * (32 * 33);
+  float rm[kMaxChunks], rs[kMaxChunks], al[kMaxChunks];
+  int ra[kMaxChunks];
+#pragma unroll
+  for (int ch = 0; ch < kMaxChunks; ++ch) {
+    const int c = ch * 32 + lane;
+    rm[ch] = -INFINITY;
+    rs[ch] = 0.f;
+    ra[ch] = 0x7fffffff;
+    al[ch] = (c < p.M && p.alpha != nullptr) ? p.alpha[c] : 1.0f;
   }
-  named_bar_sync(1, 128);
+  bool ok = true;
   int it = 0;
   for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++it) {
     const int acc = it & 1;
     const uint32_t apar = (it >> 1) & 1;
-    if (etid == 0) {
-      const bool ok = mbar_wait(&s.tfull[acc], apar, s.abort);
-      if (!ok) {
+    int good = 1;
+    if (lane == 0) {
+      good = mbar_wait(&s.tfull[acc], apar, s.abort) ? 1 : 0;
+      if (!good) {
         atomicOr(p.err, kErrMbarTimeout);
         *s.abort = 1u;
       }
-      *s.s_ok = ok ? 1 : 0;
     }
-    named_bar_sync(1, 128);
-    if (!*s.s_ok) break;
+    good = __shfl_sync(0xffffffffu, good, 0);
+    if (!good) {
+      ok = false;
+      break;
+    }
     tc_fence_after();
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * 256u;
     const int vid = tile * 128 + row;
     const bool valid_row = (vid < p.V) && (vid != p.mask_id);
-    for (int c0 = 0; c0 < nb; c0 += 16) {
-      float v[16];
-      __syncwarp();
-      tmem_ld16(tb + c0, v);
+    const int row0 = tile * 128 + q * 32;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int c = c0 + j;
-        const float z = valid_row ? v[j] * s.alpha[c] : -INFINITY;
-        const float m = warp_max_f(z);
-        const unsigned bal = __ballot_sync(0xffffffffu, z == m && m != -INFINITY);
-        const float e = (m == -INFINITY) ? 0.f : expf(z - m);
-        const float sum = warp_sum_f(e);
-        if (lane == 0) {
-          s.wp_m[q * nb + c] = m;
-          s.wp_s[q * nb + c] = sum;
-          s.wp_a[q * nb + c] = bal ? tile * 128 + q * 32 + (__ffs(bal) - 1) : 0x7fffffff;
+    for (int ch = 0; ch < kMaxChunks; ++ch) {
+      if (ch < nch) {
+        float v[16];
+        __syncwarp();
+        tmem_ld16(tb + ch * 32, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tr[lane * 33 + j] = valid_row ? v[j] : -INFINITY;
+        if (ch * 32 + 16 < nb) {
+          tmem_ld16(tb + ch * 32 + 16, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) tr[lane * 33 + 16 + j] = valid_row ? v[j] : -INFINITY;
+        }
+        __syncwarp();
+        if (ch * 32 + lane < nb) {
+          float z[32];
+          float m = -INFINITY;
+          int a = 0x7fffffff;
+#pragma unroll
+          for (int r = 0; r < 32; ++r) {
+            const float raw = tr[r * 33 + lane];
+            z[r] = (raw == -INFINITY) ? -INFINITY : raw * al[ch];
+            if (z[r] > m) {
+              m = z[r];
+              a = row0 + r;
+            }
+          }
+          float sum = 0.f;
+          if (m != -INFINITY) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) sum += expf(z[r] - m);
+          }
+          lse_merge(rm[ch], rs[ch], ra[ch], m, sum, a);
         }
       }
-      if (c0 + 16 >= nb) {
-        // all TMEM reads of this accumulator are done
-        tc_fence_before();
-      }
-      named_bar_sync(1, 128);
-      if (etid < 16) {
-        const int c = c0 + etid;
-        float m = s.run_m[c], sm = s.run_s[c];
-        int a = s.run_a[c];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) lse_merge(m, sm, a, s.wp_m[w * nb + c], s.wp_s[w * nb + c], s.wp_a[w * nb + c]);
-        s.run_m[c] = m;
-        s.run_s[c] = sm;
-        s.run_a[c] = a;
-      }
-      named_bar_sync(1, 128);
     }
-    if (etid == 0) mbar_arrive(&s.tempty[acc]);
+    // this warp is done reading the accumulator
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.tempty[acc]);
   }
+  // Merge the four warps (rows 0-31, 32-63, 64-95, 96-127 of every tile).
+#pragma unroll
+  for (int ch = 0; ch < kMaxChunks; ++ch) {
+    const int c = ch * 32 + lane;
+    if (ch < nch && c < nb) {
+      s.wp_m[q * nb + c] = rm[ch];
+      s.wp_s[q * nb + c] = rs[ch];
+      s.wp_a[q * nb + c] = ra[ch];
+    }
+  }
+  named_bar_sync(1, 128);
+  for (int c = etid; c < nb; c += 128) {
+    float m = -INFINITY, sm = 0.f;
+    int a = 0x7fffffff;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) lse_merge(m, sm, a, s.wp_m[w * nb + c], s.wp_s[w * nb + c], s.wp_a[w * nb + c]);
+    s.run_m[c] = m;
+    s.run_s[c] = sm;
+    s.run_a[c] = a;
+  }
+  (void)ok;
   // Leave together if any role gave up (the decision is broadcast so that no
   // epilogue thread is left waiting on the named barrier).
   named_bar_sync(1, 128);
@@ -256,21 +307,37 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   named_bar_sync(1, 128);
   if (!*s.s_last) return;
   __threadfence();
-  for (int n = etid; n < p.M; n += 128) {
-    float m = -INFINITY, sm = 0.f;
-    int a = 0x7fffffff;
-    for (int b = 0; b < G; ++b) {
-      const size_t i = static_cast<size_t>(b) * p.M + n;
-      lse_merge(m, sm, a, __ldcg(p.part_m + i), __ldcg(p.part_s + i), __ldcg(p.part_a + i));
+  // The pipeline is drained, so the ring's shared memory is free: stage the
+  // G partials of up to 32 positions at a time with all threads loading in
+  // parallel, then merge each position's partials in CTA order.
+  float* pm_s = reinterpret_cast<float*>(s.ring);
+  float* ps_s = pm_s + G * 32;
+  int* pa_s = reinterpret_cast<int*>(ps_s + G * 32);
+  for (int n0 = 0; n0 < p.M; n0 += 32) {
+    const int cnt = min(32, p.M - n0);
+    for (int i = etid; i < G * cnt; i += 128) {
+      const int b = i / cnt, j = i - b * cnt;
+      const size_t g = static_cast<size_t>(b) * p.M + n0 + j;
+      pm_s[b * 32 + j] = __ldcg(p.part_m + g);
+      ps_s[b * 32 + j] = __ldcg(p.part_s + g);
+      pa_s[b * 32 + j] = __ldcg(p.part_a + g);
     }
-    const float lse = m + logf(sm);
-    const float pmax = 1.0f / sm;  // = exp(m - lse)
-    if (p.argmax) p.argmax[n] = a;
-    if (p.max_logit) p.max_logit[n] = m;
-    if (p.lse) p.lse[n] = lse;
-    if (p.max_prob) p.max_prob[n] = pmax;
-    s.run_m[n] = pmax;  // reuse: per-position max probability
-    s.run_a[n] = a;
+    named_bar_sync(1, 128);
+    if (etid < cnt) {
+      const int n = n0 + etid;
+      float m = -INFINITY, sm = 0.f;
+      int a = 0x7fffffff;
+      for (int b = 0; b < G; ++b) lse_merge(m, sm, a, pm_s[b * 32 + etid], ps_s[b * 32 + etid], pa_s[b * 32 + etid]);
+      const float lse = m + logf(sm);
+      const float pmax = 1.0f / sm;  // = exp(m - lse)
+      if (p.argmax) p.argmax[n] = a;
+      if (p.max_logit) p.max_logit[n] = m;
+      if (p.lse) p.lse[n] = lse;
+      if (p.max_prob) p.max_prob[n] = pmax;
+      s.run_m[n] = pmax;  // reuse: per-position max probability
+      s.run_a[n] = a;
+    }
+    named_bar_sync(1, 128);
   }
   named_bar_sync(1, 128);
   // Unmask rule, one thread per block of positions.
@@ -325,7 +392,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s.tfull[i], 1);
-      mbar_init(&s.tempty[i], 1);
+      mbar_init(&s.tempty[i], 4);  // one arrival per epilogue warp
     }
     mbar_init(s.drain, 1);
     *s.abort = 0u;
@@ -364,7 +431,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
 
 size_t head_smem_bytes(int stages, int nb) {
   return 1024 + static_cast<size_t>(stages) * (kATileBytes + static_cast<size_t>(nb) * 128) +
-         static_cast<size_t>(nb) * (4 * 12 + 12 + 4) + static_cast<size_t>(2 * stages + 5) * 8 + 64;
+         static_cast<size_t>(nb) * (4 * 12 + 12 + 4) + 4 * 32 * 33 * sizeof(float) +
+         static_cast<size_t>(2 * stages + 5) * 8 + 64;
 }
 
 cudaError_t launch_head(const HeadArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
