@@ -52,18 +52,19 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _expert_traffic():
-    """DRAM bytes per expert-kernel launch from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "expert_ffn_clover_block32.json")
+def _expert_traffic(u_mean):
+    """DRAM bytes per expert-kernel launch from the committed ncu summary
+    (bytes per expert x experts per launch), if that summary was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "expert_ffn_clover_layer_block32.md")
     src = os.path.join(ROOT, "block_diffusion_moe_gb300", "csrc", "expert.cu")
     try:
-        with open(path) as f:
-            prof = json.load(f)
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if prof.get("expert_cu_sha256") != h:
+        text = open(path).read()
+        sha = text.split("expert.cu sha256:")[1].split()[0]
+        per = float(text.split("DRAM bytes per expert (read + write, / 155 experts):")[1].split()[0])
+        if sha != hashlib.sha256(open(src, "rb").read()).hexdigest() or u_mean is None:
             return None
-        return float(prof["dram_bytes_per_launch_scaled"])
+        return per * (u_mean + 1)
     except Exception:
         return None
 
@@ -421,7 +422,7 @@ def run_ours(args):
                    "step_roofline_frac": step_bytes / (ms / args.steps * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": roof_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _expert_traffic() if kind != "head" else None, "launches": len(durs),
+                     "traffic": _expert_traffic(u_mean) if kind != "head" else None, "launches": len(durs),
                      "mean_launch_us": float(np.mean(durs)) * 1e3, "share_of_step": share},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_step,
