@@ -408,7 +408,8 @@ def run_ours(args):
     csum = clk.summary()
     launches_per_step = {"step": 1 + 3 * n_layers + 2, "zipf": 1 + 3 * n_layers + 2, "layer": 3, "head": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
-                   else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")
+                   else "k_layer (routing + grouped SwiGLU experts + combine, one launch per MoE layer)"
+                   if n_pos <= 32 else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

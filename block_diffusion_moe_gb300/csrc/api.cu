@@ -48,7 +48,10 @@ enum CtrlWord : int {
   kCtrlMaskedLeft = 2,   // positions still masked after the last head call
   kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
   kCtrlCommitted = 4,    // positions committed by the last head call
+  kCtrlBarCtr = 5,       // fused-layer grid barrier: arrivals (back to zero after each barrier)
+  kCtrlBarGen = 6,       // fused-layer grid barrier: generation
   kCtrlTokenGroups = 8,  // [32] routing arrival counters (reset by their last CTA)
+  kCtrlStamps = 40,      // [8 x u64] phase timestamps of the last fused-layer launch (diagnostics)
 };
 
 struct MoeLayout {
@@ -243,26 +246,11 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   int32_t* topk_idx = reinterpret_cast<int32_t*>(data + L.topk_idx);
   float* topk_w = reinterpret_cast<float*>(data + L.topk_w);
 
-  RouteArgs ra;
-  ra.x = x_in;
-  ra.wr = reinterpret_cast<const bf16*>(layer.router_w);
-  ra.bias = layer.router_bias;
-  ra.logits = reinterpret_cast<float*>(data + L.logits);
-  ra.xn_rows = xg + static_cast<size_t>(MK) * H;
-  ra.tg_ctr = ctrl + kCtrlTokenGroups;
-  ra.topk_idx = topk_idx;
-  ra.topk_w = topk_w;
-  ra.M = M;
-  ra.H = H;
-  ra.E = E;
-  ra.K = K;
-  ra.eps = d.rms_eps;
-  cudaError_t e = launch_route(ra, stream, kPdl);
-  if (e != cudaSuccess) return cuda_fail(e, "launch route");
-
+  // The fused kernel gives each CTA at most kRouteExperts router rows.
+  const bool fused = M <= kLayerMaxTokens && (E + plan.sms - 1) / plan.sms <= kRouteExperts;
+  cudaError_t e = cudaSuccess;
   PermArgs pa;
-  pa.topk_idx = topk_idx;
-  pa.topk_w = topk_w;
+  memset(&pa, 0, sizeof(pa));
   pa.tok_slot = reinterpret_cast<int32_t*>(data + L.tok_slot);
   pa.cnt = reinterpret_cast<int*>(data + L.cnt);
   pa.off = reinterpret_cast<int*>(data + L.off);
@@ -271,15 +259,36 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   pa.unit_ctr = ctrl + kCtrlUnitCtr;
   pa.gu_done = reinterpret_cast<int*>(data + L.gu_done);
   pa.dn_done = reinterpret_cast<int*>(data + L.dn_done);
-  pa.xg = xg;
-  pa.out_idx = out_idx;
-  pa.out_w = out_w;
-  pa.M = M;
-  pa.H = H;
-  pa.E = E;
-  pa.K = K;
-  e = launch_perm(pa, std::max(1, std::min(MK, plan.sms)), stream, kPdl);
-  if (e != cudaSuccess) return cuda_fail(e, "launch perm");
+  if (!fused) {
+    RouteArgs ra;
+    ra.x = x_in;
+    ra.wr = reinterpret_cast<const bf16*>(layer.router_w);
+    ra.bias = layer.router_bias;
+    ra.logits = reinterpret_cast<float*>(data + L.logits);
+    ra.xn_rows = xg + static_cast<size_t>(MK) * H;
+    ra.tg_ctr = ctrl + kCtrlTokenGroups;
+    ra.topk_idx = topk_idx;
+    ra.topk_w = topk_w;
+    ra.M = M;
+    ra.H = H;
+    ra.E = E;
+    ra.K = K;
+    ra.eps = d.rms_eps;
+    e = launch_route(ra, stream, kPdl);
+    if (e != cudaSuccess) return cuda_fail(e, "launch route");
+
+    pa.topk_idx = topk_idx;
+    pa.topk_w = topk_w;
+    pa.xg = xg;
+    pa.out_idx = out_idx;
+    pa.out_w = out_w;
+    pa.M = M;
+    pa.H = H;
+    pa.E = E;
+    pa.K = K;
+    e = launch_perm(pa, std::max(1, std::min(MK, plan.sms)), stream, kPdl);
+    if (e != cudaSuccess) return cuda_fail(e, "launch perm");
+  }
 
   ExpertArgs xa;
   memset(&xa, 0, sizeof(xa));
@@ -289,7 +298,11 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   if ((rc = encode_bf16_2d(&xa.tm_sgu, layer.sh_gate_up, 2ull * F, H, 64, "shared gate_up"))) return rc;
   if ((rc = encode_bf16_2d(&xa.tm_dn, layer.down, static_cast<uint64_t>(E) * H, F, 128, "down"))) return rc;
   if ((rc = encode_bf16_2d(&xa.tm_sdn, layer.sh_down, H, F, 128, "shared down"))) return rc;
-  if ((rc = encode_bf16_2d(&xa.tm_xg, xg, R, H, 16, "gathered inputs"))) return rc;
+  if (fused) {  // the gate/up B operand is the dense block of normed rows
+    if ((rc = encode_bf16_2d(&xa.tm_xg, xg + static_cast<size_t>(MK) * H, M, H, 16, "normed rows"))) return rc;
+  } else {
+    if ((rc = encode_bf16_2d(&xa.tm_xg, xg, R, H, 16, "gathered inputs"))) return rc;
+  }
   if ((rc = encode_bf16_2d(&xa.tm_h, hbuf, R, F, 16, "swiglu outputs"))) return rc;
   xa.x_in = x_in;
   xa.x_out = x_out;
@@ -311,7 +324,8 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.E = E;
   xa.K = K;
   const int nb = (M + 15) & ~15;
-  const size_t fixed = expert_smem_bytes(0, 0, nb) + static_cast<size_t>(4 * 16) * 8;
+  const size_t fixed = expert_smem_bytes(0, 0, nb) + static_cast<size_t>(4 * 16) * 8 +
+                       (fused ? layer_rt_bytes(M, K, E) : 0);
   const size_t budget = static_cast<size_t>(kSmemBudget) - fixed;
   int sa, sb;
   if (nb <= 64) {
@@ -323,12 +337,28 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.stages_a = sa;
   xa.stages_b = sb;
   xa.nb_max = nb;
-  const size_t smem = expert_smem_bytes(sa, sb, nb);
+  size_t smem = expert_smem_bytes(sa, sb, nb);
+  if (fused) {
+    xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
+    xa.bias = layer.router_bias;
+    xa.logits = reinterpret_cast<float*>(data + L.logits);
+    xa.xn = xg + static_cast<size_t>(MK) * H;
+    xa.bar_ctr = ctrl + kCtrlBarCtr;
+    xa.bar_gen = ctrl + kCtrlBarGen;
+    xa.tg_ctr = ctrl + kCtrlTokenGroups;
+    xa.pub_idx = topk_idx;
+    xa.pub_w = topk_w;
+    xa.out_idx = out_idx;
+    xa.out_w = out_w;
+    xa.eps = d.rms_eps;
+    xa.stamps = reinterpret_cast<unsigned long long*>(ctrl + kCtrlStamps);
+    smem += layer_rt_bytes(M, K, E);
+  }
   if (g_prof.begin && g_prof.cap > 0) {
     if ((rc = record(g_prof.begin[g_prof.count % g_prof.cap], stream))) return rc;
   }
-  e = launch_expert(xa, plan.sms, smem, stream, kPdl);
-  if (e != cudaSuccess) return cuda_fail(e, "launch expert");
+  e = fused ? launch_layer(xa, plan.sms, smem, stream, kPdl) : launch_expert(xa, plan.sms, smem, stream, kPdl);
+  if (e != cudaSuccess) return cuda_fail(e, fused ? "launch layer" : "launch expert");
   if (g_prof.end && g_prof.cap > 0) {
     if ((rc = record(g_prof.end[g_prof.count % g_prof.cap], stream))) return rc;
     ++g_prof.count;

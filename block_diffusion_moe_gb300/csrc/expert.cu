@@ -32,10 +32,19 @@
 // activations (B) with TMA, warps 3..6 are the epilogue (each reads the TMEM
 // lane quarter warp % 4). Two TMEM accumulators of 256 columns let the
 // epilogue of one unit overlap the MMAs of the next.
+//
+// k_layer (at most 32 tokens) also does the layer's routing itself, so a
+// whole MoE sublayer is one launch: every CTA normalises the tokens and
+// computes the router logits of its share of the experts, one grid barrier
+// publishes the logits, then every CTA takes the same top-k and permutation
+// into shared memory. Its gate/up units use all the tokens' normed rows as
+// the B operand (N = 32 at most) and keep only the routed columns, so no
+// gather is needed.
 #include <math.h>
 
 #include "kernels.cuh"
 #include "launch.cuh"
+#include "routing.cuh"
 #include "sm100.cuh"
 
 namespace clover {
@@ -54,10 +63,23 @@ struct Unit {
   int off;    // first row of the expert in the gathered buffers
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, int n_exp, const ExpertArgs& p) {
+// Where a launch finds its routing: global tables written by k_perm
+// (k_expert) or shared-memory tables built by the launch itself (k_layer).
+struct Rt {
+  const int* act;           // active routed expert ids, ascending
+  const int* cnt;           // [E] tokens per expert
+  const int* off;           // [E] first row per expert
+  const uint32_t* mask;     // [E] token bitmask (dense mode)
+  const int32_t* tok_slot;  // [M][K] row of each selection
+  const float* topk_w;      // [M][K] weight of each selection
+  int n_exp;                // active routed experts + the shared expert
+  int dense;                // gate/up B operand = all M normed rows
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArgs& p) {
   const int SF = p.F >> 6, SH = p.H >> 7;
   Unit w;
-  const int n_gu = n_exp * SF;
+  const int n_gu = rt.n_exp * SF;
   if (u < n_gu) {
     w.kind = 0;
     w.a = u / SF;
@@ -73,11 +95,16 @@ __device__ __forceinline__ Unit decode_unit(int u, int n_exp, const ExpertArgs& 
     w.cnt = p.M;
     w.off = p.M * p.K;
   } else {
-    w.e = p.act[w.a - 1];
-    w.cnt = p.cnt[w.e];
-    w.off = p.off[w.e];
+    w.e = rt.act[w.a - 1];
+    w.cnt = rt.cnt[w.e];
+    w.off = rt.off[w.e];
   }
   return w;
+}
+
+// B rows (the MMA N) of a unit: dense gate/up units take all M token rows.
+__device__ __forceinline__ int unit_rows(const Unit& w, const Rt& rt, const ExpertArgs& p) {
+  return ((w.kind == 0 && rt.dense) ? p.M + 15 : w.cnt + 15) & ~15;
 }
 
 struct Smem {
@@ -91,6 +118,7 @@ struct Smem {
   volatile int* s_last;
   volatile int* s_unit;
   volatile int* s_ok;
+  uint8_t* rt_region;  // k_layer's routing tables
   uint32_t b_stage_bytes;
 };
 
@@ -118,6 +146,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   s.s_last = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
   s.s_unit = s.s_last + 1;
   s.s_ok = s.s_last + 2;
+  s.rt_region = reinterpret_cast<uint8_t*>(s.tmem_slot) + 128;
   return s;
 }
 
@@ -133,7 +162,7 @@ __device__ void drain_ring(uint64_t* full, int stages, uint32_t issued_mask, uin
     if (issued_mask & (1u << i)) mbar_wait_for(&full[i], (parity_bits >> i) & 1u, 200000000ull);
 }
 
-__device__ void producer_a(const ExpertArgs& p, const Smem& s, int n_exp, int n_total) {
+__device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int n_total) {
   const uint64_t pol = l2_policy_evict_first();
   const int SA = p.stages_a;
   int sa = 0;
@@ -150,7 +179,7 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, int n_exp, int n_
     s.unit_ids[us] = u;
     mbar_arrive(&s.ufull[us]);
     if (u < 0) break;
-    const Unit w = decode_unit(u, n_exp, p);
+    const Unit w = decode_unit(u, rt, p);
     const CUtensorMap* m;
     int row, nk;
     if (w.kind == 0) {
@@ -195,7 +224,7 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, int n_exp, int n_
   if (*s.abort) drain_ring(s.full_a, SA, issued, parity_bits);
 }
 
-__device__ void producer_b(const ExpertArgs& p, const Smem& s, int n_exp) {
+__device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
   const uint64_t pol = l2_policy_evict_last();
   const int SB = p.stages_b;
   const int SF = p.F >> 6;
@@ -211,8 +240,9 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, int n_exp) {
     const int u = s.unit_ids[us];
     mbar_arrive(&s.uempty[us]);
     if (u < 0) break;
-    const Unit w = decode_unit(u, n_exp, p);
-    const int nrows = (w.cnt + 15) & ~15;
+    const Unit w = decode_unit(u, rt, p);
+    const int nrows = unit_rows(w, rt, p);
+    const int row0 = (w.kind == 0 && rt.dense) ? 0 : w.off;
     const CUtensorMap* m;
     int nk;
     if (w.kind == 0) {
@@ -251,7 +281,7 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, int n_exp) {
       }
       const uint32_t dst = smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes);
       mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(nrows) * 128u);
-      for (int i = 0; i < nrows; i += 16) tma_load_2d(dst + i * 128, m, &s.full_b[sb], kc * 64, w.off + i, pol);
+      for (int i = 0; i < nrows; i += 16) tma_load_2d(dst + i * 128, m, &s.full_b[sb], kc * 64, row0 + i, pol);
       issued |= 1u << sb;
       parity_bits = (parity_bits & ~(1u << sb)) | (phb << sb);
       if (++sb == SB) {
@@ -264,7 +294,7 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, int n_exp) {
   if (*s.abort) drain_ring(s.full_b, SB, issued, parity_bits);
 }
 
-__device__ void mma_issuer(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t tmem_base) {
+__device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int SA = p.stages_a, SB = p.stages_b;
   int sa = 0, sb = 0;
   uint32_t pha = 0, phb = 0;
@@ -278,8 +308,8 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, int n_exp, uint32
     const int u = s.unit_ids[us];
     mbar_arrive(&s.uempty[us]);
     if (u < 0) break;
-    const Unit w = decode_unit(u, n_exp, p);
-    const int n = (w.cnt + 15) & ~15;
+    const Unit w = decode_unit(u, rt, p);
+    const int n = unit_rows(w, rt, p);
     const int nk = (w.kind == 0) ? (p.H >> 6) : (p.F >> 6);
     const uint32_t idesc = umma_idesc_bf16(128, n);
     const int acc = it & 1;
@@ -325,7 +355,7 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, int n_exp, uint32
 
 // Sums the weighted expert rows of one 128-wide hidden slice into the
 // residual stream: x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t).
-__device__ void combine_slice(const ExpertArgs& p, int j, int etid) {
+__device__ void combine_slice(const ExpertArgs& p, const Rt& rt, int j, int etid) {
   const int c4 = (etid & 31) * 4;
   const int g = etid >> 5;
   const size_t H = p.H;
@@ -345,8 +375,8 @@ __device__ void combine_slice(const ExpertArgs& p, int j, int etid) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const bool v = k0 + i < K;
-        r[i] = v ? p.tok_slot[t * K + k0 + i] : MK + t;
-        wk[i] = v ? p.topk_w[t * K + k0 + i] : 0.f;
+        r[i] = v ? rt.tok_slot[t * K + k0 + i] : MK + t;
+        wk[i] = v ? rt.topk_w[t * K + k0 + i] : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -374,7 +404,7 @@ __device__ void combine_slice(const ExpertArgs& p, int j, int etid) {
   }
 }
 
-__device__ void epilogue(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t tmem_base) {
+__device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;             // TMEM lane quarter this warp may read
   const int row = q * 32 + lane;      // accumulator row
@@ -396,8 +426,8 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t
     named_bar_sync(1, 128);
     const int u = *s.s_unit;
     if (u < 0) break;
-    const Unit w = decode_unit(u, n_exp, p);
-    const int n = (w.cnt + 15) & ~15;
+    const Unit w = decode_unit(u, rt, p);
+    const int n = unit_rows(w, rt, p);
     const int acc = it & 1;
     const uint32_t apar = (it >> 1) & 1;
     if (etid == 0) {
@@ -422,14 +452,23 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t
         }
         named_bar_sync(1, 128);
         if (q < 2) {
+          // dense mode: column c is token c; a routed expert keeps the
+          // columns of its tokens, stored at their rank among them
+          const uint32_t tm = (rt.dense && w.a != 0) ? rt.mask[w.e] : 0xffffffffu;
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = c0 + j;
-            if (c < w.cnt) {
+            int slot = c;
+            bool keep = c < w.cnt;
+            if (rt.dense) {
+              keep = c < p.M && ((tm >> c) & 1u);
+              slot = (w.a == 0) ? c : __popc(tm & ((1u << c) - 1u));
+            }
+            if (keep) {
               const float g = v[j];
               const float up = s.xch[row * 17 + j];
               const float h = g / (1.0f + expf(-g)) * up;
-              hrow[static_cast<size_t>(c) * p.F] = __float2bfloat16_rn(h);
+              hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(h);
             }
           }
         }
@@ -461,25 +500,23 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, int n_exp, uint32_t
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
         const int old = atomicAdd(&p.dn_done[w.slice], 1);
-        *s.s_last = (old == n_exp - 1) ? 1 : 0;
+        *s.s_last = (old == rt.n_exp - 1) ? 1 : 0;
       }
       named_bar_sync(1, 128);
       if (*s.s_last) {
         __threadfence();
-        combine_slice(p, w.slice, etid);
+        combine_slice(p, rt, w.slice, etid);
       }
     }
-    (void)SF;
   }
+  (void)SF;
 }
 
-}  // namespace
 
-__global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_constant__ ExpertArgs p) {
-  extern __shared__ uint8_t smem_raw[];
-  const Smem s = carve(smem_raw, p);
+// Barrier setup, TMEM allocation and descriptor prefetch (before the
+// dependency wait, so they overlap the previous kernel).
+__device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const Smem& s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages_a; ++i) {
       mbar_init(&s.full_a[i], 1);
@@ -514,23 +551,21 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *s.tmem_slot;
+  return *s.tmem_slot;
+}
 
-  pdl_wait();
-  pdl_trigger();
-  const int n_exp = *p.n_active + 1;
-  const int n_total = n_exp * ((p.F >> 6) + (p.H >> 7));
-
+__device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_total = rt.n_exp * ((p.F >> 6) + (p.H >> 7));
   if (warp == 0) {
-    if (lane == 0) producer_a(p, s, n_exp, n_total);
+    if (lane == 0) producer_a(p, s, rt, n_total);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(p, s, n_exp, tmem_base);
+    if (lane == 0) mma_issuer(p, s, rt, tmem_base);
   } else if (warp == 2) {
-    if (lane == 0) producer_b(p, s, n_exp);
-  } else {
-    epilogue(p, s, n_exp, tmem_base);
-  }
-
+    if (lane == 0) producer_b(p, s, rt);
+  } else if (warp < 7) {
+    epilogue(p, s, rt, tmem_base);
+  }  // warp 7 has no role here
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -540,10 +575,222 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_const
   }
 }
 
+}  // namespace
+
+__global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_constant__ ExpertArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem s = carve(smem_raw, p);
+  const uint32_t tmem_base = expert_prologue(p, s);
+  pdl_wait();
+  pdl_trigger();
+  Rt rt;
+  rt.act = p.act;
+  rt.cnt = p.cnt;
+  rt.off = p.off;
+  rt.mask = nullptr;
+  rt.tok_slot = p.tok_slot;
+  rt.topk_w = p.topk_w;
+  rt.n_exp = *p.n_active + 1;
+  rt.dense = 0;
+  expert_roles(p, s, rt, tmem_base);
+}
+
+namespace {
+
+// Grid-wide barrier for a persistent launch (every CTA is resident: one per
+// SM). The last CTA to arrive resets the counter and bumps the generation
+// word the others wait on (bounded). Returns false on timeout.
+__device__ bool grid_barrier(int* ctr, int* gen, int* err) {
+  __shared__ int s_pass;
+  fence_proxy_async_global();  // rows stored before the barrier are read by TMA after it
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int g0 = ld_acquire_gpu(gen);
+    int pass = 1;
+    if (atomicAdd(ctr, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(ctr, 0);
+      __threadfence();
+      atomicAdd(gen, 1);
+    } else {
+      const unsigned long long t0 = global_ns();
+      while (ld_acquire_gpu(gen) == g0) {
+        if (global_ns() - t0 > kWaitLimitNs) {
+          atomicOr(err, kErrDepTimeout);
+          pass = 0;
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    s_pass = pass;
+  }
+  __syncthreads();
+  __threadfence();
+  fence_proxy_async_global();
+  return s_pass != 0;
+}
+
+}  // namespace
+
+// One MoE sublayer for M <= 32 tokens in one launch: routing, experts and
+// combine (see the file comment).
+__global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_constant__ ExpertArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem s = carve(smem_raw, p);
+  const uint32_t tmem_base = expert_prologue(p, s);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const int M = p.M, K = p.K, E = p.E, H = p.H;
+  const int MK = M * K;
+
+  // shared routing tables
+  int32_t* s_idx = reinterpret_cast<int32_t*>(s.rt_region);  // [M*K]
+  float* s_w = reinterpret_cast<float*>(s_idx + MK);         // [M*K]
+  int32_t* s_slot = reinterpret_cast<int32_t*>(s_w + MK);    // [M*K]
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_slot + MK);  // [E]
+  int* s_cnt = reinterpret_cast<int*>(s_mask + E);             // [E]
+  int* s_off = s_cnt + E;                                       // [E]
+  int* s_act = s_off + E;                                       // [E]
+  int* s_nact = s_act + E;                                      // [1]
+
+  // Phase 1 work items: (8 experts, 8 tokens); one token per warp.
+  const int n_eg = (E + kRouteExperts - 1) / kRouteExperts;
+  const int n_tg = (M + kRouteTokens - 1) / kRouteTokens;
+  const int n_items = n_eg * n_tg;
+  // Router rows do not depend on earlier kernels: pull this CTA's into L2.
+  for (int item = blockIdx.x; item < n_items; item += G) {
+    const int eg = item % n_eg;
+    const int ne = min(kRouteExperts, E - eg * kRouteExperts);
+    const __nv_bfloat16* wr = p.wr + static_cast<size_t>(eg) * kRouteExperts * H;
+    for (int i = threadIdx.x * 64; i < ne * H; i += blockDim.x * 64)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wr + i));
+  }
+  unsigned long long* st = (blockIdx.x == 0 && threadIdx.x == 0) ? p.stamps : nullptr;
+  if (st) st[0] = global_ns();
+  pdl_wait();
+  pdl_trigger();
+  if (st) st[1] = global_ns();
+
+  // Phase 1: norms, normed rows (written once) and router logits. The last
+  // CTA to finish a token group takes top-k for its tokens.
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) p.gu_done[i] = 0;
+    for (int i = threadIdx.x; i < (H >> 7); i += blockDim.x) p.dn_done[i] = 0;
+    if (threadIdx.x == 0) *p.unit_ctr = 0;
+  }
+  __shared__ int s_tg_last;
+  for (int item = blockIdx.x; item < n_items; item += G) {
+    const int eg = item % n_eg, tg = item / n_eg;
+    const int e0 = eg * kRouteExperts;
+    const int ne = min(kRouteExperts, E - e0);
+    const int t = tg * kRouteTokens + warp;
+    if (warp < kRouteTokens && t < M) {
+      const float* xr = p.x_in + static_cast<size_t>(t) * H;
+      const float rstd = row_rstd(xr, H, p.eps, lane);
+      const float lg = warp_router_dots<kRouteExperts>(xr, rstd, p.wr + static_cast<size_t>(e0) * H, ne, H, lane,
+                                                       eg == 0 ? p.xn + static_cast<size_t>(t) * H : nullptr);
+      if (lane < ne) p.logits[static_cast<size_t>(t) * E + e0 + lane] = lg + (p.bias ? p.bias[e0 + lane] : 0.f);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_tg_last = (atomicAdd(&p.tg_ctr[tg], 1) == n_eg - 1) ? 1 : 0;
+    __syncthreads();
+    if (s_tg_last) {
+      __threadfence();
+      if (warp < kRouteTokens && t < M) {
+        const TopkSel sel = warp_topk(p.logits + static_cast<size_t>(t) * E, E, K, lane);
+        if (lane < K) {
+          p.pub_idx[t * K + lane] = sel.e;
+          p.pub_w[t * K + lane] = sel.w;
+        }
+      }
+      if (threadIdx.x == 0) p.tg_ctr[tg] = 0;
+    }
+  }
+  if (p.stamps != nullptr) {
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(p.stamps + 2, global_ns());
+  }
+  if (!grid_barrier(p.bar_ctr, p.bar_gen, p.err)) *s.abort = 1u;
+  if (st) st[3] = global_ns();
+
+  // Phase 2: every CTA builds the same permutation from the published top-k.
+  for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+    const int e = __ldcg(p.pub_idx + i);
+    s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
+    s_w[i] = __ldcg(p.pub_w + i);
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
+  __syncthreads();
+  if (st) st[6] = global_ns();
+  for (int i = threadIdx.x; i < MK; i += blockDim.x) atomicOr(&s_mask[s_idx[i]], 1u << (i / K));
+  __syncthreads();
+  if (st) st[7] = global_ns();
+  if (warp == 0) {  // counts, offsets and the active list, 32 experts at a time
+    int base_off = 0, base_act = 0;
+    for (int e0c = 0; e0c < E; e0c += 32) {
+      const int e = e0c + lane;
+      const int c = (e < E) ? __popc(s_mask[e]) : 0;
+      int incl = c, acti = c > 0 ? 1 : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n1 = __shfl_up_sync(0xffffffffu, incl, o);
+        const int n2 = __shfl_up_sync(0xffffffffu, acti, o);
+        if (lane >= o) {
+          incl += n1;
+          acti += n2;
+        }
+      }
+      if (e < E) {
+        s_cnt[e] = c;
+        s_off[e] = base_off + incl - c;
+        if (c > 0) s_act[base_act + acti - 1] = e;
+      }
+      base_off += __shfl_sync(0xffffffffu, incl, 31);
+      base_act += __shfl_sync(0xffffffffu, acti, 31);
+    }
+    if (lane == 0) *s_nact = base_act;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+    const int e = s_idx[i], t = i / K;
+    s_slot[i] = s_off[e] + __popc(s_mask[e] & ((1u << t) - 1u));
+  }
+  if (blockIdx.x == 0) {
+    if (p.out_idx)
+      for (int i = threadIdx.x; i < MK; i += blockDim.x) p.out_idx[i] = s_idx[i];
+    if (p.out_w)
+      for (int i = threadIdx.x; i < MK; i += blockDim.x) p.out_w[i] = s_w[i];
+  }
+  __syncthreads();
+
+  Rt rt;
+  rt.act = s_act;
+  rt.cnt = s_cnt;
+  rt.off = s_off;
+  rt.mask = s_mask;
+  rt.tok_slot = s_slot;
+  rt.topk_w = s_w;
+  rt.n_exp = (*s.abort) ? 0 : *s_nact + 1;  // after a failed barrier no unit runs
+  rt.dense = 1;
+  if (st) st[4] = global_ns();
+  expert_roles(p, s, rt, tmem_base);
+  if (p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
+}
+
 size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {
   return 1024 + static_cast<size_t>(stages_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
          64 * 17 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
-         128;
+         256;
+}
+
+size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(3 * M * K + 4 * E + 4) * 4; }
+
+cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  cudaError_t e = cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_kernel(k_layer, dim3(grid), dim3(kExpertThreads), smem, s, pdl, a);
 }
 
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {

@@ -18,8 +18,9 @@ constexpr int kMaxTokens = 256;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 
-// Expert kernel: 7 warps (A loads, MMA, B loads, 4 epilogue warps).
-constexpr int kExpertThreads = 224;
+// Expert kernel: 8 warps (A loads, MMA, B loads, 4 epilogue warps, and one
+// more that only takes part in the fused kernel's routing phase).
+constexpr int kExpertThreads = 256;
 constexpr int kExpertUnitRing = 4;
 // Head kernel: 6 warps (loads, MMA, 4 epilogue warps).
 constexpr int kHeadThreads = 192;
@@ -97,6 +98,22 @@ struct ExpertArgs {
   int* err;
   int M, H, F, E, K;
   int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
+  // fused-layer launches only (k_layer)
+  const bf16* wr;      // [E][H] router
+  const float* bias;   // [E] or null
+  float* logits;       // [M][E]
+  bf16* xn;            // [M][H] normed rows = the gate/up B operand
+  int* bar_ctr;        // grid barrier arrival counter (zero between launches)
+  int* bar_gen;        // grid barrier generation
+  int* tg_ctr;         // [ceil(M/8)] token-group arrival counters (zero between launches)
+  int32_t* pub_idx;    // [M][K] top-k ids published by the token groups' last CTAs
+  float* pub_w;        // [M][K] top-k weights, likewise
+  int32_t* out_idx;    // optional [M][K] copies for the caller
+  float* out_w;
+  float eps;
+  unsigned long long* stamps;  // optional phase timestamps (diagnostics): [0] start, [1] after the
+                               // dependency wait, [2] last CTA done with phase 1, [3] after the
+                               // barrier, [4] routing done, [5] last CTA done
 };
 
 struct HeadArgs {
@@ -126,6 +143,10 @@ cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_perm(const PermArgs& a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
+cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
+size_t layer_rt_bytes(int M, int K, int E);
+// Largest token count the fused layer kernel takes (one 32-bit mask per expert).
+constexpr int kLayerMaxTokens = 32;
 cudaError_t launch_head(const HeadArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 
 size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max);

@@ -10,6 +10,7 @@
 
 #include "kernels.cuh"
 #include "launch.cuh"
+#include "routing.cuh"
 #include "sm100.cuh"
 
 namespace clover {
@@ -40,19 +41,6 @@ __global__ void __launch_bounds__(256) k_embed(EmbedArgs a) {
     o.w = __high2float(e23) + cv.w;
     *reinterpret_cast<float4*>(xr + c) = o;
   }
-}
-
-// Reciprocal RMS of one row, computed by one warp: 1 / sqrt(mean(x^2) + eps).
-// Loads are unrolled so that several are in flight per lane.
-__device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int lane) {
-  float ss = 0.f;
-#pragma unroll 8
-  for (int c = lane * 4; c < H; c += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(xr + c);
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-  }
-  ss = warp_sum_f(ss);
-  return 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
 }
 
 // ---------------------------------------------------------------- rmsnorm
@@ -110,40 +98,8 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
   for (int t = t0 + warp; t < t1; t += 8) {
     const float* xr = a.x + static_cast<size_t>(t) * H;
     const float rstd = row_rstd(xr, H, a.eps, lane);
-    float acc[kRouteExperts];
-#pragma unroll
-    for (int e = 0; e < kRouteExperts; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int c = lane * 4; c < H; c += 128) {
-      const float4 v = *reinterpret_cast<const float4*>(xr + c);
-      __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * rstd, v.y * rstd);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * rstd, v.w * rstd);
-      if (blockIdx.x == 0) {
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t*>(&lo);
-        pk.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(a.xn_rows + static_cast<size_t>(t) * H + c) = pk;
-      }
-      const float x0 = __low2float(lo), x1 = __high2float(lo), x2 = __low2float(hi), x3 = __high2float(hi);
-#pragma unroll
-      for (int e = 0; e < kRouteExperts; ++e) {
-        if (e < ne) {
-          const uint2 wb = *reinterpret_cast<const uint2*>(w + e * H + c);
-          const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wb.x);
-          const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wb.y);
-          acc[e] = fmaf(x0, __low2float(w01), acc[e]);
-          acc[e] = fmaf(x1, __high2float(w01), acc[e]);
-          acc[e] = fmaf(x2, __low2float(w23), acc[e]);
-          acc[e] = fmaf(x3, __high2float(w23), acc[e]);
-        }
-      }
-    }
-    float mine = 0.f;
-#pragma unroll
-    for (int e = 0; e < kRouteExperts; ++e) {
-      const float s = warp_sum_f(acc[e]);
-      if (lane == e) mine = s;
-    }
+    const float mine = warp_router_dots<kRouteExperts>(
+        xr, rstd, w, ne, H, lane, blockIdx.x == 0 ? a.xn_rows + static_cast<size_t>(t) * H : nullptr);
     if (lane < ne) {
       const int e = e0 + lane;
       a.logits[static_cast<size_t>(t) * a.E + e] = mine + (a.bias ? a.bias[e] : 0.f);
@@ -163,50 +119,10 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
   // Top-k for this token group (one warp per token; lane l holds experts
   // l, l+32, ..., up to 256).
   for (int t = t0 + warp; t < t1; t += 8) {
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < a.E) ? __ldcg(a.logits + static_cast<size_t>(t) * a.E + e) : -INFINITY;
-    }
-    float my_v = -INFINITY;
-    int my_e = 0;
-    for (int k = 0; k < a.K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < a.E && (v[i] > bv || (v[i] == bv && e < be))) {
-          bv = v[i];
-          be = e;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i == (be >> 5)) v[i] = -INFINITY;
-      }
-      if (lane == k) {
-        my_v = bv;
-        my_e = be;
-      }
-    }
-    const float top = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = (lane < a.K) ? expf(my_v - top) : 0.f;
-    const float sum = warp_sum_f(ex);
+    const TopkSel sel = warp_topk(a.logits + static_cast<size_t>(t) * a.E, a.E, a.K, lane);
     if (lane < a.K) {
-      a.topk_idx[static_cast<size_t>(t) * a.K + lane] = my_e;
-      a.topk_w[static_cast<size_t>(t) * a.K + lane] = ex / sum;
+      a.topk_idx[static_cast<size_t>(t) * a.K + lane] = sel.e;
+      a.topk_w[static_cast<size_t>(t) * a.K + lane] = sel.w;
     }
   }
   if (tid == 0) a.tg_ctr[blockIdx.y] = 0;

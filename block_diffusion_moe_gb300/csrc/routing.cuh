@@ -1,0 +1,129 @@
+// Per-warp routing arithmetic shared by the standalone routing kernel and
+// the fused layer kernel, so both take identical decisions bit for bit.
+//
+// Follows "Clover-35B-A3B: how a diffusion model gets to 680 tokens a second,
+// read from its files", sections "What Clover is" (256 experts, 8 per token)
+// and "The expert selection" (top-8 routing probabilities).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "sm100.cuh"
+
+namespace clover {
+
+// Reciprocal RMS of one row, computed by one warp: 1 / sqrt(mean(x^2) + eps).
+// Loads are unrolled so that several are in flight per lane.
+__device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int lane) {
+  float ss = 0.f;
+#pragma unroll 8
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum_f(ss);
+  return 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
+}
+
+// One warp, one token row xr: xn = bf16(xr * rstd) (stored to xn_out when
+// non-null) and the router logits of experts w_rows[0..ne) (ne <= 8), each a
+// bf16 row of H. Lane e (< ne) receives logit e (without bias).
+template <int kMaxE>
+__device__ __forceinline__ float warp_router_dots(const float* xr, float rstd, const __nv_bfloat16* w_rows, int ne,
+                                                  int H, int lane, __nv_bfloat16* xn_out) {
+  float acc[kMaxE];
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) acc[e] = 0.f;
+#pragma unroll 4
+  for (int c = lane * 4; c < H; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * rstd, v.y * rstd);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * rstd, v.w * rstd);
+    if (xn_out != nullptr) {
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(xn_out + c) = pk;
+    }
+    const float x0 = __low2float(lo), x1 = __high2float(lo), x2 = __low2float(hi), x3 = __high2float(hi);
+#pragma unroll
+    for (int e = 0; e < kMaxE; ++e) {
+      if (e < ne) {
+        const uint2 wb = *reinterpret_cast<const uint2*>(w_rows + static_cast<size_t>(e) * H + c);
+        const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wb.x);
+        const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wb.y);
+        acc[e] = fmaf(x0, __low2float(w01), acc[e]);
+        acc[e] = fmaf(x1, __high2float(w01), acc[e]);
+        acc[e] = fmaf(x2, __low2float(w23), acc[e]);
+        acc[e] = fmaf(x3, __high2float(w23), acc[e]);
+      }
+    }
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) {
+    const float s = warp_sum_f(acc[e]);
+    if (lane == e) mine = s;
+  }
+  return mine;
+}
+
+struct TopkSel {
+  int e;
+  float w;
+};
+
+// One warp, one token: top-k of E (<= 256) logits by descending value, the
+// lower expert id first on ties; weights = softmax over the selected logits
+// (= the top-k probabilities renormalised). Lane k (< K) receives selection k
+// and its weight.
+__device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int K, int lane) {
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldcg(logits_row + e) : -INFINITY;
+  }
+  float my_v = -INFINITY;
+  int my_e = 0;
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
+        bv = v[i];
+        be = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (i == (be >> 5)) v[i] = -INFINITY;
+    }
+    if (lane == k) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  const float top = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = (lane < K) ? expf(my_v - top) : 0.f;
+  const float sum = warp_sum_f(ex);
+  TopkSel r;
+  r.e = my_e;
+  r.w = ex / sum;
+  return r;
+}
+
+}  // namespace clover
