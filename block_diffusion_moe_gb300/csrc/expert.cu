@@ -638,6 +638,8 @@ __device__ bool grid_barrier(int* ctr, int* gen, int* err) {
 __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_constant__ ExpertArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.tmem_slot) + 96);
+  if (threadIdx.x == 0) mbar_init(wbar, 1);  // made visible by the prologue's fence
   const uint32_t tmem_base = expert_prologue(p, s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
@@ -658,13 +660,23 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
   const int n_eg = (E + kRouteExperts - 1) / kRouteExperts;
   const int n_tg = (M + kRouteTokens - 1) / kRouteTokens;
   const int n_items = n_eg * n_tg;
-  // Router rows do not depend on earlier kernels: pull this CTA's into L2.
-  for (int item = blockIdx.x; item < n_items; item += G) {
-    const int eg = item % n_eg;
-    const int ne = min(kRouteExperts, E - eg * kRouteExperts);
-    const __nv_bfloat16* wr = p.wr + static_cast<size_t>(eg) * kRouteExperts * H;
-    for (int i = threadIdx.x * 64; i < ne * H; i += blockDim.x * 64)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(wr + i));
+  // Router rows do not depend on earlier kernels: copy this CTA's slices
+  // into the (still idle) weight ring before waiting.
+  const int my_items = (n_items > static_cast<int>(blockIdx.x)) ? (n_items - 1 - blockIdx.x) / G + 1 : 0;
+  const uint32_t wslice = kRouteExperts * H * 2;
+  const bool wr_staged = my_items * wslice <= static_cast<uint32_t>(p.stages_a) * kATileBytes;
+  if (threadIdx.x == 0 && wr_staged && my_items > 0) {
+    uint32_t bytes = 0;
+    for (int j = 0; j < my_items; ++j) {
+      const int eg = (blockIdx.x + j * G) % n_eg;
+      bytes += min(kRouteExperts, E - eg * kRouteExperts) * H * 2;
+    }
+    mbar_arrive_expect_tx(wbar, bytes);
+    for (int j = 0; j < my_items; ++j) {
+      const int eg = (blockIdx.x + j * G) % n_eg;
+      const int ne = min(kRouteExperts, E - eg * kRouteExperts);
+      bulk_load(smem_u32(s.a_ring) + j * wslice, p.wr + static_cast<size_t>(eg) * kRouteExperts * H, ne * H * 2, wbar);
+    }
   }
   unsigned long long* st = (blockIdx.x == 0 && threadIdx.x == 0) ? p.stamps : nullptr;
   if (st) st[0] = global_ns();
@@ -680,16 +692,27 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
     if (threadIdx.x == 0) *p.unit_ctr = 0;
   }
   __shared__ int s_tg_last;
-  for (int item = blockIdx.x; item < n_items; item += G) {
+  if (wr_staged && my_items > 0 && !mbar_wait(wbar, 0, s.abort)) {
+    atomicOr(p.err, kErrMbarTimeout);
+    *s.abort = 1u;
+  }
+  for (int item = blockIdx.x, j = 0; item < n_items; item += G, ++j) {
     const int eg = item % n_eg, tg = item / n_eg;
     const int e0 = eg * kRouteExperts;
     const int ne = min(kRouteExperts, E - e0);
     const int t = tg * kRouteTokens + warp;
     if (warp < kRouteTokens && t < M) {
       const float* xr = p.x_in + static_cast<size_t>(t) * H;
-      const float rstd = row_rstd(xr, H, p.eps, lane);
-      const float lg = warp_router_dots<kRouteExperts>(xr, rstd, p.wr + static_cast<size_t>(e0) * H, ne, H, lane,
-                                                       eg == 0 ? p.xn + static_cast<size_t>(t) * H : nullptr);
+      const __nv_bfloat16* w_rows = wr_staged ? reinterpret_cast<const __nv_bfloat16*>(s.a_ring + j * wslice)
+                                              : p.wr + static_cast<size_t>(e0) * H;
+      __nv_bfloat16* xn_out = eg == 0 ? p.xn + static_cast<size_t>(t) * H : nullptr;
+      float lg;
+      if (H <= 128 * 16) {
+        lg = warp_router_row_reg<kRouteExperts, 16>(xr, p.eps, w_rows, ne, H, lane, xn_out);
+      } else {
+        const float rstd = row_rstd(xr, H, p.eps, lane);
+        lg = warp_router_dots<kRouteExperts>(xr, rstd, w_rows, ne, H, lane, xn_out);
+      }
       if (lane < ne) p.logits[static_cast<size_t>(t) * E + e0 + lane] = lg + (p.bias ? p.bias[e0 + lane] : 0.f);
     }
     __threadfence();
@@ -708,6 +731,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
       if (threadIdx.x == 0) p.tg_ctr[tg] = 0;
     }
   }
+  fence_proxy_async_shared();  // the ring was read generically; TMA refills it later
   if (p.stamps != nullptr) {
     __syncthreads();
     if (threadIdx.x == 0) atomicMax(p.stamps + 2, global_ns());

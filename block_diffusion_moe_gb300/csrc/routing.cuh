@@ -26,6 +26,62 @@ __device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int
   return 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
 }
 
+// As row_rstd + warp_router_dots for H <= 128 * kChunks, with the row held
+// in registers between the two (one load of the row, all loads in flight at
+// once). Same arithmetic order, so the results are identical.
+template <int kMaxE, int kChunks>
+__device__ __forceinline__ float warp_router_row_reg(const float* xr, float eps, const __nv_bfloat16* w_rows, int ne,
+                                                     int H, int lane, __nv_bfloat16* xn_out) {
+  float4 xv[kChunks];
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int c = lane * 4 + 128 * j;
+    xv[j] = (c < H) ? *reinterpret_cast<const float4*>(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) ss += xv[j].x * xv[j].x + xv[j].y * xv[j].y + xv[j].z * xv[j].z + xv[j].w * xv[j].w;
+  ss = warp_sum_f(ss);
+  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
+  float acc[kMaxE];
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int c = lane * 4 + 128 * j;
+    if (c < H) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(xv[j].x * rstd, xv[j].y * rstd);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(xv[j].z * rstd, xv[j].w * rstd);
+      if (xn_out != nullptr) {
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(xn_out + c) = pk;
+      }
+      const float x0 = __low2float(lo), x1 = __high2float(lo), x2 = __low2float(hi), x3 = __high2float(hi);
+#pragma unroll
+      for (int e = 0; e < kMaxE; ++e) {
+        if (e < ne) {
+          const uint2 wb = *reinterpret_cast<const uint2*>(w_rows + static_cast<size_t>(e) * H + c);
+          const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wb.x);
+          const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wb.y);
+          acc[e] = fmaf(x0, __low2float(w01), acc[e]);
+          acc[e] = fmaf(x1, __high2float(w01), acc[e]);
+          acc[e] = fmaf(x2, __low2float(w23), acc[e]);
+          acc[e] = fmaf(x3, __high2float(w23), acc[e]);
+        }
+      }
+    }
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < kMaxE; ++e) {
+    const float sm = warp_sum_f(acc[e]);
+    if (lane == e) mine = sm;
+  }
+  return mine;
+}
+
 // One warp, one token row xr: xn = bf16(xr * rstd) (stored to xn_out when
 // non-null) and the router logits of experts w_rows[0..ne) (ne <= 8), each a
 // bf16 row of H. Lane e (< ne) receives logit e (without bias).
