@@ -419,7 +419,10 @@ def run_ours(args):
     if rank != 0:
         return
     csum = clk.summary()
-    launches_per_step = {"step": 1 + 3 * n_layers + 2, "zipf": 1 + 3 * n_layers + 2, "layer": 3, "head": 2}[kind]
+    # <= 32 positions: one fused launch per layer; more: route, perm, experts, combine
+    per_layer = 1 if n_pos <= 32 else 4
+    launches_per_step = {"step": 1 + per_layer * n_layers + 2, "zipf": 1 + per_layer * n_layers + 2,
+                         "layer": per_layer, "head": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
                    else "k_layer (routing + grouped SwiGLU experts + combine, one launch per MoE layer)"
                    if n_pos <= 32 else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")

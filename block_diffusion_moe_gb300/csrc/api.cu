@@ -337,6 +337,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.stages_a = sa;
   xa.stages_b = sb;
   xa.nb_max = nb;
+  // Up to 32 tokens the slice that finishes last combines (a few µs); with
+  // more tokens that serial walk would dominate, so a parallel kernel does it.
+  xa.combine = fused ? 1 : 0;
   size_t smem = expert_smem_bytes(sa, sb, nb);
   if (fused) {
     xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
@@ -359,6 +362,19 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   }
   e = fused ? launch_layer(xa, plan.sms, smem, stream, kPdl) : launch_expert(xa, plan.sms, smem, stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, fused ? "launch layer" : "launch expert");
+  if (!xa.combine) {
+    CombineArgs ca;
+    ca.x_in = x_in;
+    ca.x_out = x_out;
+    ca.yslot = xa.yslot;
+    ca.tok_slot = xa.tok_slot;
+    ca.topk_w = xa.topk_w;
+    ca.M = M;
+    ca.H = H;
+    ca.K = K;
+    e = launch_combine(ca, stream, kPdl);
+    if (e != cudaSuccess) return cuda_fail(e, "launch combine");
+  }
   if (g_prof.end && g_prof.cap > 0) {
     if ((rc = record(g_prof.end[g_prof.count % g_prof.cap], stream))) return rc;
     ++g_prof.count;

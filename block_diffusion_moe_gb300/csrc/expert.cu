@@ -499,8 +499,9 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
       named_bar_sync(1, 128);
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
-        const int old = atomicAdd(&p.dn_done[w.slice], 1);
-        *s.s_last = (old == rt.n_exp - 1) ? 1 : 0;
+        int last = 0;
+        if (p.combine) last = (atomicAdd(&p.dn_done[w.slice], 1) == rt.n_exp - 1) ? 1 : 0;
+        *s.s_last = last;
       }
       named_bar_sync(1, 128);
       if (*s.s_last) {

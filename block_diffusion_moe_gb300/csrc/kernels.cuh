@@ -75,6 +75,15 @@ struct PermArgs {
   int M, H, E, K;
 };
 
+struct CombineArgs {
+  const float* x_in;        // [M][H]
+  float* x_out;             // [M][H] (may equal x_in)
+  const float* yslot;       // [M*K + M][H] unweighted expert outputs
+  const int32_t* tok_slot;  // [M][K]
+  const float* topk_w;      // [M][K]
+  int M, H, K;
+};
+
 struct ExpertArgs {
   CUtensorMap tm_gu;   // routed gate/up  [E*2F][H]
   CUtensorMap tm_sgu;  // shared gate/up  [2F][H]
@@ -98,6 +107,7 @@ struct ExpertArgs {
   int* err;
   int M, H, F, E, K;
   int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
+  int combine;                     // 1: the last down unit of each slice combines; 0: k_combine does
   // fused-layer launches only (k_layer)
   const bf16* wr;      // [E][H] router
   const float* bias;   // [E] or null
@@ -142,6 +152,7 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_perm(const PermArgs& a, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 size_t layer_rt_bytes(int M, int K, int E);

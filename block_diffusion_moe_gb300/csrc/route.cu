@@ -233,7 +233,64 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- combine
+// x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t), one float4 of
+// outputs per thread; the sum runs in selection order, then the shared row,
+// then the residual (the same order as the expert kernel's own combine).
+__global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int q = a.H >> 2;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.M * q) return;
+  const int t = i / q;
+  const size_t col = static_cast<size_t>(i - t * q) * 4;
+  const size_t H = a.H;
+  const int K = a.K, MK = a.M * a.K;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    int r[8];
+    float wk[8];
+    float4 y[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool v = k0 + j < K;
+      r[j] = v ? a.tok_slot[t * K + k0 + j] : MK + t;
+      wk[j] = v ? a.topk_w[t * K + k0 + j] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = __ldcg(reinterpret_cast<const float4*>(a.yslot + static_cast<size_t>(r[j]) * H + col));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (k0 + j < K) {
+        acc.x = fmaf(wk[j], y[j].x, acc.x);
+        acc.y = fmaf(wk[j], y[j].y, acc.y);
+        acc.z = fmaf(wk[j], y[j].z, acc.z);
+        acc.w = fmaf(wk[j], y[j].w, acc.w);
+      }
+    }
+  }
+  const float4 ys = __ldcg(reinterpret_cast<const float4*>(a.yslot + static_cast<size_t>(MK + t) * H + col));
+  const float4 xi = *reinterpret_cast<const float4*>(a.x_in + static_cast<size_t>(t) * H + col);
+  acc.x += ys.x;
+  acc.y += ys.y;
+  acc.z += ys.z;
+  acc.w += ys.w;
+  float4 o;
+  o.x = xi.x + acc.x;
+  o.y = xi.y + acc.y;
+  o.z = xi.z + acc.z;
+  o.w = xi.w + acc.w;
+  *reinterpret_cast<float4*>(a.x_out + static_cast<size_t>(t) * H + col) = o;
+}
+
 // ---------------------------------------------------------------- launches
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl) {
+  const int n = a.M * (a.H >> 2);
+  return launch_kernel(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, pdl, a);
+}
+
 
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl) {
   return launch_kernel(k_embed, dim3(a.M), dim3(256), 0, s, pdl, a);
