@@ -56,7 +56,7 @@ def _expert_traffic(u_mean):
     """DRAM bytes per expert-kernel launch from the committed ncu summary
     (bytes per expert x experts per launch), if that summary was taken on the
     current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "expert_ffn_clover_layer_block32.md")
+    path = os.path.join(ROOT, "profiles", "moe_layer_fused_clover_block32.md")
     src = os.path.join(ROOT, "block_diffusion_moe_gb300", "csrc", "expert.cu")
     try:
         text = open(path).read()
