@@ -169,7 +169,7 @@ class _LazyBits:
         return self.c[e]
 
 
-def cpu_baseline(layers=None, n_layers: int = 8, head_rows: int = 8192, seed: int = 0):
+def cpu_baseline(layers=None, n_layers: int = 40, head_rows: int = 24832, seed: int = 0):
     """Oracle timing on the host cores: n_layers MoE layers of the
     32-position block plus head_rows rows of the head, scaled to one full
     step (40 layers, 248,320 rows). `layers` are resident synth layers (any
