@@ -46,6 +46,12 @@ Readings where the pages are silent (each is listed in the design doc):
 * Integer decisions are taken on float32 values, as the kernels take them:
   top-k on the float32-rounded router logits, argmax on the float32-rounded
   head logits, the threshold test on the float32-rounded probability.
+* Coreset selection (optional): the mass of an expert is the sum of the
+  softmax probabilities (not renormalised) of the slots that select it; the
+  kept set is the shortest prefix of experts sorted by mass (descending, ties
+  to the lower id) whose cumulative mass reaches top_p x total and that holds
+  at least k experts (the page says at least the top expert; k keeps every
+  token's k-way routing defined).
 * "Above 0.95" is a strict comparison. Fallback ties go to the lowest
   position, argmax ties to the lowest vocabulary id. The fallback considers
   only still-masked slots. Each block of `block` positions applies the rule
@@ -126,6 +132,57 @@ def route(xb, router_w_bits, top_k: int, router_bias=None):
     return logits, p, idx, w
 
 
+def coreset(p, idx, top_p: float) -> np.ndarray:
+    """Block coreset expert selection (Files, "The expert selection"): add up
+    each token's top-k routing probabilities per expert, sort the experts by
+    that total (ties to the lower id), keep the smallest prefix whose share of
+    the total reaches top_p, and always at least the top expert -- read here
+    as at least k experts, so that every token can still select k. Returns
+    the kept expert ids in that order.
+
+    p: float64 [M][E] softmax probabilities; idx: [M][K] each token's top-k."""
+    p = np.asarray(p, dtype=np.float64)
+    idx = np.asarray(idx, dtype=np.int64)
+    E = p.shape[1]
+    mass = np.zeros(E)
+    for t in range(idx.shape[0]):
+        for e in idx[t]:
+            mass[e] += p[t, e]
+    order = sorted(range(E), key=lambda e: (-mass[e], e))
+    total = float(np.sum(mass))
+    k = idx.shape[1]
+    kept, acc = [], 0.0
+    for e in order:
+        kept.append(e)
+        acc += mass[e]
+        if acc >= top_p * total and len(kept) >= k:
+            break
+    return np.asarray(kept, dtype=np.int32)
+
+
+def route_within(logits, allowed, top_k: int):
+    """Top-k restricted to the allowed experts (descending float32 logit, lower
+    id on ties); weights = softmax over the selected logits. A token selects
+    min(top_k, len(allowed)) experts."""
+    logits = np.asarray(logits, dtype=np.float64)
+    M, E = logits.shape
+    mask = np.zeros(E, dtype=bool)
+    mask[np.asarray(allowed, dtype=np.int64)] = True
+    k = min(top_k, int(mask.sum()))
+    r32 = logits.astype(np.float32).astype(np.float64)
+    idx = np.empty((M, k), dtype=np.int32)
+    w = np.empty((M, k))
+    for t in range(M):
+        cand = [e for e in range(E) if mask[e]]
+        cand.sort(key=lambda e: (-r32[t, e], e))
+        sel = cand[:k]
+        idx[t] = sel
+        z = logits[t, sel]
+        ez = np.exp(z - np.max(z))
+        w[t] = ez / np.sum(ez)
+    return idx, w
+
+
 def swiglu_expert(xb, gate_up_bits, down_bits) -> np.ndarray:
     """One SwiGLU expert on bf16 inputs xb [m][H].
 
@@ -139,7 +196,8 @@ def swiglu_expert(xb, gate_up_bits, down_bits) -> np.ndarray:
     return h @ bf16_to_f64(down_bits).T
 
 
-def moe_layer(x, layer: dict, top_k: int, eps: float, force_idx=None) -> dict:
+def moe_layer(x, layer: dict, top_k: int, eps: float, force_idx=None, coreset_top_p=None,
+              block: int | None = None) -> dict:
     """One pre-norm MoE sublayer: x_out = x + sum_k w_k E_{i_k}(xb) + S(xb).
 
     layer: dict with router_w, gate_up, down, sh_gate_up, sh_down (uint16 bit
@@ -151,6 +209,20 @@ def moe_layer(x, layer: dict, top_k: int, eps: float, force_idx=None) -> dict:
     x = np.asarray(x, dtype=np.float64)
     xb = round_to_bf16(rms_norm(x, eps))
     logits, p, idx, w = route(xb, layer["router_w"], top_k, layer.get("router_bias"))
+    kept = []
+    if coreset_top_p is not None:
+        # Files, "The expert selection": the block's coreset, then every token
+        # routes within it (denoising passes only).
+        M = x.shape[0]
+        blk = block or M
+        new_idx = np.empty_like(idx)
+        new_w = np.empty_like(w)
+        for b0 in range(0, M, blk):
+            sl = slice(b0, min(M, b0 + blk))
+            keep = coreset(p[sl], idx[sl], coreset_top_p)
+            kept.append(keep)
+            new_idx[sl], new_w[sl] = route_within(logits[sl], keep, top_k)
+        idx, w = new_idx, new_w
     if force_idx is not None:
         idx = np.asarray(force_idx, dtype=np.int32)
         psel = np.take_along_axis(p, idx.astype(np.int64), axis=1)
@@ -161,7 +233,7 @@ def moe_layer(x, layer: dict, top_k: int, eps: float, force_idx=None) -> dict:
         o = swiglu_expert(xb[toks], layer["gate_up"][int(e)], layer["down"][int(e)])
         y[toks] += w[toks, ks][:, None] * o
     y += swiglu_expert(xb, layer["sh_gate_up"], layer["sh_down"])
-    return {"x_out": x + y, "idx": idx, "w": w, "logits": logits, "p": p, "xb": xb}
+    return {"x_out": x + y, "idx": idx, "w": w, "logits": logits, "p": p, "xb": xb, "coreset": kept}
 
 
 def head_logits(x, head_bits, eps: float, alpha=None, chunk: int = 16384) -> np.ndarray:

@@ -352,3 +352,92 @@ def test_embed_closed_form():
     x = O.embed(tokens, tb, ctx)
     want = (tokens / 4.0 + np.arange(4) / 8.0)[:, None] * np.ones((1, H))
     assert np.array_equal(x, want)
+
+
+# ------------------------------------------------------------------ coreset
+
+
+def test_coreset_hand_example():
+    """Three tokens, k = 2. Masses (summed top-k probabilities): e0 0.5,
+    e1 0.3, e2 0.1, e3 0.1. top_p 0.9 keeps {0, 1, 2} (0.5, 0.8, 0.9);
+    0.95 keeps all four; 0.5 keeps {0, 1} (at least k = 2). e2 and e3 tie at
+    0.1 and e2 (lower id) comes first."""
+    p = np.zeros((3, 6))
+    p[0, [0, 1]] = [0.3, 0.2]
+    p[1, [0, 2]] = [0.2, 0.1]
+    p[2, [1, 3]] = [0.1, 0.1]
+    idx = np.array([[0, 1], [0, 2], [1, 3]])
+    assert list(O.coreset(p, idx, 0.9)) == [0, 1, 2]
+    assert list(O.coreset(p, idx, 0.95)) == [0, 1, 2, 3]
+    assert list(O.coreset(p, idx, 0.5)) == [0, 1]
+    assert list(O.coreset(p, idx, 0.0)) == [0, 1]
+
+
+def test_coreset_top_p_one_is_identity():
+    """top_p = 1 keeps every expert any token selected, so no token re-routes."""
+    d = synth.TINY
+    L = layer_to_oracle(_tiny_layer(4))
+    x = synth.make_x(d, 8, 4).numpy()
+    a = O.moe_layer(x, L, d.top_k, d.rms_eps)
+    b = O.moe_layer(x, L, d.top_k, d.rms_eps, coreset_top_p=1.0, block=8)
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.allclose(a["x_out"], b["x_out"], rtol=1e-12, atol=1e-12)
+
+
+def test_coreset_invariants_clover_shape():
+    c = synth.CLOVER
+    wr = bits(synth.make_router(c, 5, 0))
+    for blk in range(4):
+        x = synth.make_x(c, 32, 50 + blk).numpy()
+        xb = O.round_to_bf16(O.rms_norm(x, c.rms_eps))
+        logits, p, idx, w = O.route(xb, wr, c.top_k)
+        keep = O.coreset(p, idx, 0.9)
+        union = set(np.unique(idx).tolist())
+        assert set(keep.tolist()) <= union
+        assert len(keep) >= c.top_k
+        mass = np.zeros(c.n_experts)
+        for t in range(32):
+            for e in idx[t]:
+                mass[e] += p[t, e]
+        cum = mass[keep].sum()
+        assert cum >= 0.9 * mass.sum()
+        assert cum - mass[keep[-1]] < 0.9 * mass.sum()          # minimal
+        assert np.all(np.diff(mass[keep]) <= 0)                 # kept by mass
+        ki, kw = O.route_within(logits, keep, c.top_k)
+        assert set(np.unique(ki).tolist()) <= set(keep.tolist())
+        assert np.allclose(kw.sum(axis=1), 1.0)
+        for t in range(32):                                     # untouched tokens keep their routing
+            if set(idx[t].tolist()) <= set(keep.tolist()):
+                assert set(ki[t].tolist()) == set(idx[t].tolist())
+                assert np.allclose(np.sort(kw[t]), np.sort(w[t]))
+
+
+def test_coreset_shrinks_the_union_like_the_pages():
+    """Files, 'The expert selection': under independent routing a 32-token
+    block touches 163.4 experts and the selector at 0.9 keeps 126.7,
+    re-routing about 1.1 of a token's 8 slots (their synthetic logits; the
+    noise model is not given, so the check is a band; these inputs give
+    127.3 kept and 1.11 re-routed)."""
+    c = synth.CLOVER
+    wr = bits(synth.make_router(c, 6, 0))
+    kept, rerouted = [], []
+    for b in range(12):
+        x = synth.make_x(c, 32, 200 + b).numpy()
+        xb = O.round_to_bf16(O.rms_norm(x, c.rms_eps))
+        logits, p, idx, w = O.route(xb, wr, c.top_k)
+        keep = O.coreset(p, idx, 0.9)
+        ki, _ = O.route_within(logits, keep, c.top_k)
+        kept.append(len(keep))
+        rerouted.append(np.mean([len(set(idx[t]) - set(ki[t])) for t in range(32)]))
+    assert abs(np.mean(kept) - 126.7) < 6, np.mean(kept)
+    assert abs(np.mean(rerouted) - 1.1) < 0.3, np.mean(rerouted)
+
+
+def test_route_within_planted_ties_and_weights():
+    logits = np.array([[1.0, 2.0, 2.0, 0.5, 3.0]])
+    idx, w = O.route_within(logits, [1, 2, 3], 2)      # 4 is not allowed
+    assert list(idx[0]) == [1, 2]                        # tie at 2.0 -> lower id first
+    assert np.allclose(w[0], [0.5, 0.5])
+    idx, w = O.route_within(logits, [0, 3, 2], 2)
+    assert list(idx[0]) == [2, 0]
+    assert w[0, 0] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-14)
