@@ -248,7 +248,10 @@ WORKLOADS = {
     "head": "LM head + low-confidence unmask: 32 positions x hidden 2,048 into the untied 248,320-row head",
     "zipf": "batched and skewed routing: 8 blocks x 32 positions (256 tokens) through 40 Clover-shaped MoE "
             "layers + head, router biased to Zipf(1.2) expert popularity",
+    "coreset": "full block denoising step as 'step' with the block coreset expert selection (top_p 0.9) in every "
+               "MoE layer",
 }
+CORESET_TOP_P = 0.9
 
 
 def run_ours(args):
@@ -261,18 +264,20 @@ def run_ours(args):
     seed = 1000 + rank
     kind = args.workload
     n_pos = 256 if kind == "zipf" else M
-    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "layer": 1, "head": 0}[kind]
+    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "layer": 1, "head": 0}[kind]
+    full = kind in ("step", "zipf", "coreset")
+    top_p = CORESET_TOP_P if kind == "coreset" else 0.0
     zipf = 1.2 if kind == "zipf" else None
     layers = [synth.make_layer(D, seed, l, dev, zipf_s=zipf) for l in range(n_layers)]
     head_w = synth.make_head(D, seed, dev) if kind != "layer" else None
-    embed = synth.make_embed(D, seed, dev) if kind in ("step", "zipf") else None
-    model = clover.Model(D, layers, embed, head_w) if kind in ("step", "zipf") else None
+    embed = synth.make_embed(D, seed, dev) if full else None
+    model = clover.Model(D, layers, embed, head_w, coreset_top_p=top_p) if full else None
     ctx = synth.make_ctx(D, n_pos, seed, dev)
     tokens, masked = synth.masked_block(D, n_pos, dev)
     stream = torch.cuda.current_stream(dev)
     x_fixed = synth.make_x(D, n_pos, seed, dev)
     x_out = torch.empty_like(x_fixed)
-    if kind in ("step", "zipf"):
+    if full:
         ws = clover.workspace(clover.denoise_workspace_bytes(D, n_pos), dev)
     elif kind == "layer":
         ws = clover.workspace(clover.moe_workspace_bytes(D, n_pos), dev)
@@ -286,7 +291,7 @@ def run_ours(args):
     steps_in_block = [0]
 
     def step():
-        if kind in ("step", "zipf"):
+        if full:
             if steps_in_block[0] == M:
                 reset()
                 steps_in_block[0] = 0
@@ -369,7 +374,7 @@ def run_ours(args):
                 reset()
             x.copy_(model.embed[tokens.long()].float() + ctx)
             for L in layers:
-                x, idx, _ = clover.moe_block_step(D, L, x, x_out=x, ws=moe_ws)
+                x, idx, _ = clover.moe_block_step(D, L, x, x_out=x, ws=moe_ws, coreset_top_p=top_p)
                 u_per_launch.append(int(torch.unique(idx).numel()))
             clover.lmhead_unmask(D, head_w, x, tokens, masked, block=M, ws=head_ws)
         torch.cuda.synchronize()
@@ -394,14 +399,14 @@ def run_ours(args):
     _barrier(dist)
     t0 = time.perf_counter()
     for s_ in range(args.steps):
-        if kind in ("step", "zipf") and s_ > 0 and s_ % M == 0:
+        if full and s_ > 0 and s_ % M == 0:
             h_tokens.fill_(D.mask_id)
             h_masked.fill_(1)
         d_in.copy_(h_in, non_blocking=True)
         if kind != "layer":
             tokens.copy_(h_tokens, non_blocking=True)
             masked.copy_(h_masked, non_blocking=True)
-        if kind in ("step", "zipf"):
+        if full:
             clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
         else:
             step()
@@ -411,7 +416,7 @@ def run_ours(args):
             o_tokens.copy_(tokens, non_blocking=True)
             o_masked.copy_(masked, non_blocking=True)
         torch.cuda.synchronize()
-        if kind in ("step", "zipf"):
+        if full:
             h_tokens.copy_(o_tokens)
             h_masked.copy_(o_masked)
     e2e_s = time.perf_counter() - t0
@@ -431,7 +436,7 @@ def run_ours(args):
     # <= 32 positions: one fused launch per layer; more: route, perm, experts, combine
     per_layer = 1 if n_pos <= 32 else 4
     launches_per_step = {"step": 1 + per_layer * n_layers + 2, "zipf": 1 + per_layer * n_layers + 2,
-                         "layer": per_layer, "head": 2}[kind]
+                         "coreset": 1 + per_layer * n_layers + 2, "layer": per_layer, "head": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
                    else "k_layer (routing + grouped SwiGLU experts + combine, one launch per MoE layer)"
                    if n_pos <= 32 else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")

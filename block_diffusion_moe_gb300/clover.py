@@ -34,7 +34,7 @@ class CloverError(RuntimeError):
 class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("vocab", ctypes.c_int32), ("mask_id", ctypes.c_int32),
-                ("rms_eps", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("coreset_top_p", ctypes.c_float)]
 
 
 class MoeLayer(ctypes.Structure):
@@ -113,8 +113,8 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def make_dims(d: synth.Dims) -> Dims:
-    return Dims(d.hidden, d.n_experts, d.top_k, d.d_ff, d.vocab, d.mask_id, d.rms_eps)
+def make_dims(d: synth.Dims, coreset_top_p: float = 0.0) -> Dims:
+    return Dims(d.hidden, d.n_experts, d.top_k, d.d_ff, d.vocab, d.mask_id, d.rms_eps, coreset_top_p)
 
 
 def make_layer(L: synth.Layer) -> MoeLayer:
@@ -146,7 +146,7 @@ def denoise_workspace_bytes(d: synth.Dims, max_tokens: int) -> int:
 
 
 def moe_block_step(d: synth.Dims, layer: synth.Layer, x_in: torch.Tensor, x_out: torch.Tensor | None = None,
-                   ws: torch.Tensor | None = None, with_topk: bool = True, stream=None):
+                   ws: torch.Tensor | None = None, with_topk: bool = True, stream=None, coreset_top_p: float = 0.0):
     M = x_in.shape[0]
     if x_out is None:
         x_out = torch.empty_like(x_in)
@@ -154,7 +154,7 @@ def moe_block_step(d: synth.Dims, layer: synth.Layer, x_in: torch.Tensor, x_out:
         ws = workspace(moe_workspace_bytes(d, M), x_in.device)
     idx = torch.empty((M, d.top_k), dtype=torch.int32, device=x_in.device) if with_topk else None
     w = torch.empty((M, d.top_k), dtype=torch.float32, device=x_in.device) if with_topk else None
-    dims = make_dims(d)
+    dims = make_dims(d, coreset_top_p)
     lay = make_layer(layer)
     _check(lib().clover_moe_block_step(ctypes.byref(dims), ctypes.byref(lay), _ptr(x_in), _ptr(x_out), _ptr(idx),
                                        _ptr(w), M, _ptr(ws), ws.numel(), _stream(stream)))
@@ -184,13 +184,13 @@ class Model:
     """Device-resident weights of a stack of MoE sublayers plus embedding and
     head, with the ctypes layer array the denoise entry points take."""
 
-    def __init__(self, d: synth.Dims, layers, embed, head_w):
+    def __init__(self, d: synth.Dims, layers, embed, head_w, coreset_top_p: float = 0.0):
         self.d = d
         self.layers = list(layers)
         self.embed = embed
         self.head_w = head_w
         self.c_layers = (MoeLayer * max(1, len(self.layers)))(*[make_layer(L) for L in self.layers])
-        self.c_dims = make_dims(d)
+        self.c_dims = make_dims(d, coreset_top_p)
 
 
 def denoise_step(m: Model, ctx, tokens, masked, logit_scale=None, threshold: float = 0.95, block: int = 32,

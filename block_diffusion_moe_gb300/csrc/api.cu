@@ -55,7 +55,8 @@ enum CtrlWord : int {
 };
 
 struct MoeLayout {
-  size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, logits, xg, hbuf, yslot, bytes;
+  size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, topk_p, rr_idx, rr_w, logits, xg,
+      hbuf, yslot, bytes;
 };
 
 MoeLayout moe_layout(const clover_dims& d, int M) {
@@ -77,6 +78,9 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
   L.tok_slot = take(M * K * 4);
   L.topk_idx = take(M * K * 4);
   L.topk_w = take(M * K * 4);
+  L.topk_p = take(M * K * 4);
+  L.rr_idx = take(M * K * 4);
+  L.rr_w = take(M * K * 4);
   L.logits = take(static_cast<size_t>(M) * E * 4);
   L.xg = take(R * H * 2);
   L.hbuf = take(R * F * 2);
@@ -136,6 +140,8 @@ int check_dims(const clover_dims* d) {
   if (d->vocab < 2) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "vocab=%d < 2", d->vocab);
   if (d->mask_id < 0 || d->mask_id >= d->vocab)
     return fail(CLOVER_ERR_INVALID_ARG, "mask_id=%d outside [0, vocab)", d->mask_id);
+  if (!(d->coreset_top_p >= 0.f && d->coreset_top_p <= 1.f))
+    return fail(CLOVER_ERR_INVALID_ARG, "coreset_top_p=%g outside [0, 1]", d->coreset_top_p);
   return CLOVER_OK;
 }
 
@@ -248,6 +254,8 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
 
   // The fused kernel gives each CTA at most kRouteExperts router rows.
   const bool fused = M <= kLayerMaxTokens && (E + plan.sms - 1) / plan.sms <= kRouteExperts;
+  if (d.coreset_top_p > 0.f && !fused)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "the block coreset needs at most %d positions", kLayerMaxTokens);
   cudaError_t e = cudaSuccess;
   PermArgs pa;
   memset(&pa, 0, sizeof(pa));
@@ -351,6 +359,10 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     xa.tg_ctr = ctrl + kCtrlTokenGroups;
     xa.pub_idx = topk_idx;
     xa.pub_w = topk_w;
+    xa.pub_p = reinterpret_cast<float*>(data + L.topk_p);
+    xa.pub2_idx = reinterpret_cast<int32_t*>(data + L.rr_idx);
+    xa.pub2_w = reinterpret_cast<float*>(data + L.rr_w);
+    xa.coreset_top_p = d.coreset_top_p;
     xa.out_idx = out_idx;
     xa.out_w = out_w;
     xa.eps = d.rms_eps;
@@ -465,6 +477,8 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
   if (!aligned16(embed) || !aligned16(ctx) || !aligned16(head_w))
     return fail(CLOVER_ERR_INVALID_ARG, "embed/ctx/head_w must be 16-byte aligned");
   if (block < 1 || M % block != 0) return fail(CLOVER_ERR_INVALID_ARG, "block=%d must divide M=%d", block, M);
+  if (dims->coreset_top_p > 0.f && block != M)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "the block coreset needs one block per call (block == M)");
   if (!(threshold == threshold)) return fail(CLOVER_ERR_INVALID_ARG, "threshold is NaN");
   for (int i = 0; i < n_layers; ++i)
     if ((rc = check_layer(&layers[i], i))) return rc;

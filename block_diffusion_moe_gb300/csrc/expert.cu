@@ -727,6 +727,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
         if (lane < K) {
           p.pub_idx[t * K + lane] = sel.e;
           p.pub_w[t * K + lane] = sel.w;
+          p.pub_p[t * K + lane] = sel.p;
         }
       }
       if (threadIdx.x == 0) p.tg_ctr[tg] = 0;
@@ -740,11 +741,91 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
   if (!grid_barrier(p.bar_ctr, p.bar_gen, p.err)) *s.abort = 1u;
   if (st) st[3] = global_ns();
 
+  const int32_t* fin_idx = p.pub_idx;
+  const float* fin_w = p.pub_w;
+  if (p.coreset_top_p > 0.f) {
+    // Block coreset (the M tokens are one block): every CTA computes the same
+    // kept set from the published first-pass selections, CTA t re-routes
+    // token t within it, and a second barrier publishes the result.
+    float* s_mass = reinterpret_cast<float*>(s_nact + 1);  // [E]
+    float* s_smass = s_mass + E;                             // [E] masses in kept order
+    int* s_sid = reinterpret_cast<int*>(s_smass + E);        // [E] expert ids in kept order
+    uint32_t* s_allow = reinterpret_cast<uint32_t*>(s_sid + E);  // [8]
+    for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+      const int e = __ldcg(p.pub_idx + i);
+      s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
+      s_w[i] = __ldcg(p.pub_p + i);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
+    if (threadIdx.x < 8) s_allow[threadIdx.x] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < MK; i += blockDim.x) atomicOr(&s_mask[s_idx[i]], 1u << (i / K));
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {  // mass: probabilities in token order
+      float m = 0.f;
+      for (uint32_t b = s_mask[e]; b != 0u; b &= b - 1u) {
+        const int t = __ffs(b) - 1;
+        for (int k = 0; k < K; ++k)
+          if (s_idx[t * K + k] == e) m += s_w[t * K + k];
+      }
+      s_mass[e] = m;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {  // rank by (mass desc, id asc)
+      const float me = s_mass[e];
+      int r = 0;
+      for (int e2 = 0; e2 < E; ++e2) {
+        const float m2 = s_mass[e2];
+        r += (m2 > me || (m2 == me && e2 < e)) ? 1 : 0;
+      }
+      s_smass[r] = me;
+      s_sid[r] = e;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // total in kept order, then the shortest prefix reaching top_p x total
+      // that holds at least K experts
+      float total = 0.f;
+      for (int c0 = 0; c0 < E; c0 += 32) total += warp_sum_f(c0 + lane < E ? s_smass[c0 + lane] : 0.f);
+      const float target = p.coreset_top_p * total;
+      float carry = 0.f;
+      int cut = E - 1;
+      for (int c0 = 0; c0 < E; c0 += 32) {
+        float v = c0 + lane < E ? s_smass[c0 + lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float n = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += n;
+        }
+        const float cum = carry + v;
+        const unsigned hit = __ballot_sync(0xffffffffu, c0 + lane < E && cum >= target && c0 + lane >= K - 1);
+        if (hit) {
+          cut = c0 + __ffs(hit) - 1;
+          break;
+        }
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      for (int r = lane; r <= cut; r += 32) atomicOr(&s_allow[s_sid[r] >> 5], 1u << (s_sid[r] & 31));
+    }
+    __syncthreads();
+    if (static_cast<int>(blockIdx.x) < M && warp == 0) {
+      const int t = blockIdx.x;
+      const TopkSel sel = warp_topk(p.logits + static_cast<size_t>(t) * E, E, K, lane, s_allow);
+      if (lane < K) {
+        p.pub2_idx[t * K + lane] = sel.e;
+        p.pub2_w[t * K + lane] = sel.w;
+      }
+    }
+    if (!grid_barrier(p.bar_ctr, p.bar_gen, p.err)) *s.abort = 1u;
+    fin_idx = p.pub2_idx;
+    fin_w = p.pub2_w;
+  }
+
   // Phase 2: every CTA builds the same permutation from the published top-k.
   for (int i = threadIdx.x; i < MK; i += blockDim.x) {
-    const int e = __ldcg(p.pub_idx + i);
+    const int e = __ldcg(fin_idx + i);
     s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-    s_w[i] = __ldcg(p.pub_w + i);
+    s_w[i] = __ldcg(fin_w + i);
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
   __syncthreads();
@@ -810,7 +891,7 @@ size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {
          256;
 }
 
-size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(3 * M * K + 4 * E + 4) * 4; }
+size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(3 * M * K + 7 * E + 16) * 4; }
 
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
   cudaError_t e = cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -118,6 +118,10 @@ struct ExpertArgs {
   int* tg_ctr;         // [ceil(M/8)] token-group arrival counters (zero between launches)
   int32_t* pub_idx;    // [M][K] top-k ids published by the token groups' last CTAs
   float* pub_w;        // [M][K] top-k weights, likewise
+  float* pub_p;        // [M][K] full-softmax probability of each selection (coreset mass)
+  int32_t* pub2_idx;   // [M][K] selections after the coreset re-routing
+  float* pub2_w;       // [M][K] their weights
+  float coreset_top_p; // 0: no coreset
   int32_t* out_idx;    // optional [M][K] copies for the caller
   float* out_w;
   float eps;

@@ -126,20 +126,37 @@ __device__ __forceinline__ float warp_router_dots(const float* xr, float rstd, c
 }
 
 struct TopkSel {
-  int e;
-  float w;
+  int e;    // selected expert
+  float w;  // weight: softmax over the selected logits
+  float p;  // softmax probability over all E logits (coreset mass)
 };
 
 // One warp, one token: top-k of E (<= 256) logits by descending value, the
-// lower expert id first on ties; weights = softmax over the selected logits
-// (= the top-k probabilities renormalised). Lane k (< K) receives selection k
-// and its weight.
-__device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int K, int lane) {
+// lower expert id first on ties, restricted to the experts whose bit is set in
+// `allowed` (8 words; null = all). Weights = softmax over the selected
+// logits (= the top-k probabilities renormalised). Lane k (< K) receives
+// selection k, its weight and its probability under the softmax over all E.
+__device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int K, int lane,
+                                             const uint32_t* allowed = nullptr) {
   float v[8];
+  float all_max = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
     v[i] = (e < E) ? __ldcg(logits_row + e) : -INFINITY;
+    all_max = fmaxf(all_max, v[i]);
+  }
+  all_max = warp_max_f(all_max);
+  float all_sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) all_sum += (lane + 32 * i < E) ? expf(v[i] - all_max) : 0.f;
+  all_sum = warp_sum_f(all_sum);
+  if (allowed != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((allowed[e >> 5] >> (e & 31)) & 1u)) v[i] = -INFINITY;
+    }
   }
   float my_v = -INFINITY;
   int my_e = 0;
@@ -179,6 +196,7 @@ __device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int
   TopkSel r;
   r.e = my_e;
   r.w = ex / sum;
+  r.p = (lane < K) ? expf(my_v - all_max) / all_sum : 0.f;
   return r;
 }
 

@@ -55,9 +55,17 @@ typedef struct CUstream_st* clover_stream_t;
 typedef struct CUevent_st* clover_event_t;
 
 /* Model dimensions. Files, "What Clover is": hidden 2048, n_experts 256,
- * top_k 8, d_ff 512, vocab 248320, mask_id 151669. rms_eps is the epsilon of
- * the unit-weight RMSNorm placed before each MoE sublayer and before the head
- * (a reading; the pages give no norm). */
+ * top_k 8, d_ff 512, vocab 248320, mask_id 151669; moe_block_coreset_enabled
+ * with top_p 0.9. rms_eps is the epsilon of the unit-weight RMSNorm placed
+ * before each MoE sublayer and before the head (a reading; the pages give no
+ * norm).
+ * coreset_top_p: 0 disables the block coreset; a value in (0, 1] enables it
+ * (Files, "The expert selection"): per block, each expert's mass is the sum of
+ * the softmax probabilities of the slots that select it; the kept set is the
+ * shortest prefix of experts by mass (descending, lower id first) whose
+ * cumulative mass reaches coreset_top_p x total and that holds at least
+ * top_k experts; every token then takes its top_k within the kept set. The
+ * coreset is available for calls of at most 32 positions forming one block. */
 typedef struct {
     int32_t hidden;    /* H */
     int32_t n_experts; /* E, routed experts per layer */
@@ -66,6 +74,7 @@ typedef struct {
     int32_t vocab;     /* V */
     int32_t mask_id;   /* mask token id; never predicted */
     float rms_eps;
+    float coreset_top_p; /* 0 = off */
 } clover_dims;
 
 /* One MoE layer's weights (device pointers). Files, "What Clover is". */

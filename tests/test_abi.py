@@ -46,7 +46,7 @@ def test_version(lib):
 def _dims(**kw):
     d = synth.CLOVER
     base = dict(hidden=d.hidden, n_experts=d.n_experts, top_k=d.top_k, d_ff=d.d_ff, vocab=d.vocab,
-                mask_id=d.mask_id, rms_eps=d.rms_eps)
+                mask_id=d.mask_id, rms_eps=d.rms_eps, coreset_top_p=0.0)
     base.update(kw)
     return C.Dims(**base)
 
@@ -75,6 +75,7 @@ def test_workspace_sizes(lib):
     (dict(top_k=33), C.ERR_UNSUPPORTED_SHAPE),
     (dict(mask_id=248320), C.ERR_INVALID_ARG),
     (dict(hidden=0), C.ERR_INVALID_ARG),
+    (dict(coreset_top_p=1.5), C.ERR_INVALID_ARG),
 ])
 def test_bad_dims_rejected_on_host(lib, kw, code):
     d = _dims(**kw)
