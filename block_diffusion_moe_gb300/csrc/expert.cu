@@ -355,6 +355,58 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uin
 
 // Sums the weighted expert rows of one 128-wide hidden slice into the
 // residual stream: x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t).
+// One token's combined output column block (see combine_slice); the loads of
+// up to 8 selections are issued before any is used.
+struct CombineAcc {
+  float4 acc, ys, xi;
+};
+
+__device__ __forceinline__ void combine_loads(const ExpertArgs& p, const Rt& rt, int t, size_t col, int k0,
+                                              int r[8], float wk[8], float4 y[8]) {
+  const int K = p.K, MK = p.M * p.K;
+  const size_t H = p.H;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool v = k0 + i < K;
+    r[i] = v ? rt.tok_slot[t * K + k0 + i] : MK + t;
+    wk[i] = v ? rt.topk_w[t * K + k0 + i] : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    y[i] = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(r[i]) * H + col));
+}
+
+__device__ __forceinline__ void combine_accumulate(float4& acc, const float wk[8], const float4 y[8], int k0,
+                                                   int K) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (k0 + i < K) {
+      acc.x = fmaf(wk[i], y[i].x, acc.x);
+      acc.y = fmaf(wk[i], y[i].y, acc.y);
+      acc.z = fmaf(wk[i], y[i].z, acc.z);
+      acc.w = fmaf(wk[i], y[i].w, acc.w);
+    }
+  }
+}
+
+__device__ __forceinline__ void combine_store(const ExpertArgs& p, int t, size_t col, float4 acc, float4 ys,
+                                              float4 xi) {
+  acc.x += ys.x;
+  acc.y += ys.y;
+  acc.z += ys.z;
+  acc.w += ys.w;
+  float4 o;
+  o.x = xi.x + acc.x;
+  o.y = xi.y + acc.y;
+  o.z = xi.z + acc.z;
+  o.w = xi.w + acc.w;
+  *reinterpret_cast<float4*>(p.x_out + static_cast<size_t>(t) * p.H + col) = o;
+}
+
+// Sums the weighted expert rows of one 128-wide hidden slice into the
+// residual stream: x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t),
+// selections in order, then the shared row, then the residual. Two tokens
+// are in flight per thread.
 __device__ void combine_slice(const ExpertArgs& p, const Rt& rt, int j, int etid) {
   const int c4 = (etid & 31) * 4;
   const int g = etid >> 5;
@@ -362,45 +414,28 @@ __device__ void combine_slice(const ExpertArgs& p, const Rt& rt, int j, int etid
   const size_t col = static_cast<size_t>(j) * 128 + c4;
   const int MK = p.M * p.K;
   const int K = p.K;
-  for (int t = g; t < p.M; t += 4) {
+  for (int t = g; t < p.M; t += 8) {
+    const int t2 = t + 4;
+    const bool two = t2 < p.M;
     const float4 ys = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t) * H + col));
     const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * H + col);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    // Selections in groups of 8: every load of a group is issued before any
-    // is used (the sum still runs in selection order).
-    for (int k0 = 0; k0 < K; k0 += 8) {
-      int r[8];
-      float wk[8];
-      float4 y[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const bool v = k0 + i < K;
-        r[i] = v ? rt.tok_slot[t * K + k0 + i] : MK + t;
-        wk[i] = v ? rt.topk_w[t * K + k0 + i] : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        y[i] = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(r[i]) * H + col));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (k0 + i < K) {
-          acc.x = fmaf(wk[i], y[i].x, acc.x);
-          acc.y = fmaf(wk[i], y[i].y, acc.y);
-          acc.z = fmaf(wk[i], y[i].z, acc.z);
-          acc.w = fmaf(wk[i], y[i].w, acc.w);
-        }
-      }
+    float4 ys2 = make_float4(0.f, 0.f, 0.f, 0.f), xi2 = ys2;
+    if (two) {
+      ys2 = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t2) * H + col));
+      xi2 = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t2) * H + col);
     }
-    acc.x += ys.x;
-    acc.y += ys.y;
-    acc.z += ys.z;
-    acc.w += ys.w;
-    float4 o;
-    o.x = xi.x + acc.x;
-    o.y = xi.y + acc.y;
-    o.z = xi.z + acc.z;
-    o.w = xi.w + acc.w;
-    *reinterpret_cast<float4*>(p.x_out + static_cast<size_t>(t) * H + col) = o;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      int r[8], r2[8];
+      float wk[8], wk2[8];
+      float4 y[8], y2[8];
+      combine_loads(p, rt, t, col, k0, r, wk, y);
+      if (two) combine_loads(p, rt, t2, col, k0, r2, wk2, y2);
+      combine_accumulate(acc, wk, y, k0, K);
+      if (two) combine_accumulate(acc2, wk2, y2, k0, K);
+    }
+    combine_store(p, t, col, acc, ys, xi);
+    if (two) combine_store(p, t2, col, acc2, ys2, xi2);
   }
 }
 
@@ -497,6 +532,7 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
       tc_fence_before();
       __threadfence();
       named_bar_sync(1, 128);
+      if (etid == 0 && p.stamps != nullptr) atomicMax(p.stamps + 6, global_ns());
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
         int last = 0;
@@ -718,6 +754,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
     }
     __threadfence();
     __syncthreads();
+    if (threadIdx.x == 0 && p.stamps != nullptr) atomicMax(p.stamps + 7, global_ns());
     if (threadIdx.x == 0) s_tg_last = (atomicAdd(&p.tg_ctr[tg], 1) == n_eg - 1) ? 1 : 0;
     __syncthreads();
     if (s_tg_last) {
@@ -829,10 +866,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
   __syncthreads();
-  if (st) st[6] = global_ns();
   for (int i = threadIdx.x; i < MK; i += blockDim.x) atomicOr(&s_mask[s_idx[i]], 1u << (i / K));
   __syncthreads();
-  if (st) st[7] = global_ns();
   if (warp == 0) {  // counts, offsets and the active list, 32 experts at a time
     int base_off = 0, base_act = 0;
     for (int e0c = 0; e0c < E; e0c += 32) {

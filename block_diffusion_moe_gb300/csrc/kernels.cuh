@@ -127,7 +127,8 @@ struct ExpertArgs {
   float eps;
   unsigned long long* stamps;  // optional phase timestamps (diagnostics): [0] start, [1] after the
                                // dependency wait, [2] last CTA done with phase 1, [3] after the
-                               // barrier, [4] routing done, [5] last CTA done
+                               // barrier, [4] routing done, [5] last CTA done, [6] last down
+                               // unit's outputs stored
 };
 
 struct HeadArgs {
