@@ -275,6 +275,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     ra.logits = reinterpret_cast<float*>(data + L.logits);
     ra.xn_rows = xg + static_cast<size_t>(MK) * H;
     ra.tg_ctr = ctrl + kCtrlTokenGroups;
+    ra.err = ctrl + kCtrlErr;
     ra.topk_idx = topk_idx;
     ra.topk_w = topk_w;
     ra.M = M;

@@ -14,6 +14,11 @@ using bf16 = __nv_bfloat16;
 // Routing kernel tiling: 8 experts x 8 tokens (one per warp) per CTA.
 constexpr int kRouteExperts = 8;
 constexpr int kRouteTokens = 8;
+// The standalone routing kernel (more than 32 tokens): one CTA per tile of 16
+// tokens x 32 experts, contracted over the hidden size in chunks of 2048.
+constexpr int kRouteTileTokens = 16;
+constexpr int kRouteTileExperts = 32;
+constexpr int kRouteChunk = 2048;
 constexpr int kMaxTokens = 256;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
@@ -51,7 +56,8 @@ struct RouteArgs {
   const float* bias;    // [E] or null
   float* logits;        // [M][E]
   bf16* xn_rows;        // [M][H] normed input (the shared expert's rows of the gathered buffer)
-  int* tg_ctr;          // [ceil(M/8)] arrival counters, zero between launches
+  int* tg_ctr;          // [ceil(M/16)] arrival counters, zero between launches
+  int* err;             // error bits (kErr*)
   int32_t* topk_idx;    // [M][K]
   float* topk_w;        // [M][K]
   int M, H, E, K;

@@ -8,6 +8,8 @@
 // step 1 (the block re-enters with mask-token embeddings until committed).
 #include <math.h>
 
+#include <algorithm>
+
 #include "kernels.cuh"
 #include "launch.cuh"
 #include "routing.cuh"
@@ -67,48 +69,191 @@ __global__ void __launch_bounds__(256) k_rmsnorm(NormArgs a) {
 }
 
 // ------------------------------------------------------------------ route
-// Grid (ceil(E/8), ceil(M/8)). Each CTA normalises its 8 tokens (one warp
-// per token), writes the bf16 normed rows (expert group 0 only) and the
-// router logits of its 8 experts. The last CTA to finish a token group then
-// takes softmax top-k for those tokens: selection by descending logit with
-// the lower expert id first on ties, weights = softmax over the selected
-// logits (= top-k probabilities renormalised to sum to one).
-__global__ void __launch_bounds__(256) k_route(RouteArgs a) {
+// Routing for more than 32 tokens. Grid (ceil(E/32), ceil(M/16)): each CTA
+// owns a tile of 16 tokens x 32 experts.
+//  1. Its 32 router rows are bulk-copied into shared memory before the
+//     dependency wait (they do not depend on earlier kernels).
+//  2. Each warp normalises two token rows (row kept in registers for
+//     H <= 2048): xn = bf16(x * rstd), rstd = 1 / sqrt(mean(x^2) + eps),
+//     into shared memory, and expert tile 0 also writes them to xn_rows.
+//  3. The tile's logits are one bf16 contraction with fp32 accumulation on
+//     the warp tensor cores (mma m16n8k16: tokens x experts, the hidden size
+//     split eight ways across the warps, the partials summed in warp order).
+//  4. The last CTA to finish a token tile takes softmax top-k for its tokens:
+//     selection by descending logit with the lower expert id first on ties,
+//     weights = softmax over the selected logits (= top-k probabilities
+//     renormalised to sum to one).
+// H above 2048 is contracted in chunks of 2048 columns.
+__global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  bf16* w = reinterpret_cast<bf16*>(smem);  // [8][H]
+  const int H = a.H, E = a.E, M = a.M;
+  const int Hc = min(H, kRouteChunk);
+  const int ld = Hc + 8;  // padded row stride (elements): fragment loads hit 32 distinct banks
+  bf16* s_w = reinterpret_cast<bf16*>(smem);                                      // [32][ld]
+  bf16* s_x = s_w + kRouteTileExperts * ld;                                        // [16][ld]
+  float* s_part = reinterpret_cast<float*>(s_x + kRouteTileTokens * ld);          // [8][16][32]
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(s_part + 8 * kRouteTileTokens * kRouteTileExperts + 16);
   __shared__ int s_last;
+  __shared__ int s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int e0 = blockIdx.x * kRouteExperts;
-  const int ne = min(kRouteExperts, a.E - e0);
-  const int t0 = blockIdx.y * kRouteTokens;
-  const int t1 = min(a.M, t0 + kRouteTokens);  // one token per warp
-  const int H = a.H;
+  const int g = lane >> 2, q = lane & 3;
+  const int e0 = blockIdx.x * kRouteTileExperts;
+  const int ne = min(kRouteTileExperts, E - e0);
+  const int t0 = blockIdx.y * kRouteTileTokens;
+  const int nt = min(kRouteTileTokens, M - t0);
+  const int n_chunks = (H + kRouteChunk - 1) / kRouteChunk;
 
-  // Router rows do not depend on earlier kernels: stage them before waiting.
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(a.wr + static_cast<size_t>(e0) * H);
-    uint4* dst = reinterpret_cast<uint4*>(w);
-    const int n16 = ne * H / 8;
-    for (int i = tid; i < n16; i += blockDim.x) dst[i] = src[i];
+  // Rows past the tile's experts / tokens stay zero (their outputs are dropped).
+  for (int i = tid; i < (kRouteTileExperts - ne) * ld; i += blockDim.x) s_w[ne * ld + i] = __float2bfloat16_rn(0.f);
+  for (int i = tid; i < (kRouteTileTokens - nt) * ld; i += blockDim.x) s_x[nt * ld + i] = __float2bfloat16_rn(0.f);
+  if (tid == 0) {
+    s_bad = 0;
+    mbar_init(wbar, 1);
+    fence_mbar_init();
+    const int len = min(H, kRouteChunk);
+    mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(ne * len * 2));
+    for (int r = 0; r < ne; ++r)
+      bulk_load(smem_u32(s_w + r * ld), a.wr + static_cast<size_t>(e0 + r) * H, len * 2, wbar);
   }
   pdl_wait();
   pdl_trigger();
-  __syncthreads();
 
-  for (int t = t0 + warp; t < t1; t += 8) {
-    const float* xr = a.x + static_cast<size_t>(t) * H;
-    const float rstd = row_rstd(xr, H, a.eps, lane);
-    const float mine = warp_router_dots<kRouteExperts>(
-        xr, rstd, w, ne, H, lane, blockIdx.x == 0 ? a.xn_rows + static_cast<size_t>(t) * H : nullptr);
-    if (lane < ne) {
-      const int e = e0 + lane;
-      a.logits[static_cast<size_t>(t) * a.E + e] = mine + (a.bias ? a.bias[e] : 0.f);
+  // This warp's two token rows: tile rows warp and warp + 8.
+  float rs[2];
+  if (H <= kRouteChunk) {
+    float4 xv[2][16];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = warp + 8 * j;
+      const float* xr = a.x + static_cast<size_t>(t0 + r) * H;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int col = lane * 4 + 128 * c;
+        xv[j][c] = (r < nt && col < H) ? *reinterpret_cast<const float4*>(xr + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        ss += xv[j][c].x * xv[j][c].x + xv[j][c].y * xv[j][c].y + xv[j][c].z * xv[j][c].z + xv[j][c].w * xv[j][c].w;
+      ss = warp_sum_f(ss);
+      rs[j] = 1.0f / sqrtf(ss / static_cast<float>(H) + a.eps);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = warp + 8 * j;
+      if (r >= nt) continue;
+      bf16* gx = blockIdx.x == 0 ? a.xn_rows + static_cast<size_t>(t0 + r) * H : nullptr;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int col = lane * 4 + 128 * c;
+        if (col < H) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(xv[j][c].x * rs[j], xv[j][c].y * rs[j]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(xv[j][c].z * rs[j], xv[j][c].w * rs[j]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(s_x + r * ld + col) = pk;
+          if (gx != nullptr) *reinterpret_cast<uint2*>(gx + col) = pk;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int r = warp + 8 * j;
+      rs[j] = r < nt ? row_rstd(a.x + static_cast<size_t>(t0 + r) * H, H, a.eps, lane) : 0.f;
     }
   }
 
+  float acc[4][4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+
+  for (int ch = 0; ch < n_chunks; ++ch) {
+    const int c0 = ch * kRouteChunk;
+    const int len = min(kRouteChunk, H - c0);
+    if (ch > 0) {
+      // Refill: every warp is done with the previous chunk's rows.
+      __syncthreads();
+      if (tid == 0) {
+        fence_proxy_async_shared();
+        mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(ne * len * 2));
+        for (int r = 0; r < ne; ++r)
+          bulk_load(smem_u32(s_w + r * ld), a.wr + static_cast<size_t>(e0 + r) * H + c0, len * 2, wbar);
+      }
+    }
+    if (n_chunks > 1) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int r = warp + 8 * j;
+        if (r >= nt) continue;
+        const float* xr = a.x + static_cast<size_t>(t0 + r) * H + c0;
+        bf16* gx = blockIdx.x == 0 ? a.xn_rows + static_cast<size_t>(t0 + r) * H + c0 : nullptr;
+        for (int col = lane * 4; col < len; col += 128) {
+          const float4 v = *reinterpret_cast<const float4*>(xr + col);
+          __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * rs[j], v.y * rs[j]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * rs[j], v.w * rs[j]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(s_x + r * ld + col) = pk;
+          if (gx != nullptr) *reinterpret_cast<uint2*>(gx + col) = pk;
+        }
+      }
+    }
+    __syncthreads();
+    if (!mbar_wait_for(wbar, static_cast<uint32_t>(ch & 1), kWaitLimitNs) && lane == 0) {
+      atomicOr(a.err, kErrMbarTimeout);
+      s_bad = 1;
+    }
+    // This warp's eighth of the chunk (len / 8 is a multiple of 16).
+    const int kw = len >> 3;
+    const bf16* xa = s_x + g * ld + 2 * q + warp * kw;
+    const bf16* wa = s_w + g * ld + 2 * q + warp * kw;
+    for (int kb = 0; kb < kw; kb += 16) {
+      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(xa + kb);
+      const uint32_t a1 = *reinterpret_cast<const uint32_t*>(xa + 8 * ld + kb);
+      const uint32_t a2 = *reinterpret_cast<const uint32_t*>(xa + kb + 8);
+      const uint32_t a3 = *reinterpret_cast<const uint32_t*>(xa + 8 * ld + kb + 8);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bf16* wb = wa + 8 * j * ld + kb;
+        mma_bf16_16816(acc[j], a0, a1, a2, a3, *reinterpret_cast<const uint32_t*>(wb),
+                       *reinterpret_cast<const uint32_t*>(wb + 8));
+      }
+    }
+  }
+
+  // Partials [warp][token][expert], then fixed-order sums over the warps.
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float* pw = s_part + (warp * kRouteTileTokens + g) * kRouteTileExperts + 8 * j + 2 * q;
+    *reinterpret_cast<float2*>(pw) = make_float2(acc[j][0], acc[j][1]);
+    *reinterpret_cast<float2*>(pw + 8 * kRouteTileExperts) = make_float2(acc[j][2], acc[j][3]);
+  }
+  __syncthreads();
+  // A router copy that did not land has been flagged; wait once more
+  // (bounded) so that no copy is still writing shared memory when this CTA
+  // exits, and carry on so that the arrival counters stay consistent.
+  if (s_bad) mbar_wait_for(wbar, static_cast<uint32_t>((n_chunks - 1) & 1), kWaitLimitNs);
+  for (int o = tid; o < kRouteTileTokens * kRouteTileExperts; o += blockDim.x) {
+    const int r = o / kRouteTileExperts, c = o % kRouteTileExperts;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += s_part[(w * kRouteTileTokens + r) * kRouteTileExperts + c];
+    if (r < nt && c < ne) {
+      const int e = e0 + c;
+      a.logits[static_cast<size_t>(t0 + r) * E + e] = sum + (a.bias ? a.bias[e] : 0.f);
+    }
+  }
+  __threadfence();
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
     const int old = atomicAdd(&a.tg_ctr[blockIdx.y], 1);
     s_last = (old == static_cast<int>(gridDim.x) - 1);
   }
@@ -116,13 +261,23 @@ __global__ void __launch_bounds__(256) k_route(RouteArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // Top-k for this token group (one warp per token; lane l holds experts
-  // l, l+32, ..., up to 256).
-  for (int t = t0 + warp; t < t1; t += 8) {
-    const TopkSel sel = warp_topk(a.logits + static_cast<size_t>(t) * a.E, a.E, a.K, lane);
-    if (lane < a.K) {
-      a.topk_idx[static_cast<size_t>(t) * a.K + lane] = sel.e;
-      a.topk_w[static_cast<size_t>(t) * a.K + lane] = sel.w;
+  // Top-k for this token tile: warp w takes tile rows w and w + 8 together.
+  const float* rows[2];
+  bool valid[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int r = warp + 8 * j;
+    valid[j] = r < nt;
+    rows[j] = a.logits + static_cast<size_t>(t0 + (valid[j] ? r : 0)) * E;
+  }
+  TopkSel sel[2];
+  warp_topk_n<2>(rows, valid, E, a.K, lane, nullptr, sel);
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int t = t0 + warp + 8 * j;
+    if (valid[j] && lane < a.K) {
+      a.topk_idx[static_cast<size_t>(t) * a.K + lane] = sel[j].e;
+      a.topk_w[static_cast<size_t>(t) * a.K + lane] = sel[j].w;
     }
   }
   if (tid == 0) a.tg_ctr[blockIdx.y] = 0;
@@ -184,9 +339,20 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
   }
   for (int i = tid; i < kMaxExperts * (kMaxTokens / 32); i += blockDim.x) (&s_bm[0][0])[i] = 0u;
   __syncthreads();
-  for (int i = tid; i < MK; i += blockDim.x) {
-    const int e = s_idx[i], t = i / a.K;
-    atomicOr(&s_bm[e][t >> 5], 1u << (t & 31));
+  // Word wd of every expert's token mask (tokens 32wd..32wd+31) is written
+  // by warp wd alone: per selection slot, the lanes that chose the same
+  // expert merge their bits and the lowest of them stores the word.
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int wd = warp; wd < nw; wd += blockDim.x >> 5) {
+      const int t = wd * 32 + lane;
+      for (int k = 0; k < a.K; ++k) {
+        const int e = t < a.M ? s_idx[t * a.K + k] : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) s_bm[e][wd] |= peers;
+        __syncwarp();
+      }
+    }
   }
   __syncthreads();
   int c = 0;
@@ -225,11 +391,29 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
   }
   __syncthreads();
   const size_t H = a.H;
-  for (int r = blockIdx.x; r < MK; r += gridDim.x) {
-    const int t = s_row_tok[r];
-    const uint4* src = reinterpret_cast<const uint4*>(a.xg + static_cast<size_t>(MK + t) * H);
-    uint4* dst = reinterpret_cast<uint4*>(a.xg + static_cast<size_t>(r) * H);
-    for (int i = tid; i < static_cast<int>(H / 8); i += blockDim.x) dst[i] = src[i];
+  // Four consecutive rows per CTA pass, every thread's loads issued before
+  // its stores.
+  const int per_row = static_cast<int>(H / 8);
+  for (int base = blockIdx.x * 4; base < MK; base += gridDim.x * 4) {
+    const int span = 4 * per_row;
+    for (int i0 = tid; i0 < span; i0 += blockDim.x * 4) {
+      uint4 v[4];
+      int dst_i[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = i0 + j * blockDim.x;
+        const int r = base + i / per_row;
+        dst_i[j] = -1;
+        if (i < span && r < MK) {
+          const int c = i - (i / per_row) * per_row;
+          v[j] = reinterpret_cast<const uint4*>(a.xg + static_cast<size_t>(MK + s_row_tok[r]) * H)[c];
+          dst_i[j] = r * per_row + c;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (dst_i[j] >= 0) reinterpret_cast<uint4*>(a.xg)[dst_i[j]] = v[j];
+    }
   }
 }
 
@@ -300,11 +484,17 @@ cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl) {
   return launch_kernel(k_rmsnorm, dim3((a.M + 7) / 8), dim3(256), 0, s, pdl, a);
 }
 
+size_t route_smem_bytes(int H) {
+  const size_t ld = static_cast<size_t>(std::min(H, kRouteChunk)) + 8;
+  return (kRouteTileExperts + kRouteTileTokens) * ld * sizeof(bf16) +
+         (8 * kRouteTileTokens * kRouteTileExperts + 16) * sizeof(float) + sizeof(uint64_t);
+}
+
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl) {
-  const size_t smem = static_cast<size_t>(kRouteExperts) * a.H * sizeof(bf16);
+  const size_t smem = route_smem_bytes(a.H);
   cudaError_t e = cudaFuncSetAttribute(k_route, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid((a.E + kRouteExperts - 1) / kRouteExperts, (a.M + kRouteTokens - 1) / kRouteTokens);
+  dim3 grid((a.E + kRouteTileExperts - 1) / kRouteTileExperts, (a.M + kRouteTileTokens - 1) / kRouteTileTokens);
   return launch_kernel(k_route, grid, dim3(256), smem, s, pdl, a);
 }
 

@@ -1,5 +1,8 @@
-// Per-warp routing arithmetic shared by the standalone routing kernel and
-// the fused layer kernel, so both take identical decisions bit for bit.
+// Per-warp routing arithmetic: the fused layer kernel's CUDA-core router
+// dot products, the top-k selection that both routing paths share, and the
+// warp tensor-core contraction of the standalone routing kernel. The two
+// paths sum the router dot products in different orders, so their logits
+// can differ in the last bits; the selection rule itself is the same code.
 //
 // Follows "Clover-35B-A3B: how a diffusion model gets to 680 tokens a second,
 // read from its files", sections "What Clover is" (256 experts, 8 per token)
@@ -131,73 +134,127 @@ struct TopkSel {
   float p;  // softmax probability over all E logits (coreset mass)
 };
 
-// One warp, one token: top-k of E (<= 256) logits by descending value, the
-// lower expert id first on ties, restricted to the experts whose bit is set in
-// `allowed` (8 words; null = all). Weights = softmax over the selected
-// logits (= the top-k probabilities renormalised). Lane k (< K) receives
-// selection k, its weight and its probability under the softmax over all E.
-__device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int K, int lane,
-                                             const uint32_t* allowed = nullptr) {
-  float v[8];
-  float all_max = -INFINITY;
+// One warp, NT tokens at once (independent chains, interleaved for latency):
+// top-k of E (<= 256) logits by descending value, the lower expert id first
+// on ties, restricted to the experts whose bit is set in `allowed` (8 words;
+// null = all). Weights = softmax over the selected logits (= the top-k
+// probabilities renormalised). Lane k (< K) receives selection k of token n
+// in out[n], with its weight and its probability under the softmax over all
+// E. Tokens with valid[n] false read nothing; their out[n] is meaningless.
+// The per-token arithmetic does not depend on NT.
+template <int NT>
+__device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], const bool (&valid)[NT], int E, int K,
+                                            int lane, const uint32_t* allowed, TopkSel (&out)[NT]) {
+  float v[NT * 8];
+  float all_max[NT], all_sum[NT];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldcg(logits_row + e) : -INFINITY;
-    all_max = fmaxf(all_max, v[i]);
-  }
-  all_max = warp_max_f(all_max);
-  float all_sum = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) all_sum += (lane + 32 * i < E) ? expf(v[i] - all_max) : 0.f;
-  all_sum = warp_sum_f(all_sum);
-  if (allowed != nullptr) {
+  for (int n = 0; n < NT; ++n) {
+    all_max[n] = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((allowed[e >> 5] >> (e & 31)) & 1u)) v[i] = -INFINITY;
+      v[n * 8 + i] = (valid[n] && e < E) ? __ldcg(rows[n] + e) : -INFINITY;
+      all_max[n] = fmaxf(all_max[n], v[n * 8 + i]);
     }
   }
-  float my_v = -INFINITY;
-  int my_e = 0;
-  for (int k = 0; k < K; ++k) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
+  for (int n = 0; n < NT; ++n) all_max[n] = warp_max_f(all_max[n]);
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    all_sum[n] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) all_sum[n] += (lane + 32 * i < E) ? expf(v[n * 8 + i] - all_max[n]) : 0.f;
+  }
+#pragma unroll
+  for (int n = 0; n < NT; ++n) all_sum[n] = warp_sum_f(all_sum[n]);
+  if (allowed != nullptr) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((allowed[e >> 5] >> (e & 31)) & 1u)) v[n * 8 + i] = -INFINITY;
+      }
+  }
+  float my_v[NT];
+  int my_e[NT];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    my_v[n] = -INFINITY;
+    my_e[n] = 0;
+  }
+  for (int k = 0; k < K; ++k) {
+    float bv[NT];
+    int be[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      bv[n] = -INFINITY;
+      be[n] = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && (v[n * 8 + i] > bv[n] || (v[n * 8 + i] == bv[n] && e < be[n]))) {
+          bv[n] = v[n * 8 + i];
+          be[n] = e;
+        }
       }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv[n], o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be[n], o);
+        if (ov > bv[n] || (ov == bv[n] && oe < be[n])) {
+          bv[n] = ov;
+          be[n] = oe;
+        }
       }
     }
-    if ((be & 31) == lane) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (i == (be >> 5)) v[i] = -INFINITY;
-    }
-    if (lane == k) {
-      my_v = bv;
-      my_e = be;
+    for (int n = 0; n < NT; ++n) {
+      const bool mine = (be[n] & 31) == lane;
+      const int slot = be[n] >> 5;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[n * 8 + i] = (mine && i == slot) ? -INFINITY : v[n * 8 + i];
+      if (lane == k) {
+        my_v[n] = bv[n];
+        my_e[n] = be[n];
+      }
     }
   }
-  const float top = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = (lane < K) ? expf(my_v - top) : 0.f;
-  const float sum = warp_sum_f(ex);
-  TopkSel r;
-  r.e = my_e;
-  r.w = ex / sum;
-  r.p = (lane < K) ? expf(my_v - all_max) / all_sum : 0.f;
-  return r;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const float top = __shfl_sync(0xffffffffu, my_v[n], 0);
+    const float ex = (lane < K) ? expf(my_v[n] - top) : 0.f;
+    const float sum = warp_sum_f(ex);
+    out[n].e = my_e[n];
+    out[n].w = ex / sum;
+    out[n].p = (lane < K) ? expf(my_v[n] - all_max[n]) / all_sum[n] : 0.f;
+  }
+}
+
+// Single-token form of warp_topk_n.
+__device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int K, int lane,
+                                             const uint32_t* allowed = nullptr) {
+  const float* rows[1] = {logits_row};
+  const bool valid[1] = {true};
+  TopkSel out[1];
+  warp_topk_n<1>(rows, valid, E, K, lane, allowed, out);
+  return out[0];
+}
+
+// D (16x8, fp32) += A (16x16, bf16, row-major) * B (16x8, bf16, column-major)
+// on the warp's tensor cores. Fragment ownership (g = lane / 4, q = lane % 4):
+// a0 = A[g][2q..2q+1], a1 = A[g+8][2q..], a2 = A[g][2q+8..], a3 = A[g+8][2q+8..];
+// b0 = B[2q..2q+1][g], b1 = B[2q+8..2q+9][g]; d = D[g][2q..2q+1], D[g+8][2q..2q+1].
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 }  // namespace clover

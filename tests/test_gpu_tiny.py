@@ -38,6 +38,26 @@ def test_moe_layer_matches_oracle(M):
     assert ok, worst
 
 
+@pytest.mark.parametrize("M", [8, 40])
+def test_wide_hidden_matches_oracle(M):
+    """Hidden 4,096 (above the 2,048-column chunk of the standalone router
+    contraction, and above the fused kernel's register-resident rows), 32
+    experts top-4: the chunked routing path (M = 40) and the fused path
+    (M = 8) against the oracle."""
+    d = _dims(hidden=4096, n_experts=32, top_k=4)
+    layer = synth.make_layer(d, 14, 0, DEV, zipf_s=0.5)
+    x = synth.make_x(d, M, 15, DEV)
+    x_out, idx, w = clover.moe_block_step(d, layer, x)
+    torch.cuda.synchronize()
+    L = layer_to_oracle(layer)
+    xh = x.cpu().numpy()
+    ref = O.moe_layer(xh, L, d.top_k, d.rms_eps)
+    compare_routing(idx.cpu().numpy(), w.cpu().numpy(), ref, d.top_k)
+    forced = O.moe_layer(xh, L, d.top_k, d.rms_eps, force_idx=idx.cpu().numpy())
+    ok, worst = hidden_close(x_out.cpu().numpy() - xh, forced["x_out"] - xh)
+    assert ok, worst
+
+
 def test_moe_layer_in_place_and_deterministic():
     d = synth.TINY
     layer = synth.make_layer(d, 1, 0, DEV, zipf_s=1.2)
