@@ -110,7 +110,7 @@ __device__ __forceinline__ int unit_rows(const Unit& w, const Rt& rt, const Expe
 struct Smem {
   uint8_t* a_ring;
   uint8_t* b_ring;
-  float* xch;  // [64][17] up-half exchange for SwiGLU
+  float* xch;  // [2][64][17] gate/up half exchange for SwiGLU
   uint64_t *full_a, *empty_a, *full_b, *empty_b, *tfull, *tempty, *ufull, *uempty, *drain;
   int* unit_ids;  // [4]
   uint32_t* tmem_slot;
@@ -130,7 +130,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   s.a_ring = base;
   s.b_ring = s.a_ring + static_cast<size_t>(p.stages_a) * kATileBytes;
   s.xch = reinterpret_cast<float*>(s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 64 * 17);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 2 * 64 * 17);
   s.full_a = bars;
   s.empty_a = s.full_a + p.stages_a;
   s.full_b = s.empty_a + p.stages_a;
@@ -475,36 +475,45 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
     tc_fence_after();
     const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * 256u;
     if (w.kind == 0) {
-      const int f = w.slice * 64 + row;  // meaningful for the gate half (q < 2)
-      bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + f;
-      for (int c0 = 0; c0 < n; c0 += 16) {
-        float v[16];
+      // Rows 0..63 of the tile are gate rows f, rows 64..127 the up rows of
+      // the same f. Per 32 columns the gate warps take columns 0..15 and the
+      // up warps 16..31, each handing the other half of its values over.
+      const bool gate_half = q < 2;
+      const int r64 = gate_half ? row : row - 64;
+      bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + w.slice * 64 + r64;
+      float* x_up = s.xch;               // [64][17] up values of columns 0..15
+      float* x_gate = s.xch + 64 * 17;   // [64][17] gate values of columns 16..31
+      const uint32_t tm = (rt.dense && w.a != 0) ? rt.mask[w.e] : 0xffffffffu;
+      for (int c0 = 0; c0 < n; c0 += 32) {
+        float v[32];
         __syncwarp();
-        tmem_ld16(tb + c0, v);
-        if (q >= 2) {
+        tmem_ld32(tb + c0, v);  // columns past n are read but never kept
+        if (gate_half) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) s.xch[(row - 64) * 17 + j] = v[j];
+          for (int j = 0; j < 16; ++j) x_gate[r64 * 17 + j] = v[16 + j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x_up[r64 * 17 + j] = v[j];
         }
         named_bar_sync(1, 128);
-        if (q < 2) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + (gate_half ? j : 16 + j);
           // dense mode: column c is token c; a routed expert keeps the
           // columns of its tokens, stored at their rank among them
-          const uint32_t tm = (rt.dense && w.a != 0) ? rt.mask[w.e] : 0xffffffffu;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int c = c0 + j;
-            int slot = c;
-            bool keep = c < w.cnt;
-            if (rt.dense) {
-              keep = c < p.M && ((tm >> c) & 1u);
-              slot = (w.a == 0) ? c : __popc(tm & ((1u << c) - 1u));
-            }
-            if (keep) {
-              const float g = v[j];
-              const float up = s.xch[row * 17 + j];
-              const float h = g / (1.0f + expf(-g)) * up;
-              hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(h);
-            }
+          int slot = c;
+          bool keep = c < w.cnt;
+          if (rt.dense) {
+            keep = c < p.M && ((tm >> c) & 1u);
+            slot = (w.a == 0) ? c : __popc(tm & ((1u << c) - 1u));
+          }
+          if (keep) {
+            const float g = gate_half ? v[j] : x_gate[r64 * 17 + j];
+            const float up = gate_half ? x_up[r64 * 17 + j] : v[16 + j];
+            // silu(g) = g / (1 + e^-g); the exponent is capped so that the
+            // fast divide stays in its range (the capped terms are < 1e-33)
+            const float h = __fdividef(g, 1.0f + __expf(fminf(-g, 80.f))) * up;
+            hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(h);
           }
         }
         named_bar_sync(1, 128);
@@ -519,12 +528,12 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
       }
     } else {
       float* ycol = p.yslot + static_cast<size_t>(w.off) * p.H + static_cast<size_t>(w.slice) * 128 + row;
-      for (int c0 = 0; c0 < n; c0 += 16) {
-        float v[16];
+      for (int c0 = 0; c0 < n; c0 += 32) {
+        float v[32];
         __syncwarp();
-        tmem_ld16(tb + c0, v);
+        tmem_ld32(tb + c0, v);  // columns past n are read but never stored
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 32; ++j) {
           const int c = c0 + j;
           if (c < w.cnt) ycol[static_cast<size_t>(c) * p.H] = v[j];
         }
@@ -922,7 +931,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
 
 size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {
   return 1024 + static_cast<size_t>(stages_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
-         64 * 17 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
+         2 * 64 * 17 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
          256;
 }
 
