@@ -66,7 +66,7 @@ struct Unit {
 // Where a launch finds its routing: global tables written by k_perm
 // (k_expert) or shared-memory tables built by the launch itself (k_layer).
 struct Rt {
-  const int* act;           // active routed expert ids, ascending
+  const int* act;           // active routed expert ids (standalone kernel: heaviest first)
   const int* cnt;           // [E] tokens per expert
   const int* off;           // [E] first row per expert
   const uint32_t* mask;     // [E] token bitmask (dense mode)

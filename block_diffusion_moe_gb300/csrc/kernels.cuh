@@ -70,7 +70,7 @@ struct PermArgs {
   int32_t* tok_slot;        // [M][K] -> row of the gathered buffer
   int* cnt;                 // [E]
   int* off;                 // [E]
-  int* act;                 // [E] active expert ids, ascending
+  int* act;                 // [E] active expert ids, heaviest first (ties: lower id)
   int* n_active;            // scalar
   int* unit_ctr;            // scalar, reset to 0
   int* gu_done;             // [E+1], reset to 0

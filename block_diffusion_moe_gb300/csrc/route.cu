@@ -326,6 +326,7 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
   int* s_row_tok = s_idx + a.M * a.K;         // [M*K]
   __shared__ uint32_t s_bm[kMaxExperts][kMaxTokens / 32];
   __shared__ int s_off[kMaxExperts];
+  __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_tmp[9];
   const int tid = threadIdx.x;
   const int MK = a.M * a.K;
@@ -360,8 +361,9 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
     for (int wd = 0; wd < nw; ++wd) c += __popc(s_bm[tid][wd]);
   int total = 0;
   const int off = block_excl_scan_256(c, s_tmp, &total);
-  const int apos = block_excl_scan_256(c > 0 ? 1 : 0, s_tmp, &total);
+  const int n_act = __syncthreads_count(tid < a.E && c > 0);
   if (tid < a.E) s_off[tid] = off;
+  s_cnt[tid] = tid < a.E ? c : 0;
   __syncthreads();
   for (int i = tid; i < MK; i += blockDim.x) {
     const int e = s_idx[i], t = i / a.K;
@@ -376,10 +378,19 @@ __global__ void __launch_bounds__(256) k_perm(PermArgs a) {
     if (tid < a.E) {
       a.cnt[tid] = c;
       a.off[tid] = off;
-      if (c > 0) a.act[apos] = tid;
+      if (c > 0) {
+        // Active experts heaviest first (ties: lower id first), so that the
+        // longest units are handed out first and do not end the launch.
+        int rank = 0;
+        for (int j = 0; j < a.E; ++j) {
+          const int cj = s_cnt[j];
+          rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
+        }
+        a.act[rank] = tid;
+      }
     }
     if (tid == 0) {
-      *a.n_active = total;
+      *a.n_active = n_act;
       *a.unit_ctr = 0;
     }
     for (int i = tid; i <= a.E; i += blockDim.x) a.gu_done[i] = 0;
