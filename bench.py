@@ -52,16 +52,17 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _expert_traffic(u_mean):
-    """DRAM bytes per expert-kernel launch from the committed ncu summary
-    (bytes per expert x experts per launch), if that summary was taken on the
-    current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "moe_layer_fused_clover_block32.md")
+def _expert_traffic(u_mean, fused):
+    """DRAM bytes per expert-kernel launch from the committed ncu summary of
+    that kernel (bytes per expert x experts per launch), if the summary was
+    taken on the current kernel source; else None."""
+    name = "moe_layer_fused_clover_block32.md" if fused else "moe_layer_standalone_zipf256.md"
+    path = os.path.join(ROOT, "profiles", name)
     src = os.path.join(ROOT, "block_diffusion_moe_gb300", "csrc", "expert.cu")
     try:
         text = open(path).read()
         sha = text.split("expert.cu sha256:")[1].split()[0]
-        per = float(text.split("DRAM bytes per expert (read + write, / 155 experts):")[1].split()[0])
+        per = float(text.split("DRAM bytes per expert (read + write):")[1].split()[0])
         if sha != hashlib.sha256(open(src, "rb").read()).hexdigest() or u_mean is None:
             return None
         return per * (u_mean + 1)
@@ -250,6 +251,8 @@ WORKLOADS = {
             "layers + head, router biased to Zipf(1.2) expert popularity",
     "coreset": "full block denoising step as 'step' with the block coreset expert selection (top_p 0.9) in every "
                "MoE layer",
+    "zipf_layer": "one Clover-shaped MoE layer on 8 blocks x 32 positions (256 tokens), router biased to Zipf(1.2) "
+                  "expert popularity (the standalone routing and expert kernels)",
 }
 CORESET_TOP_P = 0.9
 
@@ -263,13 +266,15 @@ def run_ours(args):
     clover.lib()
     seed = 1000 + rank
     kind = args.workload
-    n_pos = 256 if kind == "zipf" else M
-    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "layer": 1, "head": 0}[kind]
+    n_pos = 256 if kind in ("zipf", "zipf_layer") else M
+    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "layer": 1, "zipf_layer": 1,
+                "head": 0}[kind]
+    one_layer = kind in ("layer", "zipf_layer")
     full = kind in ("step", "zipf", "coreset")
     top_p = CORESET_TOP_P if kind == "coreset" else 0.0
-    zipf = 1.2 if kind == "zipf" else None
+    zipf = 1.2 if kind in ("zipf", "zipf_layer") else None
     layers = [synth.make_layer(D, seed, l, dev, zipf_s=zipf) for l in range(n_layers)]
-    head_w = synth.make_head(D, seed, dev) if kind != "layer" else None
+    head_w = synth.make_head(D, seed, dev) if not one_layer else None
     embed = synth.make_embed(D, seed, dev) if full else None
     model = clover.Model(D, layers, embed, head_w, coreset_top_p=top_p) if full else None
     ctx = synth.make_ctx(D, n_pos, seed, dev)
@@ -279,7 +284,7 @@ def run_ours(args):
     x_out = torch.empty_like(x_fixed)
     if full:
         ws = clover.workspace(clover.denoise_workspace_bytes(D, n_pos), dev)
-    elif kind == "layer":
+    elif one_layer:
         ws = clover.workspace(clover.moe_workspace_bytes(D, n_pos), dev)
     else:
         ws = clover.workspace(clover.head_workspace_bytes(D, n_pos), dev)
@@ -297,7 +302,7 @@ def run_ours(args):
                 steps_in_block[0] = 0
             clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
             steps_in_block[0] += 1
-        elif kind == "layer":
+        elif one_layer:
             clover.moe_block_step(D, layers[0], x_fixed, x_out=x_out, ws=ws, with_topk=False)
         else:
             clover.lmhead_unmask(D, head_w, x_fixed, tokens, masked, block=M, ws=ws)
@@ -366,7 +371,7 @@ def run_ours(args):
         moe_ws = clover.workspace(clover.moe_workspace_bytes(D, n_pos), dev)
         head_ws = clover.workspace(clover.head_workspace_bytes(D, n_pos), dev)
         for s_ in range(args.steps):
-            if kind == "layer":
+            if one_layer:
                 _, idx, _ = clover.moe_block_step(D, layers[0], x_fixed, x_out=x, ws=moe_ws)
                 u_per_launch.append(int(torch.unique(idx).numel()))
                 continue
@@ -382,14 +387,14 @@ def run_ours(args):
     achieved = sum(alg) / (sum(durs) * 1e-3) / 1e9          # GB/s
     peak, peak_kind = _peaks()
     u_mean = float(np.mean(u_per_launch)) if u_per_launch else None
-    step_bytes = sum(alg) / args.steps + n_layers * D.router_bytes + (D.head_bytes if kind != "layer" else 0)
+    step_bytes = sum(alg) / args.steps + n_layers * D.router_bytes + (D.head_bytes if not one_layer else 0)
     share = sum(durs) / ms_instr
 
     # ---- end to end through the C ABI with host buffers
     h_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
     h_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
-    h_in = (x_fixed if kind in ("layer", "head") else ctx).cpu().pin_memory()
-    d_in = x_fixed if kind in ("layer", "head") else ctx
+    h_in = (x_fixed if one_layer or kind == "head" else ctx).cpu().pin_memory()
+    d_in = x_fixed if one_layer or kind == "head" else ctx
     o_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
     o_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
     o_x = torch.empty((n_pos, D.hidden), dtype=torch.float32).pin_memory()
@@ -403,14 +408,14 @@ def run_ours(args):
             h_tokens.fill_(D.mask_id)
             h_masked.fill_(1)
         d_in.copy_(h_in, non_blocking=True)
-        if kind != "layer":
+        if not one_layer:
             tokens.copy_(h_tokens, non_blocking=True)
             masked.copy_(h_masked, non_blocking=True)
         if full:
             clover.denoise_step(model, ctx, tokens, masked, block=M, ws=ws)
         else:
             step()
-        if kind == "layer":
+        if one_layer:
             o_x.copy_(x_out, non_blocking=True)
         else:
             o_tokens.copy_(tokens, non_blocking=True)
@@ -420,7 +425,7 @@ def run_ours(args):
             h_tokens.copy_(o_tokens)
             h_masked.copy_(o_masked)
     e2e_s = time.perf_counter() - t0
-    if kind == "layer":
+    if one_layer:
         h2d, d2h = n_pos * D.hidden * 4, n_pos * D.hidden * 4
     else:
         h2d = n_pos * 4 + n_pos + n_pos * D.hidden * 4
@@ -436,7 +441,8 @@ def run_ours(args):
     # <= 32 positions: one fused launch per layer; more: route, perm, experts, combine
     per_layer = 1 if n_pos <= 32 else 4
     launches_per_step = {"step": 1 + per_layer * n_layers + 2, "zipf": 1 + per_layer * n_layers + 2,
-                         "coreset": 1 + per_layer * n_layers + 2, "layer": per_layer, "head": 2}[kind]
+                         "coreset": 1 + per_layer * n_layers + 2, "layer": per_layer, "zipf_layer": per_layer,
+                         "head": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
                    else "k_layer (routing + grouped SwiGLU experts + combine, one launch per MoE layer)"
                    if n_pos <= 32 else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")
@@ -453,7 +459,8 @@ def run_ours(args):
                    "step_roofline_frac": step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": roof_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _expert_traffic(u_mean) if kind != "head" else None, "launches": len(durs),
+                     "traffic": _expert_traffic(u_mean, n_pos <= 32) if kind != "head" else None,
+                     "launches": len(durs),
                      "mean_launch_us": float(np.mean(durs)) * 1e3, "share_of_step": share,
                      "ms_per_step_with_events": ms_instr / args.steps},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -110,7 +110,7 @@ __device__ __forceinline__ int unit_rows(const Unit& w, const Rt& rt, const Expe
 struct Smem {
   uint8_t* a_ring;
   uint8_t* b_ring;
-  float* xch;  // [2][64][17] gate/up half exchange for SwiGLU
+  float* xch;  // [2][64][20] gate/up half exchange for SwiGLU
   uint64_t *full_a, *empty_a, *full_b, *empty_b, *tfull, *tempty, *ufull, *uempty, *drain;
   int* unit_ids;  // [4]
   uint32_t* tmem_slot;
@@ -130,7 +130,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   s.a_ring = base;
   s.b_ring = s.a_ring + static_cast<size_t>(p.stages_a) * kATileBytes;
   s.xch = reinterpret_cast<float*>(s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 2 * 64 * 17);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 2 * 64 * 20);
   s.full_a = bars;
   s.empty_a = s.full_a + p.stages_a;
   s.full_b = s.empty_a + p.stages_a;
@@ -481,21 +481,41 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
       const bool gate_half = q < 2;
       const int r64 = gate_half ? row : row - 64;
       bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + w.slice * 64 + r64;
-      float* x_up = s.xch;               // [64][17] up values of columns 0..15
-      float* x_gate = s.xch + 64 * 17;   // [64][17] gate values of columns 16..31
+      float* x_up = s.xch;              // [64][20] up values of columns 0..15
+      float* x_gate = s.xch + 64 * 20;  // [64][20] gate values of columns 16..31
       const uint32_t tm = (rt.dense && w.a != 0) ? rt.mask[w.e] : 0xffffffffu;
       for (int c0 = 0; c0 < n; c0 += 32) {
         float v[32];
         __syncwarp();
         tmem_ld32(tb + c0, v);  // columns past n are read but never kept
-        if (gate_half) {
+        float4* mine = reinterpret_cast<float4*>((gate_half ? x_gate : x_up) + r64 * 20);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x_gate[r64 * 17 + j] = v[16 + j];
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) x_up[r64 * 17 + j] = v[j];
+        for (int j = 0; j < 4; ++j) {
+          const int k = 4 * j;
+          mine[j] = gate_half ? make_float4(v[16 + k], v[17 + k], v[18 + k], v[19 + k])
+                              : make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
         }
         named_bar_sync(1, 128);
+        float o[16];
+        const float4* other = reinterpret_cast<const float4*>((gate_half ? x_up : x_gate) + r64 * 20);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 t4 = other[j];
+          o[4 * j] = t4.x;
+          o[4 * j + 1] = t4.y;
+          o[4 * j + 2] = t4.z;
+          o[4 * j + 3] = t4.w;
+        }
+        named_bar_sync(1, 128);  // the exchange rows are free again
+        // silu(g) = g / (1 + e^-g); the exponent is capped so that the fast
+        // divide stays in its range (the capped terms are below 1e-33)
+        float hv[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float g = gate_half ? v[j] : o[j];
+          const float up = gate_half ? o[j] : v[16 + j];
+          hv[j] = __fdividef(g, 1.0f + __expf(fminf(-g, 80.f))) * up;
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int c = c0 + (gate_half ? j : 16 + j);
@@ -507,16 +527,8 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
             keep = c < p.M && ((tm >> c) & 1u);
             slot = (w.a == 0) ? c : __popc(tm & ((1u << c) - 1u));
           }
-          if (keep) {
-            const float g = gate_half ? v[j] : x_gate[r64 * 17 + j];
-            const float up = gate_half ? x_up[r64 * 17 + j] : v[16 + j];
-            // silu(g) = g / (1 + e^-g); the exponent is capped so that the
-            // fast divide stays in its range (the capped terms are < 1e-33)
-            const float h = __fdividef(g, 1.0f + __expf(fminf(-g, 80.f))) * up;
-            hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(h);
-          }
+          if (keep) hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(hv[j]);
         }
-        named_bar_sync(1, 128);
       }
       tc_fence_before();
       fence_proxy_async_global();
@@ -539,7 +551,7 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
         }
       }
       tc_fence_before();
-      __threadfence();
+      if (p.combine) __threadfence();  // otherwise the rows are read by a later kernel
       named_bar_sync(1, 128);
       if (etid == 0 && p.stamps != nullptr) atomicMax(p.stamps + 6, global_ns());
       if (etid == 0) {
@@ -931,7 +943,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
 
 size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {
   return 1024 + static_cast<size_t>(stages_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
-         2 * 64 * 17 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
+         2 * 64 * 20 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
          256;
 }
 

@@ -58,6 +58,32 @@ def test_wide_hidden_matches_oracle(M):
     assert ok, worst
 
 
+@pytest.mark.parametrize("M", [40, 100, 256])
+def test_paired_units_match_oracle(M):
+    """Experts with more than 32 tokens run as paired units (two weight
+    tiles per B tile). With 4 of 16 experts per token, d_ff 128 and a skewed
+    router: M = 40 and 100 pair the shared expert and a few routed ones, all
+    within one TMEM buffer (at most 128 token columns); at M = 256 the
+    heaviest experts and the shared one exceed 128 columns and take both
+    buffers."""
+    d = _dims(n_experts=16, top_k=4, d_ff=128)
+    layer = synth.make_layer(d, 16, 0, DEV, zipf_s=1.0)
+    x = synth.make_x(d, M, 17, DEV)
+    x_out, idx, w = clover.moe_block_step(d, layer, x)
+    torch.cuda.synchronize()
+    L = layer_to_oracle(layer)
+    xh = x.cpu().numpy()
+    ref = O.moe_layer(xh, L, d.top_k, d.rms_eps)
+    compare_routing(idx.cpu().numpy(), w.cpu().numpy(), ref, d.top_k)
+    forced = O.moe_layer(xh, L, d.top_k, d.rms_eps, force_idx=idx.cpu().numpy())
+    ok, worst = hidden_close(x_out.cpu().numpy() - xh, forced["x_out"] - xh)
+    assert ok, worst
+    counts = np.bincount(idx.cpu().numpy().ravel(), minlength=d.n_experts)
+    assert (counts > 32).sum() >= 3             # routed experts that pair
+    if M == 256:
+        assert (counts > 128).sum() >= 1        # pairs over both TMEM buffers
+
+
 def test_moe_layer_in_place_and_deterministic():
     d = synth.TINY
     layer = synth.make_layer(d, 1, 0, DEV, zipf_s=1.2)
