@@ -398,12 +398,7 @@ def run_ours(args):
     o_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
     o_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
     o_x = torch.empty((n_pos, D.hidden), dtype=torch.float32).pin_memory()
-    h_tokens.fill_(D.mask_id)
-    h_masked.fill_(1)
-    steps_in_block[0] = 0
-    _barrier(dist)
-    t0 = time.perf_counter()
-    for s_ in range(args.steps):
+    def e2e_step(s_):
         if full and s_ > 0 and s_ % M == 0:
             h_tokens.fill_(D.mask_id)
             h_masked.fill_(1)
@@ -424,6 +419,18 @@ def run_ours(args):
         if full:
             h_tokens.copy_(o_tokens)
             h_masked.copy_(o_masked)
+
+    # one untimed pass first (first-use costs of the pinned buffers and copies)
+    h_tokens.fill_(D.mask_id)
+    h_masked.fill_(1)
+    e2e_step(0)
+    h_tokens.fill_(D.mask_id)
+    h_masked.fill_(1)
+    steps_in_block[0] = 0
+    _barrier(dist)
+    t0 = time.perf_counter()
+    for s_ in range(args.steps):
+        e2e_step(s_)
     e2e_s = time.perf_counter() - t0
     if one_layer:
         h2d, d2h = n_pos * D.hidden * 4, n_pos * D.hidden * 4

@@ -56,6 +56,17 @@ Readings where the pages are silent (each is listed in the design doc):
   position, argmax ties to the lowest vocabulary id. The fallback considers
   only still-masked slots. Each block of `block` positions applies the rule
   on its own.
+* Self-speculative accept test (Files, "Two ways to run it"): a verify pass
+  over B drafts gives B + 1 rows, row j being the distribution against which
+  draft j is tested and row B the one after the last draft. Exact keeps a
+  draft that equals its row's argmax; threshold keeps it when its probability
+  is at least min(ratio, delta e^-H), H the entropy of the row (the page's
+  printed formula is lost; this is the form its text describes: defaults 0.9
+  and 0.6, "the ratio never binds", 0.6 when certain and 0.22 at one nat).
+  The round keeps the longest accepted prefix of r drafts plus the boundary
+  token, taken greedily as the argmax of row r. The mask token has
+  probability zero, so it is never accepted; a draft id outside the
+  vocabulary is never accepted either.
 
 All float arithmetic is numpy float64; bf16 tensors arrive as uint16 arrays
 holding their bit patterns.
@@ -286,6 +297,71 @@ def unmask(tokens, masked, argmax, max_prob, threshold: float, block: int):
     tokens[commit] = np.asarray(argmax, dtype=np.int32)[commit]
     masked[commit] = 0
     return tokens, masked, commit
+
+
+ACCEPT_EXACT = 0
+ACCEPT_THRESHOLD = 1
+
+
+def verify_stats(z, mask_id: int, draft) -> dict:
+    """head_stats plus, per row, the entropy H = -sum_v p_v ln p_v of the
+    softmax with the mask token excluded and the probability of the row's
+    draft token (Files, "Two ways to run it"). A draft outside [0, V) has
+    probability 0."""
+    st = head_stats(z, mask_id)
+    z = np.array(z, dtype=np.float64, copy=True)
+    z[:, mask_id] = -np.inf
+    logp = z - st["lse"][:, None]
+    p = np.exp(logp)
+    ent = np.empty(z.shape[0])
+    pd = np.zeros(z.shape[0])
+    draft = np.asarray(draft, dtype=np.int64)
+    for n in range(z.shape[0]):
+        live = p[n] > 0
+        ent[n] = -np.sum(p[n, live] * logp[n, live])
+        if 0 <= draft[n] < z.shape[1]:
+            pd[n] = p[n, draft[n]]
+    st["entropy"] = ent
+    st["p_draft"] = pd
+    return st
+
+
+def accept_threshold(entropy, ratio: float, delta: float) -> np.ndarray:
+    """Probability a draft needs under the threshold rule: min(ratio,
+    delta * e^-H), float64."""
+    return np.minimum(ratio, delta * np.exp(-np.asarray(entropy, dtype=np.float64)))
+
+
+def accept(draft, argmax, p_draft, entropy, rule: int, ratio: float, delta: float, block: int) -> dict:
+    """The accept test over blocks of `block` rows (block - 1 drafts + the
+    boundary row). Per row j < block - 1 the decision is taken in float32:
+    exact, draft_j == argmax_j; threshold, float32(p_draft_j) >=
+    float32(min(ratio, delta e^-H_j)). r = the number of leading accepted
+    drafts; the round's tokens are drafts 0..r-1 then argmax of row r, the
+    remaining entries -1."""
+    draft = np.asarray(draft, dtype=np.int64)
+    argmax = np.asarray(argmax, dtype=np.int64)
+    n = draft.shape[0]
+    assert block >= 2 and n % block == 0
+    p32 = np.asarray(p_draft, dtype=np.float64).astype(np.float32)
+    t32 = accept_threshold(entropy, ratio, delta).astype(np.float32)
+    ok = np.zeros(n, dtype=bool)
+    acc_len = np.zeros(n // block, dtype=np.int32)
+    out = np.full(n, -1, dtype=np.int32)
+    for b in range(n // block):
+        r = 0
+        for j in range(block - 1):
+            i = b * block + j
+            if rule == ACCEPT_EXACT:
+                ok[i] = draft[i] == argmax[i]
+            else:
+                ok[i] = bool(p32[i] >= t32[i])
+        while r < block - 1 and ok[b * block + r]:
+            r += 1
+        acc_len[b] = r
+        out[b * block:b * block + r] = draft[b * block:b * block + r]
+        out[b * block + r] = argmax[b * block + r]
+    return {"accepted": ok, "accept_len": acc_len, "tokens": out}
 
 
 def embed(tokens, embed_bits, ctx) -> np.ndarray:

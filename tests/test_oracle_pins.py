@@ -441,3 +441,107 @@ def test_route_within_planted_ties_and_weights():
     idx, w = O.route_within(logits, [0, 3, 2], 2)
     assert list(idx[0]) == [2, 0]
     assert w[0, 0] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Self-speculative accept test (Files, "Two ways to run it")
+
+
+def _verify_rows(z):
+    return O.verify_stats(np.asarray(z, dtype=np.float64), z.shape[1] - 1, np.full(z.shape[0], -1))
+
+
+def test_entropy_closed_forms():
+    V = 1024
+    # uniform over the V - 1 tokens left once the mask token (id V - 1) is out
+    st = _verify_rows(np.full((2, V), 0.37))
+    assert np.allclose(st["entropy"], math.log(V - 1), rtol=0, atol=1e-12)
+    # two live tokens with probabilities 1/4 and 3/4
+    z = np.full((1, V), -1e4)
+    z[0, 5] = 0.0
+    z[0, 9] = math.log(3.0)
+    st = O.verify_stats(z, V - 1, np.array([9]))
+    want = -(0.25 * math.log(0.25) + 0.75 * math.log(0.75))
+    assert abs(st["entropy"][0] - want) < 1e-12
+    assert abs(st["p_draft"][0] - 0.75) < 1e-12
+    # a certain row: entropy 0, the argmax has probability 1
+    z = np.zeros((1, V))
+    z[0, 17] = 5000.0
+    st = O.verify_stats(z, V - 1, np.array([17]))
+    assert st["entropy"][0] == 0.0 and st["p_draft"][0] == 1.0 and st["argmax"][0] == 17
+
+
+def test_entropy_matches_scipy_and_bounds():
+    scipy_stats = pytest.importorskip("scipy.stats")
+    rng = np.random.default_rng(3)
+    V = 257
+    z = rng.normal(0.0, 2.0, size=(6, V))
+    st = _verify_rows(z)
+    for n in range(6):
+        p = np.exp(z[n, :V - 1] - z[n, :V - 1].max())
+        assert abs(st["entropy"][n] - scipy_stats.entropy(p)) < 1e-10
+    assert np.all(st["entropy"] >= 0) and np.all(st["entropy"] <= math.log(V - 1) + 1e-12)
+
+
+def test_verify_stats_bruteforce_loops():
+    # pure-Python softmax, entropy and draft probability on a 3 x 7 matrix,
+    # mask id 3 excluded
+    rng = np.random.default_rng(4)
+    z = rng.normal(0.0, 1.5, size=(3, 7))
+    z[1, 3] = 40.0               # the mask token's logit must not count
+    draft = np.array([2, 3, 6])  # row 1 drafts the mask token
+    st = O.verify_stats(z, 3, draft)
+    for n in range(3):
+        ex = [math.exp(z[n, v]) if v != 3 else 0.0 for v in range(7)]
+        tot = math.fsum(ex)
+        p = [e / tot for e in ex]
+        h = -math.fsum(q * math.log(q) for q in p if q > 0)
+        assert abs(st["entropy"][n] - h) < 1e-12
+        assert abs(st["p_draft"][n] - p[draft[n]]) < 1e-12
+    assert st["p_draft"][1] == 0.0
+
+
+def test_accept_threshold_matches_the_pages():
+    # defaults 0.9 / 0.6: probability 0.6 when certain, 0.22 at one nat
+    assert O.accept_threshold([0.0], 0.9, 0.6)[0] == 0.6
+    assert round(float(O.accept_threshold([1.0], 0.9, 0.6)[0]), 2) == 0.22
+    # with the defaults the ratio never binds
+    H = np.linspace(0.0, 12.0, 97)
+    assert np.allclose(O.accept_threshold(H, 0.9, 0.6), 0.6 * np.exp(-H), rtol=0, atol=0)
+    # a larger delta lets the ratio bind while the entropy is low
+    assert O.accept_threshold([0.0], 0.9, 3.0)[0] == 0.9
+    assert O.accept_threshold([3.0], 0.9, 3.0)[0] == pytest.approx(3.0 * math.exp(-3.0))
+
+
+def test_accept_golden_cases():
+    path = os.path.join(os.path.dirname(__file__), "golden", "accept_rule_cases.json")
+    cases = json.load(open(path))["cases"]
+    assert len(cases) >= 7
+    for c in cases:
+        got = O.accept(c["draft"], c["argmax"], c["p_draft"], c["entropy"], c["rule"], c["ratio"], c["delta"],
+                       c["block"])
+        assert got["accept_len"].tolist() == c["want_len"], c["name"]
+        assert got["tokens"].tolist() == c["want_tokens"], c["name"]
+
+
+def test_accept_invariants():
+    rng = np.random.default_rng(5)
+    V, block, nb = 64, 9, 40                  # rounds of 8 drafts: at most 9 tokens
+    z = rng.normal(0.0, 2.5, size=(nb * block, V))
+    st0 = _verify_rows(z)
+    draft = np.where(rng.random(nb * block) < 0.7, st0["argmax"], rng.integers(0, V - 1, nb * block))
+    st = O.verify_stats(z, V - 1, draft)
+    ex = O.accept(draft, st["argmax"], st["p_draft"], st["entropy"], O.ACCEPT_EXACT, 0.9, 0.6, block)
+    prev = None
+    for delta in (10.0, 3.0, 0.6, 0.1):
+        th = O.accept(draft, st["argmax"], st["p_draft"], st["entropy"], O.ACCEPT_THRESHOLD, 0.9, delta, block)
+        if prev is not None:                  # a more lenient rule never keeps fewer drafts
+            assert np.all(th["accept_len"] >= prev)
+        prev = th["accept_len"]
+    for b in range(nb):
+        r = ex["accept_len"][b]
+        toks = ex["tokens"][b * block:(b + 1) * block]
+        assert 0 <= r <= block - 1 and np.sum(toks >= 0) == r + 1
+        # exact matching reproduces the verifier's own greedy tokens
+        assert toks[:r + 1].tolist() == st["argmax"][b * block:b * block + r + 1].tolist()
+        assert np.all(toks[r + 1:] == -1)
