@@ -247,6 +247,8 @@ WORKLOADS = {
     "layer": "one Clover-shaped MoE layer (256 experts top-8 + shared, hidden 2,048, SwiGLU 512) on a "
              "32-position block, uniform routing",
     "head": "LM head + low-confidence unmask: 32 positions x hidden 2,048 into the untied 248,320-row head",
+    "accept": "verify-pass head + self-speculative accept test (exact rule): one block of 32 drafts (33 rows x hidden "
+              "2,048) into the untied 248,320-row head",
     "zipf": "batched and skewed routing: 8 blocks x 32 positions (256 tokens) through 40 Clover-shaped MoE "
             "layers + head, router biased to Zipf(1.2) expert popularity",
     "coreset": "full block denoising step as 'step' with the block coreset expert selection (top_p 0.9) in every "
@@ -268,7 +270,10 @@ def run_ours(args):
     kind = args.workload
     n_pos = 256 if kind in ("zipf", "zipf_layer") else M
     n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "layer": 1, "zipf_layer": 1,
-                "head": 0}[kind]
+                "head": 0, "accept": 0}[kind]
+    head_like = kind in ("head", "accept")
+    if kind == "accept":
+        n_pos = M + 1
     one_layer = kind in ("layer", "zipf_layer")
     full = kind in ("step", "zipf", "coreset")
     top_p = CORESET_TOP_P if kind == "coreset" else 0.0
@@ -286,8 +291,20 @@ def run_ours(args):
         ws = clover.workspace(clover.denoise_workspace_bytes(D, n_pos), dev)
     elif one_layer:
         ws = clover.workspace(clover.moe_workspace_bytes(D, n_pos), dev)
+    elif kind == "accept":
+        ws = clover.workspace(clover.accept_workspace_bytes(D, n_pos), dev)
     else:
         ws = clover.workspace(clover.head_workspace_bytes(D, n_pos), dev)
+    draft = acc_out = None
+    if kind == "accept":
+        # drafts: the head's own argmax with every fourth row replaced by a
+        # seeded random id (a stand-in for the preview pass's candidates)
+        acc_out = clover.lmhead_accept(D, head_w, x_fixed, torch.zeros(n_pos, dtype=torch.int32, device=dev), n_pos,
+                                       ws=ws)
+        g = torch.Generator(device="cpu").manual_seed(seed)
+        draft = acc_out["argmax"].clone()
+        draft[3::4] = torch.randint(0, D.vocab, (len(range(3, n_pos, 4)),), generator=g).to(torch.int32).to(dev)
+        draft[-1] = -1
 
     def reset():
         tokens.fill_(D.mask_id)
@@ -305,7 +322,10 @@ def run_ours(args):
         elif one_layer:
             clover.moe_block_step(D, layers[0], x_fixed, x_out=x_out, ws=ws, with_topk=False)
         else:
-            clover.lmhead_unmask(D, head_w, x_fixed, tokens, masked, block=M, ws=ws)
+            if kind == "accept":
+                clover.lmhead_accept(D, head_w, x_fixed, draft, n_pos, clover.ACCEPT_EXACT, ws=ws, out=acc_out)
+            else:
+                clover.lmhead_unmask(D, head_w, x_fixed, tokens, masked, block=M, ws=ws)
 
     for _ in range(args.warmup):
         step()
@@ -316,7 +336,7 @@ def run_ours(args):
 
     # ---- timed region: device time of K steps; per-launch events around the
     # dominant kernel (the expert kernel, or the whole head call)
-    per_step_launches = n_layers if kind != "head" else 1
+    per_step_launches = n_layers if not head_like else 1
     n_ev = args.steps * per_step_launches
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
@@ -340,18 +360,18 @@ def run_ours(args):
         # slower; it only feeds the roofline figure)
         reset()
         steps_in_block[0] = 0
-        if kind != "head":
+        if not head_like:
             clover.lib().clover_profile_expert_events(arr_b, arr_e, n_ev)
         start2.record(stream)
         for i in range(args.steps):
-            if kind == "head":
+            if head_like:
                 ev_b[i].record(stream)
             step()
-            if kind == "head":
+            if head_like:
                 ev_e[i].record(stream)
         end2.record(stream)
         torch.cuda.synchronize()
-        recorded = clover.lib().clover_profile_expert_events(None, None, 0) if kind != "head" else n_ev
+        recorded = clover.lib().clover_profile_expert_events(None, None, 0) if not head_like else n_ev
     _barrier(dist)
     clover.workspace_status(ws)
     ms = start.elapsed_time(end)
@@ -363,7 +383,7 @@ def run_ours(args):
     # are deterministic) and count the experts each launch touched.
     ebytes = D.expert_bytes
     u_per_launch = []
-    if kind == "head":
+    if head_like:
         alg = [D.head_bytes] * n_ev
     else:
         reset()
@@ -387,23 +407,28 @@ def run_ours(args):
     achieved = sum(alg) / (sum(durs) * 1e-3) / 1e9          # GB/s
     peak, peak_kind = _peaks()
     u_mean = float(np.mean(u_per_launch)) if u_per_launch else None
-    step_bytes = sum(alg) / args.steps + n_layers * D.router_bytes + (D.head_bytes if not one_layer else 0)
+    # (for the head workloads alg already is the head's bytes)
+    step_bytes = sum(alg) / args.steps + n_layers * D.router_bytes + (D.head_bytes if full else 0)
     share = sum(durs) / ms_instr
 
     # ---- end to end through the C ABI with host buffers
     h_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
     h_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
-    h_in = (x_fixed if one_layer or kind == "head" else ctx).cpu().pin_memory()
-    d_in = x_fixed if one_layer or kind == "head" else ctx
+    h_in = (x_fixed if one_layer or head_like else ctx).cpu().pin_memory()
+    d_in = x_fixed if one_layer or head_like else ctx
     o_tokens = torch.empty(n_pos, dtype=torch.int32).pin_memory()
     o_masked = torch.empty(n_pos, dtype=torch.uint8).pin_memory()
     o_x = torch.empty((n_pos, D.hidden), dtype=torch.float32).pin_memory()
+    h_draft = draft.cpu().pin_memory() if kind == "accept" else None
+    o_len = torch.empty(1, dtype=torch.int32).pin_memory()
     def e2e_step(s_):
         if full and s_ > 0 and s_ % M == 0:
             h_tokens.fill_(D.mask_id)
             h_masked.fill_(1)
         d_in.copy_(h_in, non_blocking=True)
-        if not one_layer:
+        if kind == "accept":
+            draft.copy_(h_draft, non_blocking=True)
+        elif not one_layer:
             tokens.copy_(h_tokens, non_blocking=True)
             masked.copy_(h_masked, non_blocking=True)
         if full:
@@ -412,6 +437,9 @@ def run_ours(args):
             step()
         if one_layer:
             o_x.copy_(x_out, non_blocking=True)
+        elif kind == "accept":
+            o_tokens.copy_(acc_out["tokens"], non_blocking=True)
+            o_len.copy_(acc_out["accept_len"][:1], non_blocking=True)
         else:
             o_tokens.copy_(tokens, non_blocking=True)
             o_masked.copy_(masked, non_blocking=True)
@@ -434,6 +462,8 @@ def run_ours(args):
     e2e_s = time.perf_counter() - t0
     if one_layer:
         h2d, d2h = n_pos * D.hidden * 4, n_pos * D.hidden * 4
+    elif kind == "accept":
+        h2d, d2h = n_pos * D.hidden * 4 + n_pos * 4, n_pos * 4 + 4
     else:
         h2d = n_pos * 4 + n_pos + n_pos * D.hidden * 4
         d2h = n_pos * 4 + n_pos
@@ -449,8 +479,10 @@ def run_ours(args):
     per_layer = 1 if n_pos <= 32 else 4
     launches_per_step = {"step": 1 + per_layer * n_layers + 2, "zipf": 1 + per_layer * n_layers + 2,
                          "coreset": 1 + per_layer * n_layers + 2, "layer": per_layer, "zipf_layer": per_layer,
-                         "head": 2}[kind]
+                         "head": 2, "accept": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
+                   else "k_head<accept> + k_rmsnorm (head statistics, entropy and the accept test)"
+                   if kind == "accept"
                    else "k_layer (routing + grouped SwiGLU experts + combine, one launch per MoE layer)"
                    if n_pos <= 32 else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")
     line = {
@@ -466,7 +498,7 @@ def run_ours(args):
                    "step_roofline_frac": step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": roof_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _expert_traffic(u_mean, n_pos <= 32) if kind != "head" else None,
+                     "traffic": _expert_traffic(u_mean, n_pos <= 32) if not head_like else None,
                      "launches": len(durs),
                      "mean_launch_us": float(np.mean(durs)) * 1e3, "share_of_step": share,
                      "ms_per_step_with_events": ms_instr / args.steps},

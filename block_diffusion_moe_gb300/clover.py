@@ -58,6 +58,13 @@ EXPORTS = {
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_int32, ctypes.c_void_p]),
+    "clover_accept_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),
+    "clover_lmhead_accept": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float,
+                                            ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_size_t, ctypes.c_void_p]),
     "clover_denoise_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),
     "clover_denoise_step": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.POINTER(MoeLayer), ctypes.c_int32,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -176,6 +183,38 @@ def lmhead_unmask(d: synth.Dims, head_w, x, tokens, masked, logit_scale=None, th
     _check(lib().clover_lmhead_unmask(ctypes.byref(dims), _ptr(head_w), _ptr(x), _ptr(logit_scale), threshold, block,
                                       _ptr(tokens), _ptr(masked), _ptr(out["argmax"]), _ptr(out["max_logit"]),
                                       _ptr(out["lse"]), _ptr(out["max_prob"]), _ptr(out["n_committed"]), M,
+                                      _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+ACCEPT_EXACT = 0
+ACCEPT_THRESHOLD = 1
+
+
+def accept_workspace_bytes(d: synth.Dims, max_rows: int) -> int:
+    return lib().clover_accept_workspace_bytes(ctypes.byref(make_dims(d)), max_rows)
+
+
+def lmhead_accept(d: synth.Dims, head_w, x, draft, block: int, rule: int = ACCEPT_EXACT, ratio: float = 0.9,
+                  delta: float = 0.6, logit_scale=None, ws=None, stream=None, out=None) -> dict:
+    """Verify-pass head + accept test over M = x.shape[0] rows in blocks of
+    `block` rows (block - 1 drafts + the boundary row). `out` (a dict this
+    function returned before, for the same M and block) is reused."""
+    M = x.shape[0]
+    dev = x.device
+    if ws is None:
+        ws = workspace(accept_workspace_bytes(d, M), dev)
+    if out is None:
+        f32 = lambda: torch.empty(M, dtype=torch.float32, device=dev)
+        out = {"argmax": torch.empty(M, dtype=torch.int32, device=dev), "max_logit": f32(), "lse": f32(),
+               "max_prob": f32(), "entropy": f32(), "p_draft": f32(),
+               "accept_len": torch.empty(max(1, M // max(block, 1)), dtype=torch.int32, device=dev),
+               "tokens": torch.empty(M, dtype=torch.int32, device=dev)}
+    dims = make_dims(d)
+    _check(lib().clover_lmhead_accept(ctypes.byref(dims), _ptr(head_w), _ptr(x), _ptr(logit_scale), _ptr(draft),
+                                      rule, ratio, delta, block, _ptr(out["argmax"]), _ptr(out["max_logit"]),
+                                      _ptr(out["lse"]), _ptr(out["max_prob"]), _ptr(out["entropy"]),
+                                      _ptr(out["p_draft"]), _ptr(out["accept_len"]), _ptr(out["tokens"]), M,
                                       _ptr(ws), ws.numel(), _stream(stream)))
     return out
 

@@ -90,10 +90,11 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
 }
 
 struct HeadLayout {
-  size_t xn, part_m, part_s, part_a, bytes;
+  size_t xn, part_m, part_s, part_a, part_t, part_zd, bytes;
 };
 
-HeadLayout head_layout(const clover_dims& d, int M) {
+// The accept form adds two more [G][M] partial arrays.
+HeadLayout head_layout(const clover_dims& d, int M, bool accept = false) {
   HeadLayout L;
   size_t o = 0;
   auto take = [&](size_t b) {
@@ -105,6 +106,8 @@ HeadLayout head_layout(const clover_dims& d, int M) {
   L.part_m = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
   L.part_s = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
   L.part_a = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
+  L.part_t = accept ? take(static_cast<size_t>(kHeadMaxCtas) * M * 4) : 0;
+  L.part_zd = accept ? take(static_cast<size_t>(kHeadMaxCtas) * M * 4) : 0;
   L.bytes = o;
   return L;
 }
@@ -395,11 +398,22 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   return CLOVER_OK;
 }
 
+// The accept test's inputs and outputs (null: the unmask rule).
+struct AcceptCfg {
+  const int32_t* draft;
+  int rule;
+  float ratio, delta;
+  float* entropy;
+  float* p_draft;
+  int32_t* accept_len;
+  int32_t* out_tokens;
+};
+
 int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, const float* alpha, float threshold,
                  int block, int32_t* tokens, uint8_t* masked, int32_t* argmax, float* max_logit, float* lse,
                  float* max_prob, int32_t* n_committed, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
-                 cudaStream_t stream) {
-  const HeadLayout L = head_layout(d, M);
+                 cudaStream_t stream, const AcceptCfg* acc = nullptr) {
+  const HeadLayout L = head_layout(d, M, acc != nullptr);
   bf16* xn = reinterpret_cast<bf16*>(data + L.xn);
   NormArgs na;
   na.x = x;
@@ -436,17 +450,30 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
   ha.block = block;
   ha.n_tiles = (d.vocab + 127) / 128;
   ha.threshold = threshold;
+  const bool accept = acc != nullptr;
+  if (accept) {
+    ha.draft = acc->draft;
+    ha.part_t = reinterpret_cast<float*>(data + L.part_t);
+    ha.part_zd = reinterpret_cast<float*>(data + L.part_zd);
+    ha.entropy = acc->entropy;
+    ha.p_draft = acc->p_draft;
+    ha.accept_len = acc->accept_len;
+    ha.out_tokens = acc->out_tokens;
+    ha.rule = acc->rule;
+    ha.ratio = acc->ratio;
+    ha.delta = acc->delta;
+  }
   const int nb = (M + 15) & ~15;
-  const size_t fixed = head_smem_bytes(0, nb) + 16 * 2 * 8;
+  const size_t fixed = head_smem_bytes(0, nb, accept) + 16 * 2 * 8;
   // 8 stages (128 KB of weights in flight per SM) streamed best on GB300.
   ha.stages = static_cast<int>(std::min<size_t>(
       8, (static_cast<size_t>(kSmemBudget) - fixed) / (kATileBytes + static_cast<size_t>(nb) * 128)));
   const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
-  // The final merge reuses the ring for 12 bytes x 32 positions x grid.
+  // The final merge reuses the ring for 12 (accept: 20) bytes x 32 positions x grid.
   if (static_cast<size_t>(ha.stages) * (kATileBytes + static_cast<size_t>(nb) * 128) <
-      static_cast<size_t>(grid) * 32 * 12)
+      static_cast<size_t>(grid) * 32 * (accept ? 20 : 12))
     return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
-  e = launch_head(ha, grid, head_smem_bytes(ha.stages, nb), stream, kPdl);
+  e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept), stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch head");
   return CLOVER_OK;
 }
@@ -590,6 +617,42 @@ int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const 
                     reinterpret_cast<cudaStream_t>(stream));
   if (rc) return rc;
   return check_launch_errors("lmhead unmask");
+}
+
+size_t clover_accept_workspace_bytes(const clover_dims* dims, int32_t max_rows) {
+  if (check_dims(dims) || check_tokens(max_rows)) return 0;
+  return kCtrlBytes + head_layout(*dims, max_rows, true).bytes;
+}
+
+int clover_lmhead_accept(const clover_dims* dims, const uint16_t* head_w, const float* x, const float* logit_scale,
+                         const int32_t* draft, int32_t rule, float ratio, float delta, int32_t block,
+                         int32_t* argmax, float* max_logit, float* lse, float* max_prob, float* entropy,
+                         float* p_draft, int32_t* accept_len, int32_t* out_tokens, int32_t M, void* workspace,
+                         size_t workspace_bytes, clover_stream_t stream) {
+  int rc;
+  if ((rc = check_dims(dims))) return rc;
+  if ((rc = check_tokens(M))) return rc;
+  if (!head_w || !x || !draft || !accept_len || !out_tokens)
+    return fail(CLOVER_ERR_INVALID_ARG, "NULL head_w/x/draft/accept_len/out_tokens");
+  if (!aligned16(head_w) || !aligned16(x)) return fail(CLOVER_ERR_INVALID_ARG, "head_w/x not 16-byte aligned");
+  if (block < 2 || M % block != 0)
+    return fail(CLOVER_ERR_INVALID_ARG, "block=%d: need >= 2 rows per block (drafts + 1) dividing M=%d", block, M);
+  if (rule != CLOVER_ACCEPT_EXACT && rule != CLOVER_ACCEPT_THRESHOLD)
+    return fail(CLOVER_ERR_INVALID_ARG, "rule=%d is neither exact nor threshold", rule);
+  if (rule == CLOVER_ACCEPT_THRESHOLD && !(ratio > 0.f && ratio <= 1.f && delta > 0.f && delta < 1e30f))
+    return fail(CLOVER_ERR_INVALID_ARG, "threshold rule needs 0 < ratio <= 1 and a finite delta > 0");
+  if ((rc = check_ws(workspace, workspace_bytes, kCtrlBytes + head_layout(*dims, M, true).bytes))) return rc;
+  if ((rc = get_encoder())) return rc;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* ctrl = reinterpret_cast<int*>(ws);
+  const AcceptCfg acc{draft, rule, ratio, delta, entropy, p_draft, accept_len, out_tokens};
+  rc = enqueue_head(*dims, head_w, x, logit_scale, 0.f, block, nullptr, nullptr, argmax, max_logit, lse, max_prob,
+                    nullptr, M, ws + kCtrlBytes, ctrl, ctrl + kCtrlErr, Plan{di.sms},
+                    reinterpret_cast<cudaStream_t>(stream), &acc);
+  if (rc) return rc;
+  return check_launch_errors("lmhead accept");
 }
 
 size_t clover_denoise_workspace_bytes(const clover_dims* dims, int32_t max_tokens) {

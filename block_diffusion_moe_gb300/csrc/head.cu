@@ -16,6 +16,15 @@
 // merges the G partial states in CTA order, derives log-sum-exp and the
 // maximum probability, and applies the unmask rule to every block of
 // positions. Ties in the argmax go to the lowest vocabulary id at every level.
+//
+// The accept form (section "Two ways to run it": self-speculative decoding
+// keeps the longest prefix of drafts that the causal pass accepts, plus one
+// token at the boundary; exact keeps a draft equal to the argmax, threshold
+// one whose probability is at least min(ratio, delta e^-H)) carries two more
+// per-position quantities through the same pipeline: t = sum of
+// e^(z - m) (z - m), from which the entropy is H = ln s - t / s, and the
+// draft token's logit. The last CTA then takes the accept test per block of
+// rows instead of the unmask rule.
 #include <math.h>
 
 #include "kernels.cuh"
@@ -35,6 +44,10 @@ struct HeadSmem {
   float* run_s;   // [nb]
   int* run_a;     // [nb]
   float* alpha;   // [nb]
+  float* wp_t;    // [4][nb] accept form only
+  float* wp_zd;   // [4][nb]
+  float* run_t;   // [nb]
+  float* run_zd;  // [nb]
   float* tr;      // [4][32][33] per-warp transpose tiles
   uint64_t *full, *empty, *tfull, *tempty, *drain;
   uint32_t* tmem_slot;
@@ -45,7 +58,7 @@ struct HeadSmem {
   uint32_t stage_bytes;
 };
 
-__device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int nb) {
+__device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int nb, bool accept) {
   HeadSmem s;
   const uint32_t r = smem_u32(raw);
   uint8_t* base = raw + ((1024u - (r & 1023u)) & 1023u);
@@ -59,7 +72,11 @@ __device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int n
   s.run_s = s.run_m + nb;
   s.run_a = reinterpret_cast<int*>(s.run_s + nb);
   s.alpha = reinterpret_cast<float*>(s.run_a + nb);
-  s.tr = s.alpha + nb;
+  s.wp_t = s.alpha + nb;
+  s.wp_zd = s.wp_t + (accept ? 4 * nb : 0);
+  s.run_t = s.wp_zd + (accept ? 4 * nb : 0);
+  s.run_zd = s.run_t + (accept ? nb : 0);
+  s.tr = s.run_zd + (accept ? nb : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.tr + 4 * 32 * 33);  // nb % 16 == 0 keeps 8-byte alignment
   s.full = bars;
   s.empty = s.full + p.stages;
@@ -86,6 +103,34 @@ __device__ __forceinline__ void lse_merge(float& m, float& s, int& a, float m2, 
     a = min(a, a2);
   } else {
     s += s2 * expf(m2 - m);
+  }
+}
+
+// lse_merge that also carries t = sum e^(z - m) (z - m), re-expressed at
+// the merged maximum: t' = e^(m - m') (t + (m - m') s). Empty states (m =
+// -inf, s = t = 0) are skipped, so no -inf x 0 product arises.
+__device__ __forceinline__ void lse_merge_t(float& m, float& s, float& t, int& a, float m2, float s2, float t2,
+                                            int a2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    t = t2;
+    a = a2;
+  } else if (m2 > m) {
+    const float f = expf(m - m2);
+    t = f * (t + (m - m2) * s) + t2;
+    s = s * f + s2;
+    m = m2;
+    a = a2;
+  } else if (m2 == m) {
+    s += s2;
+    t += t2;
+    a = min(a, a2);
+  } else {
+    const float f = expf(m2 - m);
+    t += f * (t2 + (m2 - m) * s2);
+    s += s2 * f;
   }
 }
 
@@ -178,7 +223,9 @@ __device__ void head_mma(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t 
 // serially: tile max, first row reaching it, and the sum of exp(z - max).
 // That folds into a running (max, sum, argmax) per column held in the lane's
 // registers across all of the CTA's tiles; warps never wait on each other
-// until the end.
+// until the end. The accept form also folds t and picks the draft's logit
+// out of the transposed tile.
+template <bool kAccept>
 __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t tmem_base) {
   constexpr int kMaxChunks = kMaxTokens / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -187,8 +234,8 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   const int etid = threadIdx.x - 64;  // 0..127
   const int nch = (nb + 31) >> 5;
   float* tr = s.tr + q * (32 * 33);
-  float rm[kMaxChunks], rs[kMaxChunks], al[kMaxChunks];
-  int ra[kMaxChunks];
+  float rm[kMaxChunks], rs[kMaxChunks], al[kMaxChunks], rt[kMaxChunks], rzd[kMaxChunks];
+  int ra[kMaxChunks], dr[kMaxChunks];
 #pragma unroll
   for (int ch = 0; ch < kMaxChunks; ++ch) {
     const int c = ch * 32 + lane;
@@ -196,6 +243,9 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
     rs[ch] = 0.f;
     ra[ch] = 0x7fffffff;
     al[ch] = (c < p.M && p.alpha != nullptr) ? p.alpha[c] : 1.0f;
+    rt[ch] = 0.f;
+    rzd[ch] = -INFINITY;
+    dr[ch] = (kAccept && c < p.M) ? p.draft[c] : -1;
   }
   bool ok = true;
   int it = 0;
@@ -247,12 +297,27 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
               a = row0 + r;
             }
           }
-          float sum = 0.f;
+          float sum = 0.f, t = 0.f;
           if (m != -INFINITY) {
 #pragma unroll
-            for (int r = 0; r < 32; ++r) sum += expf(z[r] - m);
+            for (int r = 0; r < 32; ++r) {
+              const float d = z[r] - m;
+              const float e = expf(d);
+              sum += e;
+              // a row at -inf has e = 0; the clamp keeps 0 x -inf out
+              if (kAccept) t = fmaf(e, fmaxf(d, -1e30f), t);
+            }
           }
-          lse_merge(rm[ch], rs[ch], ra[ch], m, sum, a);
+          if (kAccept) {
+            lse_merge_t(rm[ch], rs[ch], rt[ch], ra[ch], m, sum, t, a);
+            const int dj = dr[ch] - row0;
+            if (dj >= 0 && dj < 32) {
+              const float raw = tr[dj * 33 + lane];  // -inf for the mask token
+              rzd[ch] = (raw == -INFINITY) ? -INFINITY : raw * al[ch];
+            }
+          } else {
+            lse_merge(rm[ch], rs[ch], ra[ch], m, sum, a);
+          }
         }
       }
     }
@@ -269,17 +334,32 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
       s.wp_m[q * nb + c] = rm[ch];
       s.wp_s[q * nb + c] = rs[ch];
       s.wp_a[q * nb + c] = ra[ch];
+      if (kAccept) {
+        s.wp_t[q * nb + c] = rt[ch];
+        s.wp_zd[q * nb + c] = rzd[ch];
+      }
     }
   }
   named_bar_sync(1, 128);
   for (int c = etid; c < nb; c += 128) {
-    float m = -INFINITY, sm = 0.f;
+    float m = -INFINITY, sm = 0.f, t = 0.f, zd = -INFINITY;
     int a = 0x7fffffff;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) lse_merge(m, sm, a, s.wp_m[w * nb + c], s.wp_s[w * nb + c], s.wp_a[w * nb + c]);
+    for (int w = 0; w < 4; ++w) {
+      if (kAccept) {
+        lse_merge_t(m, sm, t, a, s.wp_m[w * nb + c], s.wp_s[w * nb + c], s.wp_t[w * nb + c], s.wp_a[w * nb + c]);
+        zd = fmaxf(zd, s.wp_zd[w * nb + c]);
+      } else {
+        lse_merge(m, sm, a, s.wp_m[w * nb + c], s.wp_s[w * nb + c], s.wp_a[w * nb + c]);
+      }
+    }
     s.run_m[c] = m;
     s.run_s[c] = sm;
     s.run_a[c] = a;
+    if (kAccept) {
+      s.run_t[c] = t;
+      s.run_zd[c] = zd;
+    }
   }
   (void)ok;
   // Leave together if any role gave up (the decision is broadcast so that no
@@ -292,9 +372,14 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   // Publish this CTA's partial state, then let the last CTA merge all of them.
   const int G = gridDim.x;
   for (int n = etid; n < p.M; n += 128) {
-    p.part_m[static_cast<size_t>(blockIdx.x) * p.M + n] = s.run_m[n];
-    p.part_s[static_cast<size_t>(blockIdx.x) * p.M + n] = s.run_s[n];
-    p.part_a[static_cast<size_t>(blockIdx.x) * p.M + n] = s.run_a[n];
+    const size_t g = static_cast<size_t>(blockIdx.x) * p.M + n;
+    p.part_m[g] = s.run_m[n];
+    p.part_s[g] = s.run_s[n];
+    p.part_a[g] = s.run_a[n];
+    if (kAccept) {
+      p.part_t[g] = s.run_t[n];
+      p.part_zd[g] = s.run_zd[n];
+    }
   }
   __threadfence();
   named_bar_sync(1, 128);
@@ -313,6 +398,8 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   float* pm_s = reinterpret_cast<float*>(s.ring);
   float* ps_s = pm_s + G * 32;
   int* pa_s = reinterpret_cast<int*>(ps_s + G * 32);
+  float* pt_s = reinterpret_cast<float*>(pa_s + G * 32);
+  float* pz_s = pt_s + G * 32;
   for (int n0 = 0; n0 < p.M; n0 += 32) {
     const int cnt = min(32, p.M - n0);
     for (int i = etid; i < G * cnt; i += 128) {
@@ -321,25 +408,68 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
       pm_s[b * 32 + j] = __ldcg(p.part_m + g);
       ps_s[b * 32 + j] = __ldcg(p.part_s + g);
       pa_s[b * 32 + j] = __ldcg(p.part_a + g);
+      if (kAccept) {
+        pt_s[b * 32 + j] = __ldcg(p.part_t + g);
+        pz_s[b * 32 + j] = __ldcg(p.part_zd + g);
+      }
     }
     named_bar_sync(1, 128);
     if (etid < cnt) {
       const int n = n0 + etid;
-      float m = -INFINITY, sm = 0.f;
+      float m = -INFINITY, sm = 0.f, t = 0.f, zd = -INFINITY;
       int a = 0x7fffffff;
-      for (int b = 0; b < G; ++b) lse_merge(m, sm, a, pm_s[b * 32 + etid], ps_s[b * 32 + etid], pa_s[b * 32 + etid]);
+      for (int b = 0; b < G; ++b) {
+        if (kAccept) {
+          lse_merge_t(m, sm, t, a, pm_s[b * 32 + etid], ps_s[b * 32 + etid], pt_s[b * 32 + etid],
+                      pa_s[b * 32 + etid]);
+          zd = fmaxf(zd, pz_s[b * 32 + etid]);
+        } else {
+          lse_merge(m, sm, a, pm_s[b * 32 + etid], ps_s[b * 32 + etid], pa_s[b * 32 + etid]);
+        }
+      }
       const float lse = m + logf(sm);
       const float pmax = 1.0f / sm;  // = exp(m - lse)
       if (p.argmax) p.argmax[n] = a;
       if (p.max_logit) p.max_logit[n] = m;
       if (p.lse) p.lse[n] = lse;
       if (p.max_prob) p.max_prob[n] = pmax;
-      s.run_m[n] = pmax;  // reuse: per-position max probability
+      if (kAccept) {
+        const float ent = fmaxf(logf(sm) - t / sm, 0.f);  // t <= 0
+        const float pd = expf(zd - lse);                   // 0 for a draft never seen
+        if (p.entropy) p.entropy[n] = ent;
+        if (p.p_draft) p.p_draft[n] = pd;
+        s.run_m[n] = pd;
+        s.run_s[n] = ent;
+      } else {
+        s.run_m[n] = pmax;  // reuse: per-position max probability
+      }
       s.run_a[n] = a;
     }
     named_bar_sync(1, 128);
   }
   named_bar_sync(1, 128);
+  if (kAccept) {
+    // Accept test, one thread per block of rows: the longest prefix of
+    // accepted drafts, then the boundary row's argmax.
+    const int nblk = p.M / p.block;
+    for (int b = etid; b < nblk; b += 128) {
+      const int p0 = b * p.block;
+      int r = 0;
+      while (r < p.block - 1) {
+        const int i = p0 + r;
+        const bool acc = (p.rule == 0) ? (p.draft[i] == s.run_a[i])
+                                       : (s.run_m[i] >= fminf(p.ratio, p.delta * expf(-s.run_s[i])));
+        if (!acc) break;
+        ++r;
+      }
+      p.accept_len[b] = r;
+      for (int j = 0; j < p.block; ++j)
+        p.out_tokens[p0 + j] = (j < r) ? p.draft[p0 + j] : (j == r ? s.run_a[p0 + j] : -1);
+    }
+    named_bar_sync(1, 128);
+    if (etid == 0) *p.done_ctr = 0;
+    return;
+  }
   // Unmask rule, one thread per block of positions.
   const int nblk = (p.M + p.block - 1) / p.block;
   for (int b = etid; b < nblk; b += 128) {
@@ -380,10 +510,11 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
 
 }  // namespace
 
+template <bool kAccept>
 __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant__ HeadArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const int nb = (p.M + 15) & ~15;
-  const HeadSmem s = carve(smem_raw, p, nb);
+  const HeadSmem s = carve(smem_raw, p, nb, kAccept);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages; ++i) {
@@ -418,7 +549,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
   } else if (warp == 1) {
     if (lane == 0) head_mma(p, s, nb, tmem_base);
   } else {
-    head_epilogue(p, s, nb, tmem_base);
+    head_epilogue<kAccept>(p, s, nb, tmem_base);
   }
   tc_fence_before();
   __syncthreads();
@@ -429,16 +560,17 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
   }
 }
 
-size_t head_smem_bytes(int stages, int nb) {
+size_t head_smem_bytes(int stages, int nb, bool accept) {
   return 1024 + static_cast<size_t>(stages) * (kATileBytes + static_cast<size_t>(nb) * 128) +
-         static_cast<size_t>(nb) * (4 * 12 + 12 + 4) + 4 * 32 * 33 * sizeof(float) +
+         static_cast<size_t>(nb) * (4 * 12 + 12 + 4 + (accept ? 4 * 8 + 8 : 0)) + 4 * 32 * 33 * sizeof(float) +
          static_cast<size_t>(2 * stages + 5) * 8 + 64;
 }
 
-cudaError_t launch_head(const HeadArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(k_head, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  auto* k = accept ? k_head<true> : k_head<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_kernel(k_head, dim3(grid), dim3(kHeadThreads), smem, s, pdl, a);
+  return launch_kernel(k, dim3(grid), dim3(kHeadThreads), smem, s, pdl, a);
 }
 
 }  // namespace clover

@@ -156,6 +156,17 @@ struct HeadArgs {
   int* err;
   int M, H, V, mask_id, block, n_tiles, stages;
   float threshold;
+  // Accept mode (self-speculative verify): blocks of `block` rows, row j
+  // testing draft[j]; the unmask fields above are unused then.
+  const int32_t* draft;  // [M]
+  float* part_t;         // [G][M] sum of e^(z - m) (z - m)
+  float* part_zd;        // [G][M] the draft's logit (-inf where not seen)
+  float* entropy;        // [M] out (nullable)
+  float* p_draft;        // [M] out (nullable)
+  int32_t* accept_len;   // [M / block] out
+  int32_t* out_tokens;   // [M] out
+  int rule;              // 0 exact, 1 threshold
+  float ratio, delta;
 };
 
 // Launch wrappers (return the cudaError_t of the launch).
@@ -169,9 +180,10 @@ cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_
 size_t layer_rt_bytes(int M, int K, int E);
 // Largest token count the fused layer kernel takes (one 32-bit mask per expert).
 constexpr int kLayerMaxTokens = 32;
-cudaError_t launch_head(const HeadArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
+// Launches the unmask or the accept form of the head kernel.
+cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl);
 
 size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max);
-size_t head_smem_bytes(int stages, int nb);
+size_t head_smem_bytes(int stages, int nb, bool accept);
 
 }  // namespace clover

@@ -134,6 +134,44 @@ int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const 
                          int32_t* n_committed, int32_t M,
                          void* workspace, size_t workspace_bytes, clover_stream_t stream);
 
+/* Accept rules of clover_lmhead_accept. */
+#define CLOVER_ACCEPT_EXACT 0
+#define CLOVER_ACCEPT_THRESHOLD 1
+
+/* Bytes of workspace clover_lmhead_accept needs for up to max_rows rows.
+ * Host-only. */
+size_t clover_accept_workspace_bytes(const clover_dims* dims, int32_t max_rows);
+
+/* Output head of a verify pass fused with the self-speculative accept test
+ * (Files, "Two ways to run it": a round keeps the longest prefix of drafts
+ * the causal pass accepts, plus one token at the boundary; the exact rule
+ * keeps a draft only if it is the causal pass's argmax, the threshold rule
+ * if its probability is at least min(ratio, delta e^-H), H the entropy of the
+ * causal distribution, defaults ratio 0.9 and delta 0.6).
+ * The M rows form M / block blocks; in each, row j < block - 1 is the
+ * distribution draft[j] is tested against and the last row gives the token
+ * after the final draft. Per row, as clover_lmhead_unmask (mask token at
+ * -inf): argmax, max_logit, lse, max_prob, plus
+ *   entropy_p = -sum_v p_v ln p_v  (p = softmax of z_p),
+ *   p_draft_p = p at draft[p]      (0 for the mask token or an id outside
+ *                                   [0, V); the last row of a block: ignored)
+ * Per block b: accept_len[b] = r, the number of leading rows whose draft is
+ * accepted (exact: draft == argmax; threshold: p_draft >= min(ratio,
+ * delta e^-entropy), fp32), and out_tokens[b*block + j] = draft for j < r,
+ * argmax of row r at j = r, -1 after (r + 1 tokens).
+ * head_w: bf16 [V][H]. x: fp32 [M][H] (pre-norm). logit_scale: fp32 [M] or
+ * NULL. draft: int32 [M], in. rule: CLOVER_ACCEPT_EXACT or
+ * CLOVER_ACCEPT_THRESHOLD (then 0 < ratio <= 1 and a finite delta > 0).
+ * argmax, max_logit, lse, max_prob, entropy, p_draft: [M] out, each may be
+ * NULL. accept_len int32 [M / block], out_tokens int32 [M]: out. Requires
+ * block >= 2 and M % block == 0. */
+int clover_lmhead_accept(const clover_dims* dims, const uint16_t* head_w, const float* x,
+                         const float* logit_scale, const int32_t* draft, int32_t rule, float ratio,
+                         float delta, int32_t block,
+                         int32_t* argmax, float* max_logit, float* lse, float* max_prob,
+                         float* entropy, float* p_draft, int32_t* accept_len, int32_t* out_tokens,
+                         int32_t M, void* workspace, size_t workspace_bytes, clover_stream_t stream);
+
 /* Bytes of workspace the denoise entry points need. Host-only. */
 size_t clover_denoise_workspace_bytes(const clover_dims* dims, int32_t max_tokens);
 

@@ -152,3 +152,33 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(C, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         C.lib()
+
+
+def test_accept_arg_checks(lib):
+    d = _dims()
+    need = lib.clover_accept_workspace_bytes(ctypes.byref(d), 33)
+    assert need > lib.clover_head_workspace_bytes(ctypes.byref(d), 33)
+    assert lib.clover_accept_workspace_bytes(ctypes.byref(d), 0) == 0
+    assert lib.clover_accept_workspace_bytes(ctypes.byref(d), 257) == 0
+    f = lib.clover_lmhead_accept
+    #      dims          head_w   x        scale draft   rule ratio delta block
+    base = [ctypes.byref(d), 0x10000, 0x20000, None, 0x30000, 1, 0.9, 0.6, 33,
+            None, None, None, None, None, None, 0x40000, 0x50000, 33, 0x100000, need, None]
+
+    def call(**kw):
+        a = list(base)
+        pos = {"draft": 4, "rule": 5, "ratio": 6, "delta": 7, "block": 8, "accept_len": 15, "M": 17, "ws_bytes": 19}
+        for k, v in kw.items():
+            a[pos[k]] = v
+        return f(*a)
+
+    assert call(block=1) == C.ERR_INVALID_ARG                  # no draft row
+    assert call(block=10) == C.ERR_INVALID_ARG                 # does not divide M
+    assert call(rule=3) == C.ERR_INVALID_ARG
+    assert call(delta=0.0) == C.ERR_INVALID_ARG
+    assert call(ratio=1.5) == C.ERR_INVALID_ARG
+    assert call(delta=float("inf")) == C.ERR_INVALID_ARG
+    assert call(draft=None) == C.ERR_INVALID_ARG
+    assert call(accept_len=None) == C.ERR_INVALID_ARG
+    assert call(M=300, block=30) == C.ERR_UNSUPPORTED_SHAPE
+    assert call(ws_bytes=need - 1) == C.ERR_WORKSPACE_TOO_SMALL
