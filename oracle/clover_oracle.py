@@ -68,8 +68,18 @@ Readings where the pages are silent (each is listed in the design doc):
   probability zero, so it is never accepted; a draft id outside the
   vocabulary is never accepted either.
 
-All float arithmetic is numpy float64; bf16 tensors arrive as uint16 arrays
-holding their bit patterns.
+* Low-bit expert weights (SURVEY's NEXT 4; the pages name INT4 for one
+  deployment but give no format, so this format is the build's own): each
+  expert matrix [R][K] keeps one bf16 scale per row and group of 64
+  consecutive K elements, s = bf16(float32(max |w|) / 7) (fp32 IEEE division,
+  then round to nearest even), and per element the 4-bit code
+  u = clamp(rint(float32(w) / float32(s)), -8, 7) + 8 (u = 8 where s = 0).
+  The weight the product uses is bf16((u - 8) s). Codes are packed eight to a
+  32-bit little-endian word in the nibble order e0 e2 e4 e6 e1 e3 e5 e7
+  (nibble i at bits 4i); scales are stored group-major, [K/64][R].
+
+All float arithmetic is numpy float64 unless stated; bf16 tensors arrive as
+uint16 arrays holding their bit patterns.
 """
 from __future__ import annotations
 
@@ -362,6 +372,52 @@ def accept(draft, argmax, p_draft, entropy, rule: int, ratio: float, delta: floa
         out[b * block:b * block + r] = draft[b * block:b * block + r]
         out[b * block + r] = argmax[b * block + r]
     return {"accepted": ok, "accept_len": acc_len, "tokens": out}
+
+
+Q4_GROUP = 64
+_Q4_NIBBLE_OF = np.array([0, 2, 4, 6, 1, 3, 5, 7])   # element held by nibble i of a word
+
+
+def quantize_q4(w_bits):
+    """bf16 matrix [R][K] (K % 64 == 0) -> (packed codes uint8 [R][K/2],
+    scale bits uint16 [K/64][R]) in the low-bit format above."""
+    w = bf16_to_f64(w_bits).astype(np.float32)
+    R, K = w.shape
+    g = w.reshape(R, K // Q4_GROUP, Q4_GROUP)
+    amax = np.abs(g).max(axis=2)                                   # exact
+    s32 = (amax / np.float32(7.0)).astype(np.float32)              # fp32 IEEE division
+    s_bits = bf16_bits_of(s32)
+    s = bf16_to_f64(s_bits).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(g / s[:, :, None]).astype(np.float32)          # fp32 division, half to even
+    q = np.where(s[:, :, None] > 0, q, 0.0)
+    u = (np.clip(q, -8, 7) + 8).astype(np.uint32).reshape(R, K // 8, 8)
+    words = np.zeros((R, K // 8), dtype=np.uint32)
+    for i in range(8):
+        words |= u[:, :, _Q4_NIBBLE_OF[i]] << np.uint32(4 * i)
+    packed = words.astype("<u4").view(np.uint8).reshape(R, K // 2)
+    return packed, np.ascontiguousarray(s_bits.T)
+
+
+def dequantize_q4(packed, scale_bits) -> np.ndarray:
+    """Packed codes [R][K/2] + scale bits [K/64][R] -> the bf16 bit patterns
+    [R][K] of bf16((u - 8) s)."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    R = packed.shape[0]
+    K = packed.shape[1] * 2
+    words = packed.view("<u4").reshape(R, K // 8)
+    u = np.empty((R, K // 8, 8), dtype=np.int64)
+    for i in range(8):
+        u[:, :, _Q4_NIBBLE_OF[i]] = (words >> np.uint32(4 * i)) & 0xF
+    s = bf16_to_f64(np.asarray(scale_bits).T)                      # [R][K/64]
+    w = (u.reshape(R, K) - 8) * np.repeat(s, Q4_GROUP, axis=1)     # exact in float64
+    return bf16_bits_of(w)
+
+
+def bf16_bits_of(x) -> np.ndarray:
+    """float array -> bf16 bit patterns (round to nearest even)."""
+    y = np.ascontiguousarray(round_to_bf16(np.asarray(x, dtype=np.float64)), dtype=np.float32)
+    return (y.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
 
 
 def embed(tokens, embed_bits, ctx) -> np.ndarray:

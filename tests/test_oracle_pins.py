@@ -545,3 +545,72 @@ def test_accept_invariants():
         # exact matching reproduces the verifier's own greedy tokens
         assert toks[:r + 1].tolist() == st["argmax"][b * block:b * block + r + 1].tolist()
         assert np.all(toks[r + 1:] == -1)
+
+
+# ---------------------------------------------------------------------------
+# Low-bit expert weight format (SURVEY's NEXT 4; the build's own format)
+
+
+def _bf16_bits(x):
+    return O.bf16_bits_of(np.asarray(x, dtype=np.float64))
+
+
+def test_q4_round_trip_is_exact_on_the_grid():
+    # each group holds multiples of 2^-6 from -7 to 7 with its maximum at 7:
+    # the scale is exactly 2^-6, the codes are the multiples, dequant is exact
+    rng = np.random.default_rng(6)
+    k = rng.integers(-7, 8, size=(3, 128)).astype(np.float64)
+    k[:, 0] = 7
+    k[:, 64] = -7
+    w = _bf16_bits(k * 2.0 ** -6)
+    packed, s = O.quantize_q4(w)
+    assert s.shape == (2, 3) and np.all(O.bf16_to_f64(s) == 2.0 ** -6)
+    assert np.array_equal(O.dequantize_q4(packed, s), w)
+
+
+def test_q4_packing_order_hand_example():
+    # codes u = 1..8 for elements 0..7 of row 0: nibble i holds element
+    # (0, 2, 4, 6, 1, 3, 5, 7)[i], so the word is 0x86427531
+    k = np.zeros((1, 64))
+    k[0, :8] = np.arange(1, 9) - 8          # q = u - 8
+    k[0, 8] = 7                             # sets the group maximum: s = 2^-6 below
+    w = _bf16_bits(k * 2.0 ** -6)
+    packed, s = O.quantize_q4(w)
+    assert O.bf16_to_f64(s)[0, 0] == 2.0 ** -6
+    assert packed[0, :4].tolist() == [0x31, 0x75, 0x42, 0x86]
+    assert packed[0, 4] & 0xF == 7 + 8      # element 8 is nibble 0 of the next word
+
+
+def test_q4_error_bound_and_extremes():
+    rng = np.random.default_rng(7)
+    w = _bf16_bits(rng.normal(0.0, 0.02, size=(5, 256)))
+    w[2, 64:128] = 0                        # an all-zero group
+    packed, s = O.quantize_q4(w)
+    sv = O.bf16_to_f64(s).T                 # [R][K/64]
+    wd = O.bf16_to_f64(O.dequantize_q4(packed, s))
+    wf = O.bf16_to_f64(w)
+    step = np.repeat(sv, 64, axis=1)
+    assert np.all(np.abs(wd - wf) <= step / 2 + np.abs(wd) * 2.0 ** -8 + 1e-30)
+    assert sv[2, 1] == 0 and np.all(wd[2, 64:128] == 0)
+    words = packed.view("<u4")
+    codes = np.stack([(words >> (4 * i)) & 0xF for i in range(8)], axis=-1)
+    assert codes.min() >= 1 and codes.max() <= 15   # |q| <= 7 with the /7 scale
+    # the element of largest magnitude in every live group gets code +-7
+    el = np.empty((5, 256), dtype=np.int64)           # codes in element order
+    nib = (0, 2, 4, 6, 1, 3, 5, 7)
+    for i in range(8):
+        el.reshape(5, 32, 8)[:, :, nib[i]] = codes[:, :, i]
+    g = wf.reshape(5, 4, 64)
+    at_max = el.reshape(5, 4, 64)[np.arange(5)[:, None], np.arange(4)[None, :], np.abs(g).argmax(axis=2)]
+    live = np.abs(g).max(axis=2) > 0
+    assert np.all(np.abs(at_max[live] - 8) == 7)
+
+
+def test_q4_scales_are_group_major():
+    k = np.zeros((2, 128))
+    k[0, 3] = 7 * 2.0 ** -4                 # row 0 group 0: s = 2^-4
+    k[1, 70] = 7 * 2.0 ** -2                # row 1 group 1: s = 2^-2
+    packed, s = O.quantize_q4(_bf16_bits(k))
+    sv = O.bf16_to_f64(s)
+    assert s.shape == (2, 2)
+    assert sv[0, 0] == 2.0 ** -4 and sv[1, 1] == 2.0 ** -2 and sv[0, 1] == 0 and sv[1, 0] == 0
