@@ -52,11 +52,12 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _expert_traffic(u_mean, fused):
+def _expert_traffic(u_mean, fused, q4=False):
     """DRAM bytes per expert-kernel launch from the committed ncu summary of
     that kernel (bytes per expert x experts per launch), if the summary was
     taken on the current kernel source; else None."""
-    name = "moe_layer_fused_clover_block32.md" if fused else "moe_layer_standalone_zipf256.md"
+    name = ("moe_layer_fused_int4_clover_block32.md" if q4 else
+            "moe_layer_fused_clover_block32.md" if fused else "moe_layer_standalone_zipf256.md")
     path = os.path.join(ROOT, "profiles", name)
     src = os.path.join(ROOT, "block_diffusion_moe_gb300", "csrc", "expert.cu")
     try:
@@ -253,6 +254,8 @@ WORKLOADS = {
             "layers + head, router biased to Zipf(1.2) expert popularity",
     "coreset": "full block denoising step as 'step' with the block coreset expert selection (top_p 0.9) in every "
                "MoE layer",
+    "int4": "full block denoising step as 'step' with every expert's weights in the 4-bit format (4-bit codes, one "
+            "bf16 scale per 64 weights: 1,671,168 B per expert instead of 6,291,456 B)",
     "zipf_layer": "one Clover-shaped MoE layer on 8 blocks x 32 positions (256 tokens), router biased to Zipf(1.2) "
                   "expert popularity (the standalone routing and expert kernels)",
 }
@@ -269,16 +272,22 @@ def run_ours(args):
     seed = 1000 + rank
     kind = args.workload
     n_pos = 256 if kind in ("zipf", "zipf_layer") else M
-    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "layer": 1, "zipf_layer": 1,
+    n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "int4": D.n_layers, "layer": 1,
+                "zipf_layer": 1,
                 "head": 0, "accept": 0}[kind]
     head_like = kind in ("head", "accept")
     if kind == "accept":
         n_pos = M + 1
     one_layer = kind in ("layer", "zipf_layer")
-    full = kind in ("step", "zipf", "coreset")
+    full = kind in ("step", "zipf", "coreset", "int4")
     top_p = CORESET_TOP_P if kind == "coreset" else 0.0
     zipf = 1.2 if kind in ("zipf", "zipf_layer") else None
     layers = [synth.make_layer(D, seed, l, dev, zipf_s=zipf) for l in range(n_layers)]
+    if kind == "int4":
+        # the library's own quantizer; the bf16 expert weights are dropped after
+        layers = [clover.quantize_layer_q4(L) for L in layers]
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     head_w = synth.make_head(D, seed, dev) if not one_layer else None
     embed = synth.make_embed(D, seed, dev) if full else None
     model = clover.Model(D, layers, embed, head_w, coreset_top_p=top_p) if full else None
@@ -381,7 +390,8 @@ def run_ours(args):
 
     # ---- algorithmic bytes: replay the same steps layer by layer (the kernels
     # are deterministic) and count the experts each launch touched.
-    ebytes = D.expert_bytes
+    # per expert: bf16 weights, or 4-bit codes + one bf16 scale per 64 weights
+    ebytes = D.expert_bytes if kind != "int4" else D.expert_params // 2 + D.expert_params // 64 * 2
     u_per_launch = []
     if head_like:
         alg = [D.head_bytes] * n_ev
@@ -478,7 +488,7 @@ def run_ours(args):
     # <= 32 positions: one fused launch per layer; more: route, perm, experts, combine
     per_layer = 1 if n_pos <= 32 else 4
     launches_per_step = {"step": 1 + per_layer * n_layers + 2, "zipf": 1 + per_layer * n_layers + 2,
-                         "coreset": 1 + per_layer * n_layers + 2, "layer": per_layer, "zipf_layer": per_layer,
+                         "coreset": 1 + per_layer * n_layers + 2, "int4": 1 + per_layer * n_layers + 2, "layer": per_layer, "zipf_layer": per_layer,
                          "head": 2, "accept": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
                    else "k_head<accept> + k_rmsnorm (head statistics, entropy and the accept test)"
@@ -498,7 +508,7 @@ def run_ours(args):
                    "step_roofline_frac": step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": roof_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _expert_traffic(u_mean, n_pos <= 32) if not head_like else None,
+                     "traffic": _expert_traffic(u_mean, n_pos <= 32, kind == "int4") if not head_like else None,
                      "launches": len(durs),
                      "mean_launch_us": float(np.mean(durs)) * 1e3, "share_of_step": share,
                      "ms_per_step_with_events": ms_instr / args.steps},

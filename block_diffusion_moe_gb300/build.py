@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libclover.so")
-SOURCES = ["api.cu", "route.cu", "expert.cu", "head.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "expert.cu", "head.cu", "noalloc.cu", "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]

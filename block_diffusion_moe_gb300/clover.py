@@ -39,7 +39,10 @@ class Dims(ctypes.Structure):
 
 class MoeLayer(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p), ("gate_up", ctypes.c_void_p),
-                ("down", ctypes.c_void_p), ("sh_gate_up", ctypes.c_void_p), ("sh_down", ctypes.c_void_p)]
+                ("down", ctypes.c_void_p), ("sh_gate_up", ctypes.c_void_p), ("sh_down", ctypes.c_void_p),
+                ("gate_up_q", ctypes.c_void_p), ("gate_up_s", ctypes.c_void_p), ("down_q", ctypes.c_void_p),
+                ("down_s", ctypes.c_void_p), ("sh_gate_up_q", ctypes.c_void_p), ("sh_gate_up_s", ctypes.c_void_p),
+                ("sh_down_q", ctypes.c_void_p), ("sh_down_s", ctypes.c_void_p)]
 
 
 EXPORTS = {
@@ -58,6 +61,8 @@ EXPORTS = {
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_int32, ctypes.c_void_p]),
+    "clover_quantize_q4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "clover_accept_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),
     "clover_lmhead_accept": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.c_void_p, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_float,
@@ -124,13 +129,55 @@ def make_dims(d: synth.Dims, coreset_top_p: float = 0.0) -> Dims:
     return Dims(d.hidden, d.n_experts, d.top_k, d.d_ff, d.vocab, d.mask_id, d.rms_eps, coreset_top_p)
 
 
-def make_layer(L: synth.Layer) -> MoeLayer:
-    for t in (L.router_w, L.gate_up, L.down, L.sh_gate_up, L.sh_down):
-        assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+class Q4Layer:
+    """A layer whose expert weights are in the low-bit format
+    (clover_quantize_q4): codes uint8 and scales int16 (bf16 bits), device
+    tensors; the router stays bf16."""
+
+    def __init__(self, router_w, router_bias, gate_up_q, gate_up_s, down_q, down_s, sh_gate_up_q, sh_gate_up_s,
+                 sh_down_q, sh_down_s):
+        self.router_w, self.router_bias = router_w, router_bias
+        self.gate_up_q, self.gate_up_s, self.down_q, self.down_s = gate_up_q, gate_up_s, down_q, down_s
+        self.sh_gate_up_q, self.sh_gate_up_s, self.sh_down_q, self.sh_down_s = (sh_gate_up_q, sh_gate_up_s,
+                                                                                sh_down_q, sh_down_s)
+
+
+def quantize_q4(w, stream=None):
+    """bf16 [n_mats][rows][cols] (or [rows][cols]) -> (codes uint8
+    [..][rows][cols/2], scales int16 [..][cols/64][rows]) on the device."""
+    assert w.is_cuda and w.dtype == torch.bfloat16 and w.is_contiguous()
+    shape = tuple(w.shape)
+    w3 = w.view(1, *shape) if w.dim() == 2 else w
+    n, rows, cols = w3.shape
+    q = torch.empty((n, rows, cols // 2), dtype=torch.uint8, device=w.device)
+    sc = torch.empty((n, cols // 64, rows), dtype=torch.int16, device=w.device)
+    _check(lib().clover_quantize_q4(_ptr(w3), n, rows, cols, _ptr(q), _ptr(sc), _stream(stream)))
+    if w.dim() == 2:
+        return q[0], sc[0]
+    return q, sc
+
+
+def quantize_layer_q4(L: synth.Layer, stream=None) -> Q4Layer:
+    gq, gs = quantize_q4(L.gate_up, stream)
+    dq, ds = quantize_q4(L.down, stream)
+    sgq, sgs = quantize_q4(L.sh_gate_up, stream)
+    sdq, sds = quantize_q4(L.sh_down, stream)
+    return Q4Layer(L.router_w, L.router_bias, gq, gs, dq, ds, sgq, sgs, sdq, sds)
+
+
+def make_layer(L) -> MoeLayer:
     if L.router_bias is not None:
         assert L.router_bias.is_cuda and L.router_bias.dtype == torch.float32
-    return MoeLayer(L.router_w.data_ptr(), None if L.router_bias is None else L.router_bias.data_ptr(),
-                    L.gate_up.data_ptr(), L.down.data_ptr(), L.sh_gate_up.data_ptr(), L.sh_down.data_ptr())
+    bias = None if L.router_bias is None else L.router_bias.data_ptr()
+    if isinstance(L, Q4Layer):
+        ts = (L.gate_up_q, L.gate_up_s, L.down_q, L.down_s, L.sh_gate_up_q, L.sh_gate_up_s, L.sh_down_q, L.sh_down_s)
+        for t in ts:
+            assert t.is_cuda and t.is_contiguous()
+        return MoeLayer(L.router_w.data_ptr(), bias, None, None, None, None, *[t.data_ptr() for t in ts])
+    for t in (L.router_w, L.gate_up, L.down, L.sh_gate_up, L.sh_down):
+        assert t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+    return MoeLayer(L.router_w.data_ptr(), bias, L.gate_up.data_ptr(), L.down.data_ptr(), L.sh_gate_up.data_ptr(),
+                    L.sh_down.data_ptr())
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:

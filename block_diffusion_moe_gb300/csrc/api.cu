@@ -153,10 +153,17 @@ int check_tokens(int M) {
   return CLOVER_OK;
 }
 
+bool layer_is_q4(const clover_moe_layer& l) { return l.gate_up_q != nullptr; }
+
 int check_layer(const clover_moe_layer* l, int i) {
   if (l == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "layer %d is NULL", i);
-  const void* ps[] = {l->router_w, l->gate_up, l->down, l->sh_gate_up, l->sh_down};
-  for (const void* p : ps) {
+  const void* bf[] = {l->router_w, l->gate_up, l->down, l->sh_gate_up, l->sh_down};
+  const void* q4[] = {l->router_w, l->gate_up_q, l->gate_up_s, l->down_q, l->down_s, l->sh_gate_up_q,
+                      l->sh_gate_up_s, l->sh_down_q, l->sh_down_s};
+  const bool low = layer_is_q4(*l);
+  const int n = low ? 9 : 5;
+  for (int k = 0; k < n; ++k) {
+    const void* p = low ? q4[k] : bf[k];
     if (p == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "layer %d: NULL weight pointer", i);
     if (!aligned16(p)) return fail(CLOVER_ERR_INVALID_ARG, "layer %d: weight pointer not 16-byte aligned", i);
   }
@@ -216,6 +223,24 @@ int encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CLOVER_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
+  return CLOVER_OK;
+}
+
+// 4-bit codes as bytes: rows of `cols_bytes`, boxes of box_cols bytes x
+// box_rows (the converter warps read them).
+int encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols_bytes, uint32_t box_cols,
+                 uint32_t box_rows, const char* what) {
+  cuuint64_t dims[2] = {cols_bytes, rows};
+  cuuint64_t strides[1] = {cols_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  // 128-byte rows take the 128-byte swizzle (16-byte chunk c of row r at
+  // chunk c ^ (r % 8)), so the converter's row reads do not share banks
+  const CUtensorMapSwizzle sw = box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(CLOVER_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
   return CLOVER_OK;
@@ -306,10 +331,34 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   memset(&xa, 0, sizeof(xa));
   const int R = MK + M;
   int rc;
-  if ((rc = encode_bf16_2d(&xa.tm_gu, layer.gate_up, static_cast<uint64_t>(E) * 2 * F, H, 64, "gate_up"))) return rc;
-  if ((rc = encode_bf16_2d(&xa.tm_sgu, layer.sh_gate_up, 2ull * F, H, 64, "shared gate_up"))) return rc;
-  if ((rc = encode_bf16_2d(&xa.tm_dn, layer.down, static_cast<uint64_t>(E) * H, F, 128, "down"))) return rc;
-  if ((rc = encode_bf16_2d(&xa.tm_sdn, layer.sh_down, H, F, 128, "shared down"))) return rc;
+  const bool q4 = layer_is_q4(layer);
+  if (q4) {
+    // K groups per staging slot: the largest of 4, 2, 1 dividing the groups
+    auto slot_groups = [](int groups) { return groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : 1); };
+    xa.kq_gu = slot_groups(H / 64);
+    xa.kq_dn = slot_groups(F / 64);
+    if ((rc = encode_u8_2d(&xa.tm_gu_q, layer.gate_up_q, static_cast<uint64_t>(E) * 2 * F, H / 2, xa.kq_gu * 32, 64,
+                           "gate_up codes")))
+      return rc;
+    if ((rc = encode_u8_2d(&xa.tm_sgu_q, layer.sh_gate_up_q, 2ull * F, H / 2, xa.kq_gu * 32, 64,
+                           "shared gate_up codes")))
+      return rc;
+    if ((rc = encode_u8_2d(&xa.tm_dn_q, layer.down_q, static_cast<uint64_t>(E) * H, F / 2, xa.kq_dn * 32, 128,
+                           "down codes")))
+      return rc;
+    if ((rc = encode_u8_2d(&xa.tm_sdn_q, layer.sh_down_q, H, F / 2, xa.kq_dn * 32, 128, "shared down codes")))
+      return rc;
+    xa.gu_s = layer.gate_up_s;
+    xa.sgu_s = layer.sh_gate_up_s;
+    xa.dn_s = layer.down_s;
+    xa.sdn_s = layer.sh_down_s;
+    xa.q4 = 1;
+  } else {
+    if ((rc = encode_bf16_2d(&xa.tm_gu, layer.gate_up, static_cast<uint64_t>(E) * 2 * F, H, 64, "gate_up"))) return rc;
+    if ((rc = encode_bf16_2d(&xa.tm_sgu, layer.sh_gate_up, 2ull * F, H, 64, "shared gate_up"))) return rc;
+    if ((rc = encode_bf16_2d(&xa.tm_dn, layer.down, static_cast<uint64_t>(E) * H, F, 128, "down"))) return rc;
+    if ((rc = encode_bf16_2d(&xa.tm_sdn, layer.sh_down, H, F, 128, "shared down"))) return rc;
+  }
   if (fused) {  // the gate/up B operand is the dense block of normed rows
     if ((rc = encode_bf16_2d(&xa.tm_xg, xg + static_cast<size_t>(MK) * H, M, H, 16, "normed rows"))) return rc;
   } else {
@@ -336,23 +385,33 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.E = E;
   xa.K = K;
   const int nb = (M + 15) & ~15;
-  const size_t fixed = expert_smem_bytes(0, 0, nb) + static_cast<size_t>(4 * 16) * 8 +
+  const size_t fixed = expert_smem_bytes(0, 0, 0, nb, 0) + static_cast<size_t>(4 * 16) * 8 +
                        (fused ? layer_rt_bytes(M, K, E) : 0);
   const size_t budget = static_cast<size_t>(kSmemBudget) - fixed;
-  int sa, sb;
-  if (nb <= 64) {
+  int sa, sb, sq = 0;
+  if (q4) {
+    // The staging ring carries the HBM stream (4 KiB of codes per K group,
+    // 4x the weights per byte); four bf16 stages feed the MMA.
+    sa = 4;
+    sb = nb <= 64 ? 6 : 3;
+    const size_t rest = budget - static_cast<size_t>(sa) * kATileBytes - static_cast<size_t>(sb) * nb * 128;
+    sq = static_cast<int>(std::min<size_t>(24, rest / (kQSlotBytes + 16)));
+  } else if (nb <= 64) {
     sa = sb = static_cast<int>(std::min<size_t>(16, budget / (kATileBytes + static_cast<size_t>(nb) * 128)));
   } else {
     sb = 3;
     sa = static_cast<int>(std::min<size_t>(16, (budget - static_cast<size_t>(sb) * nb * 128) / kATileBytes));
   }
+  const int smem_a = sa;
+  xa.smem_a = smem_a;
   xa.stages_a = sa;
   xa.stages_b = sb;
+  xa.stages_q = sq;
   xa.nb_max = nb;
   // Up to 32 tokens the slice that finishes last combines (a few µs); with
   // more tokens that serial walk would dominate, so a parallel kernel does it.
   xa.combine = fused ? 1 : 0;
-  size_t smem = expert_smem_bytes(sa, sb, nb);
+  size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq);
   if (fused) {
     xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
     xa.bias = layer.router_bias;
@@ -617,6 +676,24 @@ int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const 
                     reinterpret_cast<cudaStream_t>(stream));
   if (rc) return rc;
   return check_launch_errors("lmhead unmask");
+}
+
+int clover_quantize_q4(const uint16_t* w, int32_t n_mats, int32_t rows, int32_t cols, uint8_t* q, uint16_t* s,
+                       clover_stream_t stream) {
+  if (!w || !q || !s) return fail(CLOVER_ERR_INVALID_ARG, "NULL w/q/s");
+  if (!aligned16(w) || !aligned16(q) || !aligned16(s)) return fail(CLOVER_ERR_INVALID_ARG, "w/q/s not 16-byte aligned");
+  if (n_mats < 1 || rows < 1 || cols < 64 || cols % 64 != 0)
+    return fail(CLOVER_ERR_INVALID_ARG, "n_mats=%d rows=%d cols=%d: need >= 1 and cols %% 64 == 0", n_mats, rows, cols);
+  QuantArgs a;
+  a.w = reinterpret_cast<const bf16*>(w);
+  a.q = q;
+  a.s = s;
+  a.n_mats = n_mats;
+  a.rows = rows;
+  a.cols = cols;
+  cudaError_t e = launch_quantize_q4(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launch quantize");
+  return check_launch_errors("quantize q4");
 }
 
 size_t clover_accept_workspace_bytes(const clover_dims* dims, int32_t max_rows) {

@@ -103,6 +103,20 @@ __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArg
 }
 
 // B rows (the MMA N) of a unit: dense gate/up units take all M token rows.
+// Start of a unit's K walk (in K steps), fixed by (expert, slice) so that
+// concurrent units request different offsets within the weight rows and
+// independent of scheduling, so results stay reproducible. A multiple of kq
+// (the K groups of one low-bit staging slot; 1 for bf16 weights).
+__device__ __forceinline__ int unit_rot(const Unit& w, int nk, int kq) {
+  const int ns = nk / kq;
+  return kq * static_cast<int>((static_cast<unsigned>(w.e) * 5u + static_cast<unsigned>(w.slice) * 3u) %
+                               static_cast<unsigned>(ns));
+}
+
+__device__ __forceinline__ int unit_kq(const Unit& w, const ExpertArgs& p) {
+  return p.q4 ? (w.kind == 0 ? p.kq_gu : p.kq_dn) : 1;
+}
+
 __device__ __forceinline__ int unit_rows(const Unit& w, const Rt& rt, const ExpertArgs& p) {
   return ((w.kind == 0 && rt.dense) ? p.M + 15 : w.cnt + 15) & ~15;
 }
@@ -110,8 +124,9 @@ __device__ __forceinline__ int unit_rows(const Unit& w, const Rt& rt, const Expe
 struct Smem {
   uint8_t* a_ring;
   uint8_t* b_ring;
+  uint8_t* q_ring;  // low-bit staging slots (stages_q x kQSlotBytes)
   float* xch;  // [2][64][20] gate/up half exchange for SwiGLU
-  uint64_t *full_a, *empty_a, *full_b, *empty_b, *tfull, *tempty, *ufull, *uempty, *drain;
+  uint64_t *full_a, *empty_a, *full_b, *empty_b, *tfull, *tempty, *ufull, *uempty, *drain, *full_q, *empty_q;
   int* unit_ids;  // [4]
   uint32_t* tmem_slot;
   volatile uint32_t* abort;
@@ -128,8 +143,9 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   uint8_t* base = raw + ((1024u - (r & 1023u)) & 1023u);
   s.b_stage_bytes = static_cast<uint32_t>(p.nb_max) * 128u;
   s.a_ring = base;
-  s.b_ring = s.a_ring + static_cast<size_t>(p.stages_a) * kATileBytes;
-  s.xch = reinterpret_cast<float*>(s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes);
+  s.b_ring = s.a_ring + static_cast<size_t>(p.smem_a) * kATileBytes;
+  s.q_ring = s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes;  // 1 KiB aligned
+  s.xch = reinterpret_cast<float*>(s.q_ring + static_cast<size_t>(p.stages_q) * kQSlotBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 2 * 64 * 20);
   s.full_a = bars;
   s.empty_a = s.full_a + p.stages_a;
@@ -140,7 +156,9 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   s.ufull = s.tempty + 2;
   s.uempty = s.ufull + kExpertUnitRing;
   s.drain = s.uempty + kExpertUnitRing;
-  s.unit_ids = reinterpret_cast<int*>(s.drain + 1);
+  s.full_q = s.drain + 1;
+  s.empty_q = s.full_q + p.stages_q;
+  s.unit_ids = reinterpret_cast<int*>(s.empty_q + p.stages_q);
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.unit_ids + kExpertUnitRing);
   s.abort = s.tmem_slot + 1;
   s.s_last = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
@@ -162,9 +180,15 @@ __device__ void drain_ring(uint64_t* full, int stages, uint32_t issued_mask, uin
     if (issued_mask & (1u << i)) mbar_wait_for(&full[i], (parity_bits >> i) & 1u, 200000000ull);
 }
 
+// Weight producer. bf16 weights go straight into the A ring by TMA; low-bit
+// weights (kQ4) go into the staging ring, codes by TMA and scales by bulk
+// copy, for the converter warps to expand.
+template <bool kQ4>
 __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int n_total) {
   const uint64_t pol = l2_policy_evict_first();
-  const int SA = p.stages_a;
+  const int SA = kQ4 ? p.stages_q : p.stages_a;
+  uint64_t* const full = kQ4 ? s.full_q : s.full_a;
+  uint64_t* const empty = kQ4 ? s.empty_q : s.empty_a;
   int sa = 0;
   uint32_t pha = 0, issued = 0, parity_bits = 0;
   for (int it = 0;; ++it) {
@@ -191,26 +215,49 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
       row = (w.a == 0 ? 0 : w.e * p.H) + w.slice * 128;
       nk = p.F >> 6;
     }
-    // Start each unit's K walk at an offset fixed by (expert, slice), so that
-    // concurrent units request different offsets within the weight rows; the
-    // offset does not depend on scheduling, so results stay reproducible.
-    const int rot = static_cast<int>((static_cast<unsigned>(w.e) * 5u + static_cast<unsigned>(w.slice) * 3u) %
-                                     static_cast<unsigned>(nk));
+    const int kq = kQ4 ? unit_kq(w, p) : 1;
+    const int rot = unit_rot(w, nk, kq);
     bool ok = true;
-    for (int kc0 = 0; kc0 < nk; ++kc0) {
+    // one stage per K step (bf16) or per kq K steps (low-bit slot)
+    for (int kc0 = 0; kc0 < nk; kc0 += kq) {
       const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
-      if (!mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
+      if (!mbar_wait(&empty[sa], pha ^ 1u, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
         ok = false;
         break;
       }
-      const uint32_t dst = smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes);
-      mbar_arrive_expect_tx(&s.full_a[sa], kATileBytes);
-      if (w.kind == 0) {
-        tma_load_2d(dst, m, &s.full_a[sa], kc * 64, row, pol);           // 64 gate rows
-        tma_load_2d(dst + 8192, m, &s.full_a[sa], kc * 64, row + p.F, pol);  // 64 up rows
+      if (kQ4) {
+        // codes: rows of kq x 32 bytes (gate/up: 64 gate rows then 64 up
+        // rows; down: 128 rows), then the kq groups' 128 row scales each
+        const uint32_t dst = smem_u32(s.q_ring + static_cast<size_t>(sa) * kQSlotBytes);
+        mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(kq * kQGroupBytes));
+        const uint32_t sdst = dst + kq * 4096;
+        if (w.kind == 0) {
+          const CUtensorMap* mq = (w.a == 0) ? &p.tm_sgu_q : &p.tm_gu_q;
+          tma_load_2d(dst, mq, &full[sa], kc * 32, row, pol);
+          tma_load_2d(dst + kq * 2048, mq, &full[sa], kc * 32, row + p.F, pol);
+          const uint16_t* sc = (w.a == 0 ? p.sgu_s : p.gu_s + static_cast<size_t>(w.e) * (p.H >> 6) * 2 * p.F) +
+                               static_cast<size_t>(kc) * 2 * p.F + w.slice * 64;
+          for (int g = 0; g < kq; ++g) {
+            bulk_load(sdst + g * 256, sc + static_cast<size_t>(g) * 2 * p.F, 128, &full[sa]);
+            bulk_load(sdst + g * 256 + 128, sc + static_cast<size_t>(g) * 2 * p.F + p.F, 128, &full[sa]);
+          }
+        } else {
+          const CUtensorMap* mq = (w.a == 0) ? &p.tm_sdn_q : &p.tm_dn_q;
+          tma_load_2d(dst, mq, &full[sa], kc * 32, row, pol);
+          const uint16_t* sc = (w.a == 0 ? p.sdn_s : p.dn_s + static_cast<size_t>(w.e) * (p.F >> 6) * p.H) +
+                               static_cast<size_t>(kc) * p.H + w.slice * 128;
+          for (int g = 0; g < kq; ++g) bulk_load(sdst + g * 256, sc + static_cast<size_t>(g) * p.H, 256, &full[sa]);
+        }
       } else {
-        tma_load_2d(dst, m, &s.full_a[sa], kc * 64, row, pol);  // 128 down rows
+        const uint32_t dst = smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes);
+        mbar_arrive_expect_tx(&full[sa], kATileBytes);
+        if (w.kind == 0) {
+          tma_load_2d(dst, m, &full[sa], kc * 64, row, pol);            // 64 gate rows
+          tma_load_2d(dst + 8192, m, &full[sa], kc * 64, row + p.F, pol);  // 64 up rows
+        } else {
+          tma_load_2d(dst, m, &full[sa], kc * 64, row, pol);  // 128 down rows
+        }
       }
       issued |= 1u << sa;
       parity_bits = (parity_bits & ~(1u << sa)) | (pha << sa);
@@ -221,7 +268,95 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
     }
     if (!ok) break;
   }
-  if (*s.abort) drain_ring(s.full_a, SA, issued, parity_bits);
+  if (*s.abort) drain_ring(full, SA, issued, parity_bits);
+}
+
+// Low-bit tiles -> bf16 A tiles (warps 8-11, one tile row per thread). In a
+// slot of kq K groups, row r's codes of group g and its scale sit at
+// slot + r kq 32 + 32 g (16-byte chunks swizzled when the row is 128 bytes)
+// and slot + kq 4096 + 256 g + 2 r, for both unit kinds.
+// Each pair of codes becomes a bf16x2 by the exponent trick
+// (0x4300 | u = 128 + u), then (128 + u) - 136 = u - 8 exactly and one bf16
+// multiply by the scale gives bf16((u - 8) s). The row is written in the
+// 128-byte swizzle the TMA would have used, so the MMA is unchanged.
+__device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
+  const int r = threadIdx.x - 8 * 32;  // 0..127
+  const int lane = threadIdx.x & 31;
+  const int SA = p.stages_a, SQ = p.stages_q;
+  int sa = 0, sq = 0;
+  uint32_t pha = 0, phq = 0;
+  const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
+  for (int it = 0;; ++it) {
+    const int us = it & (kExpertUnitRing - 1);
+    const uint32_t upar = (it / kExpertUnitRing) & 1;
+    const bool got = mbar_wait(&s.ufull[us], upar, s.abort);
+    const int u = got ? s.unit_ids[us] : kUnitAbort;
+    named_bar_sync(2, 128);  // every converter thread has read the slot
+    if (r == 0) {
+      if (got) mbar_arrive(&s.uempty[us]);
+      else raise_abort(s, p.err, kErrMbarTimeout);
+    }
+    if (u < 0) break;
+    const Unit w = decode_unit(u, rt, p);
+    const int nk = (w.kind == 0) ? (p.H >> 6) : (p.F >> 6);
+    const int kq = unit_kq(w, p);
+    bool ok = true;
+    for (int kc0 = 0; kc0 < nk && ok; kc0 += kq) {
+      if (!mbar_wait(&s.full_q[sq], phq, s.abort)) {
+        raise_abort(s, p.err, kErrMbarTimeout);
+        ok = false;
+        break;
+      }
+      const uint8_t* slot = s.q_ring + static_cast<size_t>(sq) * kQSlotBytes;
+      for (int g = 0; g < kq; ++g) {
+        if (!mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
+          raise_abort(s, p.err, kErrMbarTimeout);
+          ok = false;
+          break;
+        }
+        // 128-byte code rows (kq = 4) arrive in the 128-byte swizzle
+        const uint8_t* src = slot + r * kq * 32;
+        const int ch0 = (kq == 4) ? ((2 * g) ^ (r & 7)) : 2 * g;
+        const int ch1 = (kq == 4) ? ((2 * g + 1) ^ (r & 7)) : 2 * g + 1;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(src + ch0 * 16);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(src + ch1 * 16);
+        const unsigned short sb = *reinterpret_cast<const unsigned short*>(slot + kq * 4096 + g * 256 + 2 * r);
+        const __nv_bfloat162 sc = __halves2bfloat162(__ushort_as_bfloat16(sb), __ushort_as_bfloat16(sb));
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t o[32];  // word 4j + i holds elements 8j + 2i (low half) and 8j + 2i + 1
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t x = ((words[j] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+            const __nv_bfloat162 v = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&x), k136), sc);
+            o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
+          }
+        }
+        uint8_t* row = s.a_ring + static_cast<size_t>(sa) * kATileBytes + r * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) =
+              make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s.full_a[sa]);
+        if (++sa == SA) {
+          sa = 0;
+          pha ^= 1u;
+        }
+      }
+      // this thread's reads of the slot are done (the fence above ordered
+      // them before any later copy into it)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty_q[sq]);
+      if (++sq == SQ) {
+        sq = 0;
+        phq ^= 1u;
+      }
+    }
+    if (!ok) break;
+  }
 }
 
 __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
@@ -269,8 +404,7 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       if (!ok) break;
       fence_proxy_async_global();
     }
-    const int rot = static_cast<int>((static_cast<unsigned>(w.e) * 5u + static_cast<unsigned>(w.slice) * 3u) %
-                                     static_cast<unsigned>(nk));
+    const int rot = unit_rot(w, nk, unit_kq(w, p));
     bool ok = true;
     for (int kc0 = 0; kc0 < nk; ++kc0) {
       const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
@@ -328,8 +462,8 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uin
         break;
       }
       tc_fence_after();
-      const uint64_t ad = umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes));
       const uint64_t bd = umma_desc_sw128(smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes));
+      const uint64_t ad = umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes));
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
@@ -573,12 +707,17 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
 
 // Barrier setup, TMEM allocation and descriptor prefetch (before the
 // dependency wait, so they overlap the previous kernel).
+template <bool kQ4>
 __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const Smem& s) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages_a; ++i) {
-      mbar_init(&s.full_a[i], 1);
+      mbar_init(&s.full_a[i], kQ4 ? 4 : 1);  // low-bit: one arrival per converter warp
       mbar_init(&s.empty_a[i], 1);
+    }
+    for (int i = 0; kQ4 && i < p.stages_q; ++i) {
+      mbar_init(&s.full_q[i], 1);
+      mbar_init(&s.empty_q[i], 4);
     }
     for (int i = 0; i < p.stages_b; ++i) {
       mbar_init(&s.full_b[i], 1);
@@ -590,17 +729,17 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
     }
     for (int i = 0; i < kExpertUnitRing; ++i) {
       mbar_init(&s.ufull[i], 1);
-      mbar_init(&s.uempty[i], 3);  // B loader, MMA issuer, epilogue leader
+      mbar_init(&s.uempty[i], kQ4 ? 4 : 3);  // B loader, MMA issuer, epilogue leader (+ converter leader)
     }
     mbar_init(s.drain, 1);
     *s.abort = 0u;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tm_gu);
-    tma_prefetch_desc(&p.tm_sgu);
-    tma_prefetch_desc(&p.tm_dn);
-    tma_prefetch_desc(&p.tm_sdn);
+    tma_prefetch_desc(kQ4 ? &p.tm_gu_q : &p.tm_gu);
+    tma_prefetch_desc(kQ4 ? &p.tm_sgu_q : &p.tm_sgu);
+    tma_prefetch_desc(kQ4 ? &p.tm_dn_q : &p.tm_dn);
+    tma_prefetch_desc(kQ4 ? &p.tm_sdn_q : &p.tm_sdn);
   }
   if (warp == 1) {
     tmem_alloc(s.tmem_slot, 512);
@@ -612,17 +751,20 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
   return *s.tmem_slot;
 }
 
+template <bool kQ4>
 __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_total = rt.n_exp * ((p.F >> 6) + (p.H >> 7));
   if (warp == 0) {
-    if (lane == 0) producer_a(p, s, rt, n_total);
+    if (lane == 0) producer_a<kQ4>(p, s, rt, n_total);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(p, s, rt, tmem_base);
   } else if (warp == 2) {
     if (lane == 0) producer_b(p, s, rt);
   } else if (warp < 7) {
     epilogue(p, s, rt, tmem_base);
+  } else if (kQ4 && warp >= 8) {
+    converter(p, s, rt);
   }  // warp 7 has no role here
   tc_fence_before();
   __syncthreads();
@@ -635,10 +777,12 @@ __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s,
 
 }  // namespace
 
-__global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_constant__ ExpertArgs p) {
+template <bool kQ4>
+__global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
+    k_expert(const __grid_constant__ ExpertArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
-  const uint32_t tmem_base = expert_prologue(p, s);
+  const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
   pdl_wait();
   pdl_trigger();
   Rt rt;
@@ -650,7 +794,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_expert(const __grid_const
   rt.topk_w = p.topk_w;
   rt.n_exp = *p.n_active + 1;
   rt.dense = 0;
-  expert_roles(p, s, rt, tmem_base);
+  expert_roles<kQ4>(p, s, rt, tmem_base);
 }
 
 namespace {
@@ -693,12 +837,14 @@ __device__ bool grid_barrier(int* ctr, int* gen, int* err) {
 
 // One MoE sublayer for M <= 32 tokens in one launch: routing, experts and
 // combine (see the file comment).
-__global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_constant__ ExpertArgs p) {
+template <bool kQ4>
+__global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
+    k_layer(const __grid_constant__ ExpertArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
   uint64_t* wbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.tmem_slot) + 96);
   if (threadIdx.x == 0) mbar_init(wbar, 1);  // made visible by the prologue's fence
-  const uint32_t tmem_base = expert_prologue(p, s);
+  const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int M = p.M, K = p.K, E = p.E, H = p.H;
@@ -722,7 +868,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
   // into the (still idle) weight ring before waiting.
   const int my_items = (n_items > static_cast<int>(blockIdx.x)) ? (n_items - 1 - blockIdx.x) / G + 1 : 0;
   const uint32_t wslice = kRouteExperts * H * 2;
-  const bool wr_staged = my_items * wslice <= static_cast<uint32_t>(p.stages_a) * kATileBytes;
+  const bool wr_staged = my_items * wslice <= static_cast<uint32_t>(p.smem_a) * kATileBytes;
   if (threadIdx.x == 0 && wr_staged && my_items > 0) {
     uint32_t bytes = 0;
     for (int j = 0; j < my_items; ++j) {
@@ -937,28 +1083,32 @@ __global__ void __launch_bounds__(kExpertThreads, 1) k_layer(const __grid_consta
   rt.n_exp = (*s.abort) ? 0 : *s_nact + 1;  // after a failed barrier no unit runs
   rt.dense = 1;
   if (st) st[4] = global_ns();
-  expert_roles(p, s, rt, tmem_base);
+  expert_roles<kQ4>(p, s, rt, tmem_base);
   if (p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
 }
 
-size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max) {
-  return 1024 + static_cast<size_t>(stages_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
-         2 * 64 * 20 * sizeof(float) + static_cast<size_t>(2 * stages_a + 2 * stages_b + 5 + 2 * kExpertUnitRing) * 8 +
-         256;
+// smem_a: A stages in shared memory; stages_a: A barriers (the A stages of the
+// pipeline, in shared or tensor memory).
+size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q) {
+  return 1024 + static_cast<size_t>(smem_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
+         static_cast<size_t>(stages_q) * kQSlotBytes + 2 * 64 * 20 * sizeof(float) +
+         static_cast<size_t>(2 * stages_a + 2 * stages_b + 2 * stages_q + 5 + 2 * kExpertUnitRing) * 8 + 256;
 }
 
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(3 * M * K + 7 * E + 16) * 4; }
 
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(k_layer, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto* k = a.q4 ? k_layer<true> : k_layer<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_kernel(k_layer, dim3(grid), dim3(kExpertThreads), smem, s, pdl, a);
+  return launch_kernel(k, dim3(grid), dim3(a.q4 ? kExpertThreadsQ4 : kExpertThreads), smem, s, pdl, a);
 }
 
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
-  cudaError_t e = cudaFuncSetAttribute(k_expert, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto* k = a.q4 ? k_expert<true> : k_expert<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_kernel(k_expert, dim3(grid), dim3(kExpertThreads), smem, s, pdl, a);
+  return launch_kernel(k, dim3(grid), dim3(a.q4 ? kExpertThreadsQ4 : kExpertThreads), smem, s, pdl, a);
 }
 
 }  // namespace clover

@@ -26,12 +26,20 @@ constexpr int kMaxTopK = 32;
 // Expert kernel: 8 warps (A loads, MMA, B loads, 4 epilogue warps, and one
 // more that only takes part in the fused kernel's routing phase).
 constexpr int kExpertThreads = 256;
+// With low-bit expert weights four more warps expand the 4-bit codes.
+constexpr int kExpertThreadsQ4 = 384;
 constexpr int kExpertUnitRing = 4;
 // Head kernel: 6 warps (loads, MMA, 4 epilogue warps).
 constexpr int kHeadThreads = 192;
 constexpr int kHeadMaxCtas = 512;
 
 constexpr int kATileBytes = 128 * 64 * 2;  // 128 rows x 64 bf16
+// Low-bit staging: per K group of 64, a tile is 128 rows x 32 bytes of codes
+// (4 KiB) + 128 bf16 scales; a slot holds up to 4 consecutive groups, so each
+// row arrives as one contiguous piece of up to 128 bytes.
+constexpr int kQGroupBytes = 128 * 32 + 128 * 2;
+constexpr int kQSlotGroups = 4;
+constexpr int kQSlotBytes = kQSlotGroups * kQGroupBytes;
 constexpr int kSmemBudget = 227 * 1024;
 
 struct EmbedArgs {
@@ -97,6 +105,19 @@ struct ExpertArgs {
   CUtensorMap tm_sdn;  // shared down     [H][F]
   CUtensorMap tm_xg;   // gathered inputs [M*K+M][H]
   CUtensorMap tm_h;    // SwiGLU outputs  [M*K+M][F]
+  // Low-bit expert weights (q4 != 0): codes by TMA (uint8, box 32 B x rows),
+  // scales by bulk copy; stages_q staging slots of kQSlotBytes.
+  CUtensorMap tm_gu_q;   // [E*2F][H/2]
+  CUtensorMap tm_sgu_q;  // [2F][H/2]
+  CUtensorMap tm_dn_q;   // [E*H][F/2]
+  CUtensorMap tm_sdn_q;  // [H][F/2]
+  const uint16_t* gu_s;   // [E][H/64][2F]
+  const uint16_t* sgu_s;  // [H/64][2F]
+  const uint16_t* dn_s;   // [E][F/64][H]
+  const uint16_t* sdn_s;  // [F/64][H]
+  int q4, stages_q;
+  int kq_gu, kq_dn;  // K groups per staging slot for gate/up and down units (1, 2 or 4)
+  int smem_a;  // A stages in shared memory (= stages_a)
   const float* x_in;
   float* x_out;
   bf16* hbuf;          // [M*K+M][F]
@@ -169,7 +190,15 @@ struct HeadArgs {
   float ratio, delta;
 };
 
+struct QuantArgs {
+  const bf16* w;  // [n_mats][rows][cols]
+  uint8_t* q;     // [n_mats][rows][cols / 2] codes
+  uint16_t* s;    // [n_mats][cols / 64][rows] bf16 scales
+  int n_mats, rows, cols;
+};
+
 // Launch wrappers (return the cudaError_t of the launch).
+cudaError_t launch_quantize_q4(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
@@ -177,13 +206,14 @@ cudaError_t launch_perm(const PermArgs& a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
+// (both launch the low-bit form when a.q4 != 0)
 size_t layer_rt_bytes(int M, int K, int E);
 // Largest token count the fused layer kernel takes (one 32-bit mask per expert).
 constexpr int kLayerMaxTokens = 32;
 // Launches the unmask or the accept form of the head kernel.
 cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl);
 
-size_t expert_smem_bytes(int stages_a, int stages_b, int nb_max);
+size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q);
 size_t head_smem_bytes(int stages, int nb, bool accept);
 
 }  // namespace clover

@@ -85,6 +85,17 @@ typedef struct {
     const uint16_t* down;       /* bf16 [E][H][F]                                */
     const uint16_t* sh_gate_up; /* bf16 [2F][H], shared expert                   */
     const uint16_t* sh_down;    /* bf16 [H][F],  shared expert                   */
+    /* Low-bit expert weights (format of clover_quantize_q4). When gate_up_q is
+     * non-NULL all eight fields below must be set and the four bf16 expert
+     * pointers above are ignored (may be NULL); the router stays bf16. */
+    const uint8_t* gate_up_q;    /* codes [E][2F][H/2]   */
+    const uint16_t* gate_up_s;   /* scales [E][H/64][2F] */
+    const uint8_t* down_q;       /* codes [E][H][F/2]    */
+    const uint16_t* down_s;      /* scales [E][F/64][H]  */
+    const uint8_t* sh_gate_up_q; /* codes [2F][H/2]      */
+    const uint16_t* sh_gate_up_s;/* scales [H/64][2F]    */
+    const uint8_t* sh_down_q;    /* codes [H][F/2]       */
+    const uint16_t* sh_down_s;   /* scales [F/64][H]     */
 } clover_moe_layer;
 
 /* Bytes of workspace clover_moe_block_step needs for up to max_tokens tokens.
@@ -107,6 +118,20 @@ int clover_moe_block_step(const clover_dims* dims, const clover_moe_layer* layer
                           const float* x_in, float* x_out,
                           int32_t* topk_idx, float* topk_w, int32_t M,
                           void* workspace, size_t workspace_bytes, clover_stream_t stream);
+
+/* Low-bit expert weights. The pages name INT4 for one deployment (Files,
+ * "What 680 tokens a second has to be") but give no format; this format is
+ * the library's own. Quantizes n_mats bf16 matrices w [n_mats][rows][cols]
+ * (cols % 64 == 0) into 4-bit codes q [n_mats][rows][cols/2] and bf16 scales
+ * s [n_mats][cols/64][rows]: per row and group of 64 columns,
+ *   s = bf16(float32(max |w|) / 7)          (IEEE fp32 division, nearest even)
+ *   u = clamp(rint(float32(w) / s), -8, 7) + 8   (u = 8 where s = 0)
+ * and the weight a product then uses is bf16((u - 8) s). Codes are packed
+ * eight to a little-endian 32-bit word, nibble i (bits 4i..4i+3) holding
+ * element (0, 2, 4, 6, 1, 3, 5, 7)[i] of the eight. All pointers are device
+ * pointers, 16-byte aligned; asynchronous on `stream`. */
+int clover_quantize_q4(const uint16_t* w, int32_t n_mats, int32_t rows, int32_t cols, uint8_t* q,
+                       uint16_t* s, clover_stream_t stream);
 
 /* Bytes of workspace clover_lmhead_unmask needs. Host-only. */
 size_t clover_head_workspace_bytes(const clover_dims* dims, int32_t max_tokens);

@@ -159,3 +159,33 @@ def decisions_clear(max_prob, masked, tau, block):
             if s[0] - s[1] < REL_BAND * s[0]:
                 return False
     return True
+
+
+def q4_bits(b: np.ndarray) -> np.ndarray:
+    """The oracle's own low-bit round trip of a bf16 matrix: the bf16 bits of
+    the weights a product uses after quantization."""
+    import oracle as O
+    return O.dequantize_q4(*O.quantize_q4(b))
+
+
+class LazyQ4Experts(LazyExperts):
+    def __getitem__(self, e):
+        e = int(e)
+        if e not in self.cache:
+            self.cache[e] = q4_bits(bits(self.t[e]))
+        return self.cache[e]
+
+
+def layer_to_oracle_q4(layer: synth.Layer, lazy: bool = False) -> dict:
+    """layer_to_oracle with every expert matrix replaced by the oracle's own
+    low-bit round trip of it (the router stays bf16)."""
+    d = layer_to_oracle(layer, lazy=True)
+    d["sh_gate_up"] = q4_bits(d["sh_gate_up"])
+    d["sh_down"] = q4_bits(d["sh_down"])
+    if lazy:
+        d["gate_up"] = LazyQ4Experts(layer.gate_up)
+        d["down"] = LazyQ4Experts(layer.down)
+    else:
+        d["gate_up"] = np.stack([q4_bits(bits(layer.gate_up[e])) for e in range(layer.gate_up.shape[0])])
+        d["down"] = np.stack([q4_bits(bits(layer.down[e])) for e in range(layer.down.shape[0])])
+    return d
