@@ -385,22 +385,32 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.E = E;
   xa.K = K;
   const int nb = (M + 15) & ~15;
-  const size_t fixed = expert_smem_bytes(0, 0, 0, nb, 0) + static_cast<size_t>(4 * 16) * 8 +
+  // Two K groups per A/B stage (8 MMAs per pipeline step instead of 4) when
+  // the token tile is small; 256-token tiles keep one group per stage.
+  const int kg_gu = (nb <= 64 && (H / 64) % 2 == 0) ? 2 : 1;
+  const int kg_dn = (nb <= 64 && (F / 64) % 2 == 0) ? 2 : 1;
+  const int kg = std::max(kg_gu, kg_dn);
+  xa.kg_gu = kg_gu;
+  xa.kg_dn = kg_dn;
+  xa.kg_stage = kg;
+  const size_t a_stage = static_cast<size_t>(kg) * kATileBytes;
+  const size_t b_stage = static_cast<size_t>(kg) * nb * 128;
+  const size_t fixed = expert_smem_bytes(0, 0, 0, nb, 0, kg) + static_cast<size_t>(4 * 16) * 8 +
                        (fused ? layer_rt_bytes(M, K, E) : 0);
   const size_t budget = static_cast<size_t>(kSmemBudget) - fixed;
   int sa, sb, sq = 0;
   if (q4) {
     // The staging ring carries the HBM stream (4 KiB of codes per K group,
-    // 4x the weights per byte); four bf16 stages feed the MMA.
-    sa = 4;
-    sb = nb <= 64 ? 6 : 3;
-    const size_t rest = budget - static_cast<size_t>(sa) * kATileBytes - static_cast<size_t>(sb) * nb * 128;
+    // 4x the weights per byte); a few bf16 stages feed the MMA.
+    sa = kg == 2 ? 2 : 4;
+    sb = nb <= 64 ? 3 : 3;
+    const size_t rest = budget - static_cast<size_t>(sa) * a_stage - static_cast<size_t>(sb) * b_stage;
     sq = static_cast<int>(std::min<size_t>(24, rest / (kQSlotBytes + 16)));
   } else if (nb <= 64) {
-    sa = sb = static_cast<int>(std::min<size_t>(16, budget / (kATileBytes + static_cast<size_t>(nb) * 128)));
+    sa = sb = static_cast<int>(std::min<size_t>(16, budget / (a_stage + b_stage)));
   } else {
     sb = 3;
-    sa = static_cast<int>(std::min<size_t>(16, (budget - static_cast<size_t>(sb) * nb * 128) / kATileBytes));
+    sa = static_cast<int>(std::min<size_t>(16, (budget - static_cast<size_t>(sb) * b_stage) / a_stage));
   }
   const int smem_a = sa;
   xa.smem_a = smem_a;
@@ -411,7 +421,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   // Up to 32 tokens the slice that finishes last combines (a few µs); with
   // more tokens that serial walk would dominate, so a parallel kernel does it.
   xa.combine = fused ? 1 : 0;
-  size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq);
+  size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq, kg);
   if (fused) {
     xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
     xa.bias = layer.router_bias;

@@ -117,6 +117,15 @@ __device__ __forceinline__ int unit_kq(const Unit& w, const ExpertArgs& p) {
   return p.q4 ? (w.kind == 0 ? p.kq_gu : p.kq_dn) : 1;
 }
 
+// K groups per A/B stage of a unit (1 or 2).
+__device__ __forceinline__ int unit_kg(const Unit& w, const ExpertArgs& p) { return w.kind == 0 ? p.kg_gu : p.kg_dn; }
+
+// Granularity of a unit's K walk: a low-bit slot (kq groups, a multiple of
+// kg) or one A/B stage (kg groups).
+__device__ __forceinline__ int unit_kstep(const Unit& w, const ExpertArgs& p) {
+  return p.q4 ? unit_kq(w, p) : unit_kg(w, p);
+}
+
 __device__ __forceinline__ int unit_rows(const Unit& w, const Rt& rt, const ExpertArgs& p) {
   return ((w.kind == 0 && rt.dense) ? p.M + 15 : w.cnt + 15) & ~15;
 }
@@ -134,16 +143,20 @@ struct Smem {
   volatile int* s_unit;
   volatile int* s_ok;
   uint8_t* rt_region;  // k_layer's routing tables
-  uint32_t b_stage_bytes;
+  uint32_t a_stage_bytes;  // kg_stage A tiles of 16 KiB
+  uint32_t b_stage_bytes;  // kg_stage B tiles of nb_max x 128 bytes
+  uint32_t b_half_bytes;   // one B tile
 };
 
 __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   Smem s;
   const uint32_t r = smem_u32(raw);
   uint8_t* base = raw + ((1024u - (r & 1023u)) & 1023u);
-  s.b_stage_bytes = static_cast<uint32_t>(p.nb_max) * 128u;
+  s.b_half_bytes = static_cast<uint32_t>(p.nb_max) * 128u;
+  s.b_stage_bytes = s.b_half_bytes * static_cast<uint32_t>(p.kg_stage);
+  s.a_stage_bytes = static_cast<uint32_t>(kATileBytes) * static_cast<uint32_t>(p.kg_stage);
   s.a_ring = base;
-  s.b_ring = s.a_ring + static_cast<size_t>(p.smem_a) * kATileBytes;
+  s.b_ring = s.a_ring + static_cast<size_t>(p.smem_a) * s.a_stage_bytes;
   s.q_ring = s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes;  // 1 KiB aligned
   s.xch = reinterpret_cast<float*>(s.q_ring + static_cast<size_t>(p.stages_q) * kQSlotBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 2 * 64 * 20);
@@ -216,10 +229,12 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
       nk = p.F >> 6;
     }
     const int kq = kQ4 ? unit_kq(w, p) : 1;
-    const int rot = unit_rot(w, nk, kq);
+    const int kg = unit_kg(w, p);
+    const int kstep = unit_kstep(w, p);
+    const int rot = unit_rot(w, nk, kstep);
     bool ok = true;
-    // one stage per K step (bf16) or per kq K steps (low-bit slot)
-    for (int kc0 = 0; kc0 < nk; kc0 += kq) {
+    // one stage per kg K groups (bf16) or one slot per kq K groups (low-bit)
+    for (int kc0 = 0; kc0 < nk; kc0 += kstep) {
       const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
       if (!mbar_wait(&empty[sa], pha ^ 1u, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
@@ -250,13 +265,16 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
           for (int g = 0; g < kq; ++g) bulk_load(sdst + g * 256, sc + static_cast<size_t>(g) * p.H, 256, &full[sa]);
         }
       } else {
-        const uint32_t dst = smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes);
-        mbar_arrive_expect_tx(&full[sa], kATileBytes);
-        if (w.kind == 0) {
-          tma_load_2d(dst, m, &full[sa], kc * 64, row, pol);            // 64 gate rows
-          tma_load_2d(dst + 8192, m, &full[sa], kc * 64, row + p.F, pol);  // 64 up rows
-        } else {
-          tma_load_2d(dst, m, &full[sa], kc * 64, row, pol);  // 128 down rows
+        const uint32_t dst0 = smem_u32(s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes);
+        mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(kg * kATileBytes));
+        for (int h = 0; h < kg; ++h) {
+          const uint32_t dst = dst0 + h * kATileBytes;
+          if (w.kind == 0) {
+            tma_load_2d(dst, m, &full[sa], (kc + h) * 64, row, pol);            // 64 gate rows
+            tma_load_2d(dst + 8192, m, &full[sa], (kc + h) * 64, row + p.F, pol);  // 64 up rows
+          } else {
+            tma_load_2d(dst, m, &full[sa], (kc + h) * 64, row, pol);  // 128 down rows
+          }
         }
       }
       issued |= 1u << sa;
@@ -300,6 +318,7 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
     const Unit w = decode_unit(u, rt, p);
     const int nk = (w.kind == 0) ? (p.H >> 6) : (p.F >> 6);
     const int kq = unit_kq(w, p);
+    const int kg = unit_kg(w, p);  // kq is a multiple of kg
     bool ok = true;
     for (int kc0 = 0; kc0 < nk && ok; kc0 += kq) {
       if (!mbar_wait(&s.full_q[sq], phq, s.abort)) {
@@ -309,7 +328,8 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       }
       const uint8_t* slot = s.q_ring + static_cast<size_t>(sq) * kQSlotBytes;
       for (int g = 0; g < kq; ++g) {
-        if (!mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
+        const int h = g % kg;  // half of the A stage this group fills
+        if (h == 0 && !mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
           raise_abort(s, p.err, kErrMbarTimeout);
           ok = false;
           break;
@@ -333,17 +353,19 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
             o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
           }
         }
-        uint8_t* row = s.a_ring + static_cast<size_t>(sa) * kATileBytes + r * 128;
+        uint8_t* row = s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes + r * 128;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) =
               make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s.full_a[sa]);
-        if (++sa == SA) {
-          sa = 0;
-          pha ^= 1u;
+        if (h == kg - 1) {
+          fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s.full_a[sa]);
+          if (++sa == SA) {
+            sa = 0;
+            pha ^= 1u;
+          }
         }
       }
       // this thread's reads of the slot are done (the fence above ordered
@@ -404,18 +426,22 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       if (!ok) break;
       fence_proxy_async_global();
     }
-    const int rot = unit_rot(w, nk, unit_kq(w, p));
+    const int kg = unit_kg(w, p);
+    const int rot = unit_rot(w, nk, unit_kstep(w, p));
     bool ok = true;
-    for (int kc0 = 0; kc0 < nk; ++kc0) {
+    for (int kc0 = 0; kc0 < nk; kc0 += kg) {
       const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
       if (!mbar_wait(&s.empty_b[sb], phb ^ 1u, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
         ok = false;
         break;
       }
-      const uint32_t dst = smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes);
-      mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(nrows) * 128u);
-      for (int i = 0; i < nrows; i += 16) tma_load_2d(dst + i * 128, m, &s.full_b[sb], kc * 64, row0 + i, pol);
+      const uint32_t dst0 = smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes);
+      mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(kg * nrows) * 128u);
+      for (int h = 0; h < kg; ++h) {
+        const uint32_t dst = dst0 + h * s.b_half_bytes;
+        for (int i = 0; i < nrows; i += 16) tma_load_2d(dst + i * 128, m, &s.full_b[sb], (kc + h) * 64, row0 + i, pol);
+      }
       issued |= 1u << sb;
       parity_bits = (parity_bits & ~(1u << sb)) | (phb << sb);
       if (++sb == SB) {
@@ -455,19 +481,23 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uin
     tc_fence_after();
     const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * 256u;
     bool ok = true;
-    for (int kc = 0; kc < nk; ++kc) {
+    const int kg = unit_kg(w, p);
+    for (int kc = 0; kc < nk; kc += kg) {
       if (!mbar_wait(&s.full_a[sa], pha, s.abort) || !mbar_wait(&s.full_b[sb], phb, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint64_t bd = umma_desc_sw128(smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes));
-      const uint64_t ad = umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * kATileBytes));
+      for (int h = 0; h < kg; ++h) {
+        const uint64_t bd =
+            umma_desc_sw128(smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes + h * s.b_half_bytes));
+        const uint64_t ad = umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes));
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                  (kc | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < 4; ++k)
+          umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                    (kc | h | k) != 0 ? 1u : 0u);
+      }
       umma_commit(&s.empty_a[sa]);
       umma_commit(&s.empty_b[sb]);
       if (++sa == SA) {
@@ -868,7 +898,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   // into the (still idle) weight ring before waiting.
   const int my_items = (n_items > static_cast<int>(blockIdx.x)) ? (n_items - 1 - blockIdx.x) / G + 1 : 0;
   const uint32_t wslice = kRouteExperts * H * 2;
-  const bool wr_staged = my_items * wslice <= static_cast<uint32_t>(p.smem_a) * kATileBytes;
+  const bool wr_staged = my_items * wslice <= static_cast<uint32_t>(p.smem_a) * s.a_stage_bytes;
   if (threadIdx.x == 0 && wr_staged && my_items > 0) {
     uint32_t bytes = 0;
     for (int j = 0; j < my_items; ++j) {
@@ -1087,10 +1117,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   if (p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
 }
 
-// smem_a: A stages in shared memory; stages_a: A barriers (the A stages of the
-// pipeline, in shared or tensor memory).
-size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q) {
-  return 1024 + static_cast<size_t>(smem_a) * kATileBytes + static_cast<size_t>(stages_b) * nb_max * 128 +
+// smem_a: A stages in shared memory; stages_a: A barriers; kg: K groups of
+// room per A/B stage.
+size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q, int kg) {
+  return 1024 + static_cast<size_t>(smem_a) * kg * kATileBytes + static_cast<size_t>(stages_b) * kg * nb_max * 128 +
          static_cast<size_t>(stages_q) * kQSlotBytes + 2 * 64 * 20 * sizeof(float) +
          static_cast<size_t>(2 * stages_a + 2 * stages_b + 2 * stages_q + 5 + 2 * kExpertUnitRing) * 8 + 256;
 }

@@ -118,6 +118,9 @@ struct ExpertArgs {
   int q4, stages_q;
   int kq_gu, kq_dn;  // K groups per staging slot for gate/up and down units (1, 2 or 4)
   int smem_a;  // A stages in shared memory (= stages_a)
+  // K groups of 64 per A/B stage (1 or 2) for gate/up and down units; a
+  // stage holds kg_stage groups of room (half h of a stage: group h).
+  int kg_gu, kg_dn, kg_stage;
   const float* x_in;
   float* x_out;
   bf16* hbuf;          // [M*K+M][F]
@@ -213,7 +216,7 @@ constexpr int kLayerMaxTokens = 32;
 // Launches the unmask or the accept form of the head kernel.
 cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl);
 
-size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q);
+size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q, int kg);
 size_t head_smem_bytes(int stages, int nb, bool accept);
 
 }  // namespace clover
