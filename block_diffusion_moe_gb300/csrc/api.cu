@@ -403,15 +403,18 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     // The staging ring carries the HBM stream (4 KiB of codes per K group,
     // 4x the weights per byte); a few bf16 stages feed the MMA.
     sa = kg == 2 ? 2 : 4;
-    sb = nb <= 64 ? 3 : 3;
-    const size_t rest = budget - static_cast<size_t>(sa) * a_stage - static_cast<size_t>(sb) * b_stage;
-    sq = static_cast<int>(std::min<size_t>(24, rest / (kQSlotBytes + 16)));
+    sb = 3;
+    const size_t used = static_cast<size_t>(sa) * a_stage + static_cast<size_t>(sb) * b_stage;
+    sq = used < budget ? static_cast<int>(std::min<size_t>(24, (budget - used) / (kQSlotBytes + 16))) : 0;
+    if (sq < 1) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "no shared memory left for the low-bit staging ring");
   } else if (nb <= 64) {
     sa = sb = static_cast<int>(std::min<size_t>(16, budget / (a_stage + b_stage)));
   } else {
     sb = 3;
-    sa = static_cast<int>(std::min<size_t>(16, (budget - static_cast<size_t>(sb) * b_stage) / a_stage));
+    const size_t used = static_cast<size_t>(sb) * b_stage;
+    sa = used < budget ? static_cast<int>(std::min<size_t>(16, (budget - used) / a_stage)) : 0;
   }
+  if (sa < 1 || sb < 1) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "expert pipeline does not fit in shared memory");
   const int smem_a = sa;
   xa.smem_a = smem_a;
   xa.stages_a = sa;
