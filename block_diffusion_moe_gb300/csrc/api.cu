@@ -536,16 +536,19 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
     ha.delta = acc->delta;
   }
   const int nb = (M + 15) & ~15;
-  const size_t fixed = head_smem_bytes(0, nb, accept) + 16 * 2 * 8;
-  // 8 stages (128 KB of weights in flight per SM) streamed best on GB300.
+  // Two K groups per stage at up to 64 positions (half the pipeline steps);
+  // 8 groups of weights (128 KiB) in flight per SM streamed best on GB300.
+  const int kg = (nb <= 64 && (d.hidden / 64) % 2 == 0) ? 2 : 1;
+  ha.kg = kg;
+  const size_t fixed = head_smem_bytes(0, nb, accept, kg) + 16 * 2 * 8;
   ha.stages = static_cast<int>(std::min<size_t>(
-      8, (static_cast<size_t>(kSmemBudget) - fixed) / (kATileBytes + static_cast<size_t>(nb) * 128)));
+      8 / kg, (static_cast<size_t>(kSmemBudget) - fixed) / (kg * (kATileBytes + static_cast<size_t>(nb) * 128))));
   const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
   // The final merge reuses the ring for 12 (accept: 20) bytes x 32 positions x grid.
-  if (static_cast<size_t>(ha.stages) * (kATileBytes + static_cast<size_t>(nb) * 128) <
-      static_cast<size_t>(grid) * 32 * (accept ? 20 : 12))
+  if (ha.stages < 1 || static_cast<size_t>(ha.stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) <
+                           static_cast<size_t>(grid) * 32 * (accept ? 20 : 12))
     return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
-  e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept), stream, kPdl);
+  e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept, kg), stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch head");
   return CLOVER_OK;
 }

@@ -55,14 +55,16 @@ struct HeadSmem {
   volatile int* s_ok;
   volatile int* s_last;
   int* s_counts;  // [2]: committed, still masked
-  uint32_t stage_bytes;
+  uint32_t half_bytes;   // one K group: A tile 16 KiB + B tile nb x 128 B
+  uint32_t stage_bytes;  // kg K groups
 };
 
 __device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int nb, bool accept) {
   HeadSmem s;
   const uint32_t r = smem_u32(raw);
   uint8_t* base = raw + ((1024u - (r & 1023u)) & 1023u);
-  s.stage_bytes = kATileBytes + static_cast<uint32_t>(nb) * 128u;
+  s.half_bytes = kATileBytes + static_cast<uint32_t>(nb) * 128u;
+  s.stage_bytes = s.half_bytes * static_cast<uint32_t>(p.kg);
   s.ring = base;
   float* f = reinterpret_cast<float*>(base + static_cast<size_t>(p.stages) * s.stage_bytes);
   s.wp_m = f;
@@ -142,12 +144,13 @@ __device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
   // CTAs' simultaneous requests do not all share the same offset within the
   // head rows (which would concentrate them on few DRAM channels). The MMA
   // consumes stages in issue order; only the accumulation order changes.
-  const int rot = static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(nk));
+  const int kg = p.kg;
+  const int rot = kg * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(nk / kg));
   int st = 0;
   uint32_t ph = 0, issued = 0, parity_bits = 0;
   bool ok = true;
   for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
-    for (int kc0 = 0; kc0 < nk; ++kc0) {
+    for (int kc0 = 0; kc0 < nk; kc0 += kg) {
       const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
       if (!mbar_wait(&s.empty[st], ph ^ 1u, s.abort)) {
         atomicOr(p.err, kErrMbarTimeout);
@@ -155,10 +158,14 @@ __device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
         ok = false;
         break;
       }
-      const uint32_t dst = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
+      const uint32_t dst0 = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
       mbar_arrive_expect_tx(&s.full[st], s.stage_bytes);
-      tma_load_2d(dst, &p.tm_w, &s.full[st], kc * 64, tile * 128, pol_w);
-      for (int i = 0; i < nb; i += 16) tma_load_2d(dst + kATileBytes + i * 128, &p.tm_x, &s.full[st], kc * 64, i, pol_x);
+      for (int h = 0; h < kg; ++h) {  // half h: K group kc + h (A tile, then B tile)
+        const uint32_t dst = dst0 + h * s.half_bytes;
+        tma_load_2d(dst, &p.tm_w, &s.full[st], (kc + h) * 64, tile * 128, pol_w);
+        for (int i = 0; i < nb; i += 16)
+          tma_load_2d(dst + kATileBytes + i * 128, &p.tm_x, &s.full[st], (kc + h) * 64, i, pol_x);
+      }
       issued |= 1u << st;
       parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
       if (++st == p.stages) {
@@ -190,7 +197,7 @@ __device__ void head_mma(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t 
     }
     tc_fence_after();
     const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * 256u;
-    for (int kc = 0; kc < nk; ++kc) {
+    for (int kc = 0; kc < nk; kc += p.kg) {
       if (!mbar_wait(&s.full[st], ph, s.abort)) {
         atomicOr(p.err, kErrMbarTimeout);
         *s.abort = 1u;
@@ -198,13 +205,15 @@ __device__ void head_mma(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t 
         break;
       }
       tc_fence_after();
-      const uint32_t a_addr = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
-      const uint64_t ad = umma_desc_sw128(a_addr);
-      const uint64_t bd = umma_desc_sw128(a_addr + kATileBytes);
+      for (int h = 0; h < p.kg; ++h) {
+        const uint32_t a_addr = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes + h * s.half_bytes);
+        const uint64_t ad = umma_desc_sw128(a_addr);
+        const uint64_t bd = umma_desc_sw128(a_addr + kATileBytes);
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                  (kc | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < 4; ++k)
+          umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                    (kc | h | k) != 0 ? 1u : 0u);
+      }
       umma_commit(&s.empty[st]);
       if (++st == p.stages) {
         st = 0;
@@ -560,8 +569,8 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
   }
 }
 
-size_t head_smem_bytes(int stages, int nb, bool accept) {
-  return 1024 + static_cast<size_t>(stages) * (kATileBytes + static_cast<size_t>(nb) * 128) +
+size_t head_smem_bytes(int stages, int nb, bool accept, int kg) {
+  return 1024 + static_cast<size_t>(stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) +
          static_cast<size_t>(nb) * (4 * 12 + 12 + 4 + (accept ? 4 * 8 + 8 : 0)) + 4 * 32 * 33 * sizeof(float) +
          static_cast<size_t>(2 * stages + 5) * 8 + 64;
 }

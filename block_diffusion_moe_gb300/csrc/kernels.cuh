@@ -179,6 +179,7 @@ struct HeadArgs {
   int* n_masked_left;  // scalar out (nullable)
   int* err;
   int M, H, V, mask_id, block, n_tiles, stages;
+  int kg;  // K groups of 64 per pipeline stage (1 or 2)
   float threshold;
   // Accept mode (self-speculative verify): blocks of `block` rows, row j
   // testing draft[j]; the unmask fields above are unused then.
@@ -217,6 +218,6 @@ constexpr int kLayerMaxTokens = 32;
 cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl);
 
 size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q, int kg);
-size_t head_smem_bytes(int stages, int nb, bool accept);
+size_t head_smem_bytes(int stages, int nb, bool accept, int kg);
 
 }  // namespace clover
