@@ -2,8 +2,7 @@
 //
 // Some callers cannot allocate device memory at all: a plug-in that runs
 // inside a host application which owns every byte of the GPU (a serving
-// process with a fixed memory budget or its own pool), code that runs while
-// a CUDA graph is being captured (where cudaMalloc is not allowed), or a
+// process with a fixed memory budget or its own pool), or a
 // latency-critical loop that cannot afford the synchronisation an allocation
 // may imply. For them this file keeps the scratch memory of
 // clover_lmhead_unmask in a fixed, file-scope device array that exists for as

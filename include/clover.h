@@ -246,9 +246,9 @@ int32_t clover_last_error(char* buf, size_t n);
 /* Same operation and arguments as clover_lmhead_unmask, without the
  * workspace. (The pages have no counterpart: this is a library convenience.)
  * For callers that cannot allocate device memory -- a plug-in inside an
- * application that owns all GPU memory, code running during CUDA graph
- * capture, a latency-critical loop that must not synchronise on an
- * allocation. The scratch lives in a 1 MiB array inside the library that
+ * application that owns all GPU memory and hands out no allocator, or a
+ * latency-critical loop that must not synchronise on an allocation. The
+ * scratch lives in a 1 MiB array inside the library that
  * every GPU loading the library keeps until the process exits; it fits up to
  * 102 positions at hidden 2048 (the rule: clover_head_workspace_bytes(dims, M)
  * <= 1 MiB). Larger sizes return CLOVER_ERR_WORKSPACE_TOO_SMALL and nothing

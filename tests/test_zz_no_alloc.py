@@ -1,9 +1,8 @@
 """The allocation-free head + unmask entry point.
 
 clover_lmhead_unmask_static exists for callers that cannot allocate device
-memory (a plug-in inside an application that owns all GPU memory, code that
-runs during CUDA graph capture, latency-critical loops that must not wait on
-an allocation): its scratch is a fixed 1 MiB array inside the library. These
+memory (a plug-in inside an application that owns all GPU memory,
+latency-critical loops that must not wait on an allocation): its scratch is a fixed 1 MiB array inside the library. These
 checks call it through the C ABI, twice in a row, and compare each result
 with the regular workspace-based clover_lmhead_unmask on the same inputs.
 This file is collected last on purpose."""
