@@ -48,8 +48,7 @@ enum CtrlWord : int {
   kCtrlMaskedLeft = 2,   // positions still masked after the last head call
   kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
   kCtrlCommitted = 4,    // positions committed by the last head call
-  kCtrlBarCtr = 5,       // fused-layer grid barrier: arrivals (back to zero after each barrier)
-  kCtrlBarGen = 6,       // fused-layer grid barrier: generation
+  kCtrlBarCount = 6,     // [u64, words 6-7] fused-layer grid barrier arrivals (only grows)
   kCtrlTokenGroups = 8,  // [32] routing arrival counters (reset by their last CTA)
   kCtrlStamps = 40,      // [8 x u64] phase timestamps of the last fused-layer launch (diagnostics)
 };
@@ -271,7 +270,7 @@ int record(cudaEvent_t ev, cudaStream_t s) {
 // block; err: status word to flag.
 int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const float* x_in, float* x_out,
                       int32_t* out_idx, float* out_w, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, const void* next_router = nullptr) {
   const MoeLayout L = moe_layout(d, M);
   const int H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
   const int MK = M * K;
@@ -359,12 +358,22 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     if ((rc = encode_bf16_2d(&xa.tm_dn, layer.down, static_cast<uint64_t>(E) * H, F, 128, "down"))) return rc;
     if ((rc = encode_bf16_2d(&xa.tm_sdn, layer.sh_down, H, F, 128, "shared down"))) return rc;
   }
+  // B tiles move in boxes of up to 64 rows (one TMA instruction each), with
+  // 16-row boxes for the rest; fewer, larger copies stream faster.
+  const int nb_rows = (M + 15) & ~15;
   if (fused) {  // the gate/up B operand is the dense block of normed rows
-    if ((rc = encode_bf16_2d(&xa.tm_xg, xg + static_cast<size_t>(MK) * H, M, H, 16, "normed rows"))) return rc;
+    const bf16* xn_rows = xg + static_cast<size_t>(MK) * H;
+    if ((rc = encode_bf16_2d(&xa.tm_xg, xn_rows, M, H, 16, "normed rows"))) return rc;
+    if ((rc = encode_bf16_2d(&xa.tm_xg_big, xn_rows, M, H, nb_rows, "normed rows"))) return rc;
+    xa.xg_box = nb_rows;
   } else {
     if ((rc = encode_bf16_2d(&xa.tm_xg, xg, R, H, 16, "gathered inputs"))) return rc;
+    if ((rc = encode_bf16_2d(&xa.tm_xg_big, xg, R, H, 64, "gathered inputs"))) return rc;
+    xa.xg_box = 64;
   }
   if ((rc = encode_bf16_2d(&xa.tm_h, hbuf, R, F, 16, "swiglu outputs"))) return rc;
+  if ((rc = encode_bf16_2d(&xa.tm_h_big, hbuf, R, F, 64, "swiglu outputs"))) return rc;
+  xa.h_box = 64;
   xa.x_in = x_in;
   xa.x_out = x_out;
   xa.hbuf = hbuf;
@@ -421,18 +430,18 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.stages_b = sb;
   xa.stages_q = sq;
   xa.nb_max = nb;
-  // Up to 32 tokens the slice that finishes last combines (a few µs); with
-  // more tokens that serial walk would dominate, so a parallel kernel does it.
+  // Up to 32 tokens the down unit that completes a hidden slice combines it
+  // (a few µs); with more tokens that serial walk would dominate, so a
+  // parallel kernel does it.
   xa.combine = fused ? 1 : 0;
   size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq, kg);
   if (fused) {
     xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
+    xa.wr_next = reinterpret_cast<const bf16*>(next_router);
     xa.bias = layer.router_bias;
     xa.logits = reinterpret_cast<float*>(data + L.logits);
     xa.xn = xg + static_cast<size_t>(MK) * H;
-    xa.bar_ctr = ctrl + kCtrlBarCtr;
-    xa.bar_gen = ctrl + kCtrlBarGen;
-    xa.tg_ctr = ctrl + kCtrlTokenGroups;
+    xa.bar_count = reinterpret_cast<unsigned long long*>(ctrl + kCtrlBarCount);
     xa.pub_idx = topk_idx;
     xa.pub_w = topk_w;
     xa.pub_p = reinterpret_cast<float*>(data + L.topk_p);
@@ -500,7 +509,10 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
   memset(&ha, 0, sizeof(ha));
   int rc;
   if ((rc = encode_bf16_2d(&ha.tm_w, head_w, d.vocab, d.hidden, 128, "head"))) return rc;
-  if ((rc = encode_bf16_2d(&ha.tm_x, xn, M, d.hidden, 16, "normed positions"))) return rc;
+  // One box carries a K group of all positions (rows past M read as zeros).
+  const int nb = (M + 15) & ~15;
+  if ((rc = encode_bf16_2d(&ha.tm_x, xn, M, d.hidden, static_cast<uint32_t>(nb), "normed positions"))) return rc;
+  ha.x_box = nb;
   ha.alpha = alpha;
   ha.part_m = reinterpret_cast<float*>(data + L.part_m);
   ha.part_s = reinterpret_cast<float*>(data + L.part_s);
@@ -535,7 +547,6 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
     ha.ratio = acc->ratio;
     ha.delta = acc->delta;
   }
-  const int nb = (M + 15) & ~15;
   // Two K groups per stage at up to 64 positions (half the pipeline steps);
   // 8 groups of weights (128 KiB) in flight per SM streamed best on GB300.
   const int kg = (nb <= 64 && (d.hidden / 64) % 2 == 0) ? 2 : 1;
@@ -610,7 +621,8 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
   if (e != cudaSuccess) return cuda_fail(e, "launch embed");
   for (int l = 0; l < n_layers; ++l) {
     rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,
-                           reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s);
+                           reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s,
+                           l + 1 < n_layers ? layers[l + 1].router_w : nullptr);
     if (rc) return rc;
   }
   rc = enqueue_head(*dims, head_w, x, logit_scale, threshold, block, tokens, masked, nullptr, nullptr, nullptr,

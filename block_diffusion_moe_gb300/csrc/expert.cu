@@ -206,7 +206,21 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
   uint32_t pha = 0, issued = 0, parity_bits = 0;
   for (int it = 0;; ++it) {
     int u = atomicAdd(p.unit_ctr, 1);
-    if (u >= n_total) u = kUnitEnd;
+    if (u >= n_total) {
+      u = kUnitEnd;
+      if (p.wr_next != nullptr) {
+        // No unit left: while the last units drain, ask L2 for the router
+        // rows this CTA will stage in the next layer (same item mapping).
+        const int n_eg = (p.E + kRouteExperts - 1) / kRouteExperts;
+        const int n_items = n_eg * ((p.M + kRouteTokens - 1) / kRouteTokens);
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+          const int eg = item % n_eg;
+          const int ne = min(kRouteExperts, p.E - eg * kRouteExperts);
+          bulk_prefetch_l2(p.wr_next + static_cast<size_t>(eg) * kRouteExperts * p.H,
+                           static_cast<uint32_t>(ne * p.H * 2));
+        }
+      }
+    }
     const int us = it & (kExpertUnitRing - 1);
     const uint32_t upar = (it / kExpertUnitRing) & 1;
     if (!mbar_wait(&s.uempty[us], upar ^ 1u, s.abort)) {
@@ -401,12 +415,17 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
     const int nrows = unit_rows(w, rt, p);
     const int row0 = (w.kind == 0 && rt.dense) ? 0 : w.off;
     const CUtensorMap* m;
-    int nk;
+    const CUtensorMap* mb;
+    int nk, box;
     if (w.kind == 0) {
       m = &p.tm_xg;
+      mb = &p.tm_xg_big;
+      box = p.xg_box;
       nk = p.H >> 6;
     } else {
       m = &p.tm_h;
+      mb = &p.tm_h_big;
+      box = p.h_box;
       nk = p.F >> 6;
       // The expert's SwiGLU rows must be complete before they are loaded.
       const unsigned long long t0 = global_ns();
@@ -440,7 +459,11 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(kg * nrows) * 128u);
       for (int h = 0; h < kg; ++h) {
         const uint32_t dst = dst0 + h * s.b_half_bytes;
-        for (int i = 0; i < nrows; i += 16) tma_load_2d(dst + i * 128, m, &s.full_b[sb], (kc + h) * 64, row0 + i, pol);
+        for (int i = 0; i < nrows;) {
+          const bool big = nrows - i >= box;
+          tma_load_2d(dst + i * 128, big ? mb : m, &s.full_b[sb], (kc + h) * 64, row0 + i, pol);
+          i += big ? box : 16;
+        }
       }
       issued |= 1u << sb;
       parity_bits = (parity_bits & ~(1u << sb)) | (phb << sb);
@@ -567,20 +590,20 @@ __device__ __forceinline__ void combine_store(const ExpertArgs& p, int t, size_t
   *reinterpret_cast<float4*>(p.x_out + static_cast<size_t>(t) * p.H + col) = o;
 }
 
-// Sums the weighted expert rows of one 128-wide hidden slice into the
-// residual stream: x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t),
-// selections in order, then the shared row, then the residual. Two tokens
-// are in flight per thread.
-__device__ void combine_slice(const ExpertArgs& p, const Rt& rt, int j, int etid) {
+// Sums the weighted expert rows of tokens t0..t1-1 in one 128-wide hidden
+// slice into the residual stream: x_out = x_in + (sum_k w_tk y_{slot(t,k)})
+// + y_shared(t), selections in order, then the shared row, then the
+// residual. Two tokens are in flight per thread.
+__device__ void combine_slice(const ExpertArgs& p, const Rt& rt, int j, int t0, int t1, int etid) {
   const int c4 = (etid & 31) * 4;
   const int g = etid >> 5;
   const size_t H = p.H;
   const size_t col = static_cast<size_t>(j) * 128 + c4;
   const int MK = p.M * p.K;
   const int K = p.K;
-  for (int t = g; t < p.M; t += 8) {
+  for (int t = t0 + g; t < t1; t += 8) {
     const int t2 = t + 4;
-    const bool two = t2 < p.M;
+    const bool two = t2 < t1;
     const float4 ys = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t) * H + col));
     const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * H + col);
     float4 ys2 = make_float4(0.f, 0.f, 0.f, 0.f), xi2 = ys2;
@@ -725,9 +748,9 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
         *s.s_last = last;
       }
       named_bar_sync(1, 128);
-      if (*s.s_last) {
+      if (*s.s_last) {  // this unit completed the slice: combine it for all tokens
         __threadfence();
-        combine_slice(p, rt, w.slice, etid);
+        combine_slice(p, rt, w.slice, 0, p.M, etid);
       }
     }
   }
@@ -770,6 +793,12 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
     tma_prefetch_desc(kQ4 ? &p.tm_sgu_q : &p.tm_sgu);
     tma_prefetch_desc(kQ4 ? &p.tm_dn_q : &p.tm_dn);
     tma_prefetch_desc(kQ4 ? &p.tm_sdn_q : &p.tm_sdn);
+  }
+  if (warp == 2 && lane == 0) {
+    tma_prefetch_desc(&p.tm_xg);
+    tma_prefetch_desc(&p.tm_xg_big);
+    tma_prefetch_desc(&p.tm_h);
+    tma_prefetch_desc(&p.tm_h_big);
   }
   if (warp == 1) {
     tmem_alloc(s.tmem_slot, 512);
@@ -830,29 +859,29 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
 namespace {
 
 // Grid-wide barrier for a persistent launch (every CTA is resident: one per
-// SM). The last CTA to arrive resets the counter and bumps the generation
-// word the others wait on (bounded). Returns false on timeout.
-__device__ bool grid_barrier(int* ctr, int* gen, int* err) {
+// SM). The arrival count only grows: the arrival number a CTA draws tells it
+// which multiple of the grid size ends its barrier, so nothing is reset and
+// the last CTA to arrive leaves at once. Waits are bounded; returns false on
+// timeout.
+__device__ bool grid_barrier(unsigned long long* count, int* err) {
   __shared__ int s_pass;
   fence_proxy_async_global();  // rows stored before the barrier are read by TMA after it
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int g0 = ld_acquire_gpu(gen);
+    const unsigned long long g = gridDim.x;
+    const unsigned long long old = atom_add_acq_rel_gpu_u64(count, 1ull);
+    const unsigned long long target = (old / g + 1ull) * g;
     int pass = 1;
-    if (atomicAdd(ctr, 1) == static_cast<int>(gridDim.x) - 1) {
-      atomicExch(ctr, 0);
-      __threadfence();
-      atomicAdd(gen, 1);
-    } else {
+    if (old + 1ull != target) {
       const unsigned long long t0 = global_ns();
-      while (ld_acquire_gpu(gen) == g0) {
+      while (ld_acquire_gpu_u64(count) < target) {
         if (global_ns() - t0 > kWaitLimitNs) {
           atomicOr(err, kErrDepTimeout);
           pass = 0;
           break;
         }
-        __nanosleep(32);
+        __nanosleep(20);
       }
     }
     s_pass = pass;
@@ -872,8 +901,13 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     k_layer(const __grid_constant__ ExpertArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
+  // bulk-copy barriers: router slices, token rows
   uint64_t* wbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.tmem_slot) + 96);
-  if (threadIdx.x == 0) mbar_init(wbar, 1);  // made visible by the prologue's fence
+  uint64_t* xbar = wbar + 1;
+  if (threadIdx.x == 0) {  // made visible by the prologue's fence
+    mbar_init(wbar, 1);
+    mbar_init(xbar, 1);
+  }
   const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
@@ -898,7 +932,14 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   // into the (still idle) weight ring before waiting.
   const int my_items = (n_items > static_cast<int>(blockIdx.x)) ? (n_items - 1 - blockIdx.x) / G + 1 : 0;
   const uint32_t wslice = kRouteExperts * H * 2;
-  const bool wr_staged = my_items * wslice <= static_cast<uint32_t>(p.smem_a) * s.a_stage_bytes;
+  const uint32_t ring_bytes = static_cast<uint32_t>(p.smem_a) * s.a_stage_bytes;
+  const bool wr_staged = my_items * wslice <= ring_bytes;
+  // A CTA with one item also stages that item's token rows (contiguous in
+  // x_in) behind its router slices, when they fit.
+  const int xt0 = (blockIdx.x / n_eg) * kRouteTokens;
+  const uint32_t x_off = my_items * wslice;
+  const uint32_t x_bytes = my_items == 1 ? static_cast<uint32_t>(min(kRouteTokens, M - xt0)) * H * 4 : 0u;
+  const bool x_staged = wr_staged && my_items == 1 && x_off + x_bytes <= ring_bytes;
   if (threadIdx.x == 0 && wr_staged && my_items > 0) {
     uint32_t bytes = 0;
     for (int j = 0; j < my_items; ++j) {
@@ -917,15 +958,19 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pdl_wait();
   pdl_trigger();
   if (st) st[1] = global_ns();
+  if (threadIdx.x == 0 && x_staged) {  // written by the previous kernel
+    mbar_arrive_expect_tx(xbar, x_bytes);
+    bulk_load(smem_u32(s.a_ring) + x_off, p.x_in + static_cast<size_t>(xt0) * H, x_bytes, xbar);
+  }
 
-  // Phase 1: norms, normed rows (written once) and router logits. The last
-  // CTA to finish a token group takes top-k for its tokens.
+  // Phase 1: norms, normed rows (written once) and router logits.
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i <= E; i += blockDim.x) p.gu_done[i] = 0;
     for (int i = threadIdx.x; i < (H >> 7); i += blockDim.x) p.dn_done[i] = 0;
-    if (threadIdx.x == 0) *p.unit_ctr = 0;
+    if (threadIdx.x == 0) {
+      *p.unit_ctr = 0;
+    }
   }
-  __shared__ int s_tg_last;
   if (wr_staged && my_items > 0 && !mbar_wait(wbar, 0, s.abort)) {
     atomicOr(p.err, kErrMbarTimeout);
     *s.abort = 1u;
@@ -936,7 +981,12 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     const int ne = min(kRouteExperts, E - e0);
     const int t = tg * kRouteTokens + warp;
     if (warp < kRouteTokens && t < M) {
-      const float* xr = p.x_in + static_cast<size_t>(t) * H;
+      if (x_staged && !mbar_wait(xbar, 0, s.abort)) {
+        atomicOr(p.err, kErrMbarTimeout);
+        *s.abort = 1u;
+      }
+      const float* xr = x_staged ? reinterpret_cast<const float*>(s.a_ring + x_off) + static_cast<size_t>(warp) * H
+                                 : p.x_in + static_cast<size_t>(t) * H;
       const __nv_bfloat16* w_rows = wr_staged ? reinterpret_cast<const __nv_bfloat16*>(s.a_ring + j * wslice)
                                               : p.wr + static_cast<size_t>(e0) * H;
       __nv_bfloat16* xn_out = eg == 0 ? p.xn + static_cast<size_t>(t) * H : nullptr;
@@ -947,24 +997,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
         const float rstd = row_rstd(xr, H, p.eps, lane);
         lg = warp_router_dots<kRouteExperts>(xr, rstd, w_rows, ne, H, lane, xn_out);
       }
-      if (lane < ne) p.logits[static_cast<size_t>(t) * E + e0 + lane] = lg + (p.bias ? p.bias[e0 + lane] : 0.f);
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0 && p.stamps != nullptr) atomicMax(p.stamps + 7, global_ns());
-    if (threadIdx.x == 0) s_tg_last = (atomicAdd(&p.tg_ctr[tg], 1) == n_eg - 1) ? 1 : 0;
-    __syncthreads();
-    if (s_tg_last) {
-      __threadfence();
-      if (warp < kRouteTokens && t < M) {
-        const TopkSel sel = warp_topk(p.logits + static_cast<size_t>(t) * E, E, K, lane);
-        if (lane < K) {
-          p.pub_idx[t * K + lane] = sel.e;
-          p.pub_w[t * K + lane] = sel.w;
-          p.pub_p[t * K + lane] = sel.p;
-        }
+      if (lane < ne) {
+        const float v = lg + (p.bias ? p.bias[e0 + lane] : 0.f);
+        p.logits[static_cast<size_t>(t) * E + e0 + lane] = v;
       }
-      if (threadIdx.x == 0) p.tg_ctr[tg] = 0;
     }
   }
   fence_proxy_async_shared();  // the ring was read generically; TMA refills it later
@@ -972,24 +1008,47 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0) atomicMax(p.stamps + 2, global_ns());
   }
-  if (!grid_barrier(p.bar_ctr, p.bar_gen, p.err)) *s.abort = 1u;
+  if (!grid_barrier(p.bar_count, p.err)) *s.abort = 1u;
   if (st) st[3] = global_ns();
 
-  const int32_t* fin_idx = p.pub_idx;
-  const float* fin_w = p.pub_w;
-  if (p.coreset_top_p > 0.f) {
-    // Block coreset (the M tokens are one block): every CTA computes the same
-    // kept set from the published first-pass selections, CTA t re-routes
-    // token t within it, and a second barrier publishes the result.
-    float* s_mass = reinterpret_cast<float*>(s_nact + 1);  // [E]
+  // Top-k: CTA t (< M) takes token t with one warp and publishes its
+  // selections; a second barrier, then every CTA copies all of them into
+  // its routing tables. (The same selection in every CTA for all M tokens
+  // costs several µs of cross-lane reductions per CTA; spread over M CTAs it
+  // is one token's worth.)
+  const bool coreset = p.coreset_top_p > 0.f;
+  float* s_p = reinterpret_cast<float*>(s_nact + 1);  // [M*K] full-softmax probability of each selection
+  auto route_token = [&](int t, const uint32_t* allowed, bool want_p, int32_t* out_idx, float* out_w, float* out_p) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? __ldcg(p.logits + static_cast<size_t>(t) * E + e) : -INFINITY;
+    }
+    TopkSel sel[1];
+    warp_topk_regs<1>(v, E, K, lane, allowed, want_p, sel);
+    if (lane < K) {
+      out_idx[t * K + lane] = sel[0].e;
+      out_w[t * K + lane] = sel[0].w;
+      if (want_p) out_p[t * K + lane] = sel[0].p;
+    }
+  };
+  if (static_cast<int>(blockIdx.x) < M && warp == 0) route_token(blockIdx.x, nullptr, coreset, p.pub_idx, p.pub_w, p.pub_p);
+  if (!grid_barrier(p.bar_count, p.err)) *s.abort = 1u;
+  for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+    const int e = __ldcg(p.pub_idx + i);
+    s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
+    s_w[i] = __ldcg(p.pub_w + i);
+    if (coreset) s_p[i] = __ldcg(p.pub_p + i);
+  }
+  if (coreset) {
+    // Block coreset (the M tokens are one block): every CTA computes the
+    // same kept set from the first-pass selections, CTA t re-routes token t
+    // within it, and a third barrier publishes the result.
+    float* s_mass = s_p + MK;                                // [E]
     float* s_smass = s_mass + E;                             // [E] masses in kept order
     int* s_sid = reinterpret_cast<int*>(s_smass + E);        // [E] expert ids in kept order
     uint32_t* s_allow = reinterpret_cast<uint32_t*>(s_sid + E);  // [8]
-    for (int i = threadIdx.x; i < MK; i += blockDim.x) {
-      const int e = __ldcg(p.pub_idx + i);
-      s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-      s_w[i] = __ldcg(p.pub_p + i);
-    }
     for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
     if (threadIdx.x < 8) s_allow[threadIdx.x] = 0u;
     __syncthreads();
@@ -997,10 +1056,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {  // mass: probabilities in token order
       float m = 0.f;
-      for (uint32_t b = s_mask[e]; b != 0u; b &= b - 1u) {
-        const int t = __ffs(b) - 1;
+      for (uint32_t bm = s_mask[e]; bm != 0u; bm &= bm - 1u) {
+        const int t = __ffs(bm) - 1;
         for (int k = 0; k < K; ++k)
-          if (s_idx[t * K + k] == e) m += s_w[t * K + k];
+          if (s_idx[t * K + k] == e) m += s_p[t * K + k];
       }
       s_mass[e] = m;
     }
@@ -1025,70 +1084,73 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
       float carry = 0.f;
       int cut = E - 1;
       for (int c0 = 0; c0 < E; c0 += 32) {
-        float v = c0 + lane < E ? s_smass[c0 + lane] : 0.f;
+        float cv = c0 + lane < E ? s_smass[c0 + lane] : 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const float n = __shfl_up_sync(0xffffffffu, v, o);
-          if (lane >= o) v += n;
+          const float nb = __shfl_up_sync(0xffffffffu, cv, o);
+          if (lane >= o) cv += nb;
         }
-        const float cum = carry + v;
+        const float cum = carry + cv;
         const unsigned hit = __ballot_sync(0xffffffffu, c0 + lane < E && cum >= target && c0 + lane >= K - 1);
         if (hit) {
           cut = c0 + __ffs(hit) - 1;
           break;
         }
-        carry += __shfl_sync(0xffffffffu, v, 31);
+        carry += __shfl_sync(0xffffffffu, cv, 31);
       }
       for (int r = lane; r <= cut; r += 32) atomicOr(&s_allow[s_sid[r] >> 5], 1u << (s_sid[r] & 31));
     }
     __syncthreads();
-    if (static_cast<int>(blockIdx.x) < M && warp == 0) {
-      const int t = blockIdx.x;
-      const TopkSel sel = warp_topk(p.logits + static_cast<size_t>(t) * E, E, K, lane, s_allow);
-      if (lane < K) {
-        p.pub2_idx[t * K + lane] = sel.e;
-        p.pub2_w[t * K + lane] = sel.w;
-      }
+    if (static_cast<int>(blockIdx.x) < M && warp == 0)
+      route_token(blockIdx.x, s_allow, false, p.pub2_idx, p.pub2_w, nullptr);
+    if (!grid_barrier(p.bar_count, p.err)) *s.abort = 1u;
+    for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+      const int e = __ldcg(p.pub2_idx + i);
+      s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
+      s_w[i] = __ldcg(p.pub2_w + i);
     }
-    if (!grid_barrier(p.bar_ctr, p.bar_gen, p.err)) *s.abort = 1u;
-    fin_idx = p.pub2_idx;
-    fin_w = p.pub2_w;
   }
 
-  // Phase 2: every CTA builds the same permutation from the published top-k.
-  for (int i = threadIdx.x; i < MK; i += blockDim.x) {
-    const int e = __ldcg(fin_idx + i);
-    s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-    s_w[i] = __ldcg(fin_w + i);
-  }
+  // Phase 2: every CTA builds the same permutation from its top-k tables.
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_mask[e] = 0u;
   __syncthreads();
   for (int i = threadIdx.x; i < MK; i += blockDim.x) atomicOr(&s_mask[s_idx[i]], 1u << (i / K));
   __syncthreads();
-  if (warp == 0) {  // counts, offsets and the active list, 32 experts at a time
-    int base_off = 0, base_act = 0;
-    for (int e0c = 0; e0c < E; e0c += 32) {
-      const int e = e0c + lane;
-      const int c = (e < E) ? __popc(s_mask[e]) : 0;
-      int incl = c, acti = c > 0 ? 1 : 0;
+  {  // counts, offsets and the active list: warp w scans experts 32w..32w+31
+    __shared__ int s_wsum[2][kMaxExperts / 32];
+    const int e = threadIdx.x;
+    const bool in = warp < kMaxExperts / 32;
+    const int c = (in && e < E) ? __popc(s_mask[e]) : 0;
+    int incl = c, acti = c > 0 ? 1 : 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n1 = __shfl_up_sync(0xffffffffu, incl, o);
-        const int n2 = __shfl_up_sync(0xffffffffu, acti, o);
-        if (lane >= o) {
-          incl += n1;
-          acti += n2;
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n1 = __shfl_up_sync(0xffffffffu, incl, o);
+      const int n2 = __shfl_up_sync(0xffffffffu, acti, o);
+      if (lane >= o) {
+        incl += n1;
+        acti += n2;
       }
-      if (e < E) {
-        s_cnt[e] = c;
-        s_off[e] = base_off + incl - c;
-        if (c > 0) s_act[base_act + acti - 1] = e;
-      }
-      base_off += __shfl_sync(0xffffffffu, incl, 31);
-      base_act += __shfl_sync(0xffffffffu, acti, 31);
     }
-    if (lane == 0) *s_nact = base_act;
+    if (in && lane == 31) {
+      s_wsum[0][warp] = incl;
+      s_wsum[1][warp] = acti;
+    }
+    __syncthreads();
+    if (in && e < E) {
+      int base_off = 0, base_act = 0;
+      for (int w2 = 0; w2 < warp; ++w2) {
+        base_off += s_wsum[0][w2];
+        base_act += s_wsum[1][w2];
+      }
+      s_cnt[e] = c;
+      s_off[e] = base_off + incl - c;
+      if (c > 0) s_act[base_act + acti - 1] = e;
+    }
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w2 = 0; w2 < kMaxExperts / 32; ++w2) tot += s_wsum[1][w2];
+      *s_nact = tot;
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < MK; i += blockDim.x) {
@@ -1125,7 +1187,10 @@ size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int
          static_cast<size_t>(2 * stages_a + 2 * stages_b + 2 * stages_q + 5 + 2 * kExpertUnitRing) * 8 + 256;
 }
 
-size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(3 * M * K + 7 * E + 16) * 4; }
+// idx, w, slot, coreset probability [M*K] each; mask, count, offset, active,
+// coreset mass, sorted mass, sorted id [E] each; the active count and the
+// coreset's allowed-set words.
+size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }
 
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
   auto* k = a.q4 ? k_layer<true> : k_layer<false>;

@@ -163,7 +163,7 @@ __device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
       for (int h = 0; h < kg; ++h) {  // half h: K group kc + h (A tile, then B tile)
         const uint32_t dst = dst0 + h * s.half_bytes;
         tma_load_2d(dst, &p.tm_w, &s.full[st], (kc + h) * 64, tile * 128, pol_w);
-        for (int i = 0; i < nb; i += 16)
+        for (int i = 0; i < nb; i += p.x_box)
           tma_load_2d(dst + kATileBytes + i * 128, &p.tm_x, &s.full[st], (kc + h) * 64, i, pol_x);
       }
       issued |= 1u << st;

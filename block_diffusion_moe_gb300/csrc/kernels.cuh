@@ -103,8 +103,11 @@ struct ExpertArgs {
   CUtensorMap tm_sgu;  // shared gate/up  [2F][H]
   CUtensorMap tm_dn;   // routed down     [E*H][F]
   CUtensorMap tm_sdn;  // shared down     [H][F]
-  CUtensorMap tm_xg;   // gathered inputs [M*K+M][H]
-  CUtensorMap tm_h;    // SwiGLU outputs  [M*K+M][F]
+  CUtensorMap tm_xg;   // gathered inputs [M*K+M][H], boxes of 16 rows
+  CUtensorMap tm_h;    // SwiGLU outputs  [M*K+M][F], boxes of 16 rows
+  CUtensorMap tm_xg_big;  // the same, boxes of xg_box rows
+  CUtensorMap tm_h_big;   // the same, boxes of h_box rows
+  int xg_box, h_box;      // rows per big box (multiples of 16)
   // Low-bit expert weights (q4 != 0): codes by TMA (uint8, box 32 B x rows),
   // scales by bulk copy; stages_q staging slots of kQSlotBytes.
   CUtensorMap tm_gu_q;   // [E*2F][H/2]
@@ -137,16 +140,15 @@ struct ExpertArgs {
   int* err;
   int M, H, F, E, K;
   int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
-  int combine;                     // 1: the last down unit of each slice combines; 0: k_combine does
+  int combine;  // 1: the down unit that completes a hidden slice combines it; 0: k_combine does
   // fused-layer launches only (k_layer)
   const bf16* wr;      // [E][H] router
+  const bf16* wr_next; // [E][H] the next layer's router (nullable): its slices are prefetched into L2
   const float* bias;   // [E] or null
   float* logits;       // [M][E]
   bf16* xn;            // [M][H] normed rows = the gate/up B operand
-  int* bar_ctr;        // grid barrier arrival counter (zero between launches)
-  int* bar_gen;        // grid barrier generation
-  int* tg_ctr;         // [ceil(M/8)] token-group arrival counters (zero between launches)
-  int32_t* pub_idx;    // [M][K] top-k ids published by the token groups' last CTAs
+  unsigned long long* bar_count;  // grid barrier arrivals (only grows; 8-byte aligned)
+  int32_t* pub_idx;    // [M][K] top-k ids published by CTA t for token t
   float* pub_w;        // [M][K] top-k weights, likewise
   float* pub_p;        // [M][K] full-softmax probability of each selection (coreset mass)
   int32_t* pub2_idx;   // [M][K] selections after the coreset re-routing
@@ -156,9 +158,9 @@ struct ExpertArgs {
   float* out_w;
   float eps;
   unsigned long long* stamps;  // optional phase timestamps (diagnostics): [0] start, [1] after the
-                               // dependency wait, [2] last CTA done with phase 1, [3] after the
-                               // barrier, [4] routing done, [5] last CTA done, [6] last down
-                               // unit's outputs stored
+                               // dependency wait, [2] last CTA done with the router logits, [3]
+                               // after the barrier, [4] routing done, [5] last CTA done, [6] last
+                               // down unit's outputs stored
 };
 
 struct HeadArgs {
@@ -179,7 +181,8 @@ struct HeadArgs {
   int* n_masked_left;  // scalar out (nullable)
   int* err;
   int M, H, V, mask_id, block, n_tiles, stages;
-  int kg;  // K groups of 64 per pipeline stage (1 or 2)
+  int kg;     // K groups of 64 per pipeline stage (1 or 2)
+  int x_box;  // rows per TMA box of the normed positions (a multiple of 16)
   float threshold;
   // Accept mode (self-speculative verify): blocks of `block` rows, row j
   // testing draft[j]; the unmask fields above are unused then.

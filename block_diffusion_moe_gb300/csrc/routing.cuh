@@ -134,47 +134,67 @@ struct TopkSel {
   float p;  // softmax probability over all E logits (coreset mass)
 };
 
+// Unsigned key with the order of the float values (-0 and +0, equal as
+// floats, share one key), and back.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  b = (b == 0x80000000u) ? 0u : b;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // One warp, NT tokens at once (independent chains, interleaved for latency):
 // top-k of E (<= 256) logits by descending value, the lower expert id first
 // on ties, restricted to the experts whose bit is set in `allowed` (8 words;
-// null = all). Weights = softmax over the selected logits (= the top-k
+// null = all). v[n * 8 + i] holds the logit of expert lane + 32 i of token n
+// (-inf past E). Weights = softmax over the selected logits (= the top-k
 // probabilities renormalised). Lane k (< K) receives selection k of token n
-// in out[n], with its weight and its probability under the softmax over all
-// E. Tokens with valid[n] false read nothing; their out[n] is meaningless.
-// The per-token arithmetic does not depend on NT.
+// in out[n], with its weight and, when want_p, its probability under the
+// softmax over all E. Tokens with valid[n] false give meaningless out[n].
+// Each round takes the warp-wide largest key with one reduction and the
+// lowest expert id holding it with a second one; the per-token arithmetic
+// does not depend on NT.
 template <int NT>
-__device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], const bool (&valid)[NT], int E, int K,
-                                            int lane, const uint32_t* allowed, TopkSel (&out)[NT]) {
-  float v[NT * 8];
+__device__ __forceinline__ void warp_topk_regs(const float (&v)[NT * 8], int E, int K, int lane,
+                                               const uint32_t* allowed, bool want_p, TopkSel (&out)[NT]) {
   float all_max[NT], all_sum[NT];
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
     all_max[n] = -INFINITY;
+    all_sum[n] = 1.f;
+  }
+  if (want_p) {
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) all_max[n] = fmaxf(all_max[n], v[n * 8 + i]);
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) all_max[n] = warp_max_f(all_max[n]);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      all_sum[n] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) all_sum[n] += (lane + 32 * i < E) ? expf(v[n * 8 + i] - all_max[n]) : 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) all_sum[n] = warp_sum_f(all_sum[n]);
+  }
+  // Removed and disallowed experts compete as -inf (as a -inf logit would);
+  // slots past E have key 0, below every value.
+  const uint32_t kNegInf = order_key(-INFINITY);
+  uint32_t key[NT * 8];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
-      v[n * 8 + i] = (valid[n] && e < E) ? __ldcg(rows[n] + e) : -INFINITY;
-      all_max[n] = fmaxf(all_max[n], v[n * 8 + i]);
+      const bool ok = allowed == nullptr || ((allowed[e >> 5] >> (e & 31)) & 1u);
+      key[n * 8 + i] = (e < E) ? (ok ? order_key(v[n * 8 + i]) : kNegInf) : 0u;
     }
-  }
-#pragma unroll
-  for (int n = 0; n < NT; ++n) all_max[n] = warp_max_f(all_max[n]);
-#pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    all_sum[n] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) all_sum[n] += (lane + 32 * i < E) ? expf(v[n * 8 + i] - all_max[n]) : 0.f;
-  }
-#pragma unroll
-  for (int n = 0; n < NT; ++n) all_sum[n] = warp_sum_f(all_sum[n]);
-  if (allowed != nullptr) {
-#pragma unroll
-    for (int n = 0; n < NT; ++n)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((allowed[e >> 5] >> (e & 31)) & 1u)) v[n * 8 + i] = -INFINITY;
-      }
   }
   float my_v[NT];
   int my_e[NT];
@@ -184,42 +204,44 @@ __device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], cons
     my_e[n] = 0;
   }
   for (int k = 0; k < K; ++k) {
-    float bv[NT];
-    int be[NT];
+    uint32_t lmax[NT], gmax[NT], esel[NT];
+    int li[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      bv[n] = -INFINITY;
-      be[n] = 0x7fffffff;
+      // pairwise tree over the 8 slots; on equal keys the lower slot (= the
+      // lower expert id) wins; key 0 never wins (li stays 8)
+      uint32_t k4[4];
+      int i4[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && (v[n * 8 + i] > bv[n] || (v[n * 8 + i] == bv[n] && e < be[n]))) {
-          bv[n] = v[n * 8 + i];
-          be[n] = e;
-        }
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t a = key[n * 8 + 2 * q], b = key[n * 8 + 2 * q + 1];
+        k4[q] = (b > a) ? b : a;
+        i4[q] = (b > a) ? 2 * q + 1 : 2 * q;
       }
+      const uint32_t k01 = (k4[1] > k4[0]) ? k4[1] : k4[0];
+      const int i01 = (k4[1] > k4[0]) ? i4[1] : i4[0];
+      const uint32_t k23 = (k4[3] > k4[2]) ? k4[3] : k4[2];
+      const int i23 = (k4[3] > k4[2]) ? i4[3] : i4[2];
+      lmax[n] = (k23 > k01) ? k23 : k01;
+      li[n] = (k23 > k01) ? i23 : i01;
+      if (lmax[n] == 0u) li[n] = 8;
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int n = 0; n < NT; ++n) gmax[n] = __reduce_max_sync(0xffffffffu, lmax[n]);
 #pragma unroll
-      for (int n = 0; n < NT; ++n) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv[n], o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be[n], o);
-        if (ov > bv[n] || (ov == bv[n] && oe < be[n])) {
-          bv[n] = ov;
-          be[n] = oe;
-        }
-      }
+    for (int n = 0; n < NT; ++n) {
+      const uint32_t cand = (li[n] < 8 && lmax[n] == gmax[n]) ? static_cast<uint32_t>(lane + 32 * li[n]) : 0xffffffffu;
+      esel[n] = __reduce_min_sync(0xffffffffu, cand);
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-      const bool mine = (be[n] & 31) == lane;
-      const int slot = be[n] >> 5;
+      const bool mine = static_cast<int>(esel[n] & 31u) == lane;
+      const int slot = static_cast<int>(esel[n] >> 5);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[n * 8 + i] = (mine && i == slot) ? -INFINITY : v[n * 8 + i];
+      for (int i = 0; i < 8; ++i) key[n * 8 + i] = (mine && i == slot) ? kNegInf : key[n * 8 + i];
       if (lane == k) {
-        my_v[n] = bv[n];
-        my_e[n] = be[n];
+        my_v[n] = key_value(gmax[n]);
+        my_e[n] = static_cast<int>(esel[n]);
       }
     }
   }
@@ -230,8 +252,26 @@ __device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], cons
     const float sum = warp_sum_f(ex);
     out[n].e = my_e[n];
     out[n].w = ex / sum;
-    out[n].p = (lane < K) ? expf(my_v[n] - all_max[n]) / all_sum[n] : 0.f;
+    out[n].p = (want_p && lane < K) ? expf(my_v[n] - all_max[n]) / all_sum[n] : 0.f;
   }
+}
+
+// As warp_topk_regs, reading token n's logits from the global row rows[n]
+// (written by other CTAs of this launch: loads bypass L1). Tokens with
+// valid[n] false read nothing.
+template <int NT>
+__device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], const bool (&valid)[NT], int E, int K,
+                                            int lane, const uint32_t* allowed, TopkSel (&out)[NT]) {
+  float v[NT * 8];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[n * 8 + i] = (valid[n] && e < E) ? __ldcg(rows[n] + e) : -INFINITY;
+    }
+  }
+  warp_topk_regs<NT>(v, E, K, lane, allowed, true, out);
 }
 
 // Single-token form of warp_topk_n.
