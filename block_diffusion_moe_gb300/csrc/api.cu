@@ -44,7 +44,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr size_t kCtrlBytes = 256;
 enum CtrlWord : int {
   kCtrlErr = 0,          // kernel status bits
-  kCtrlUnitCtr = 1,      // expert kernel work counter (reset by the permutation kernel)
+  kCtrlUnitCtr = 1,      // expert kernel work counter (reset by the kernel before its barrier)
   kCtrlMaskedLeft = 2,   // positions still masked after the last head call
   kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
   kCtrlCommitted = 4,    // positions committed by the last head call
@@ -284,16 +284,6 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   if (d.coreset_top_p > 0.f && !fused)
     return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "the block coreset needs at most %d positions", kLayerMaxTokens);
   cudaError_t e = cudaSuccess;
-  PermArgs pa;
-  memset(&pa, 0, sizeof(pa));
-  pa.tok_slot = reinterpret_cast<int32_t*>(data + L.tok_slot);
-  pa.cnt = reinterpret_cast<int*>(data + L.cnt);
-  pa.off = reinterpret_cast<int*>(data + L.off);
-  pa.act = reinterpret_cast<int*>(data + L.act);
-  pa.n_active = reinterpret_cast<int*>(data + L.n_active);
-  pa.unit_ctr = ctrl + kCtrlUnitCtr;
-  pa.gu_done = reinterpret_cast<int*>(data + L.gu_done);
-  pa.dn_done = reinterpret_cast<int*>(data + L.dn_done);
   if (!fused) {
     RouteArgs ra;
     ra.x = x_in;
@@ -313,17 +303,6 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     e = launch_route(ra, stream, kPdl);
     if (e != cudaSuccess) return cuda_fail(e, "launch route");
 
-    pa.topk_idx = topk_idx;
-    pa.topk_w = topk_w;
-    pa.xg = xg;
-    pa.out_idx = out_idx;
-    pa.out_w = out_w;
-    pa.M = M;
-    pa.H = H;
-    pa.E = E;
-    pa.K = K;
-    e = launch_perm(pa, std::max(1, std::min(MK, plan.sms)), stream, kPdl);
-    if (e != cudaSuccess) return cuda_fail(e, "launch perm");
   }
 
   ExpertArgs xa;
@@ -378,15 +357,21 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.x_out = x_out;
   xa.hbuf = hbuf;
   xa.yslot = reinterpret_cast<float*>(data + L.yslot);
-  xa.n_active = pa.n_active;
-  xa.act = pa.act;
-  xa.cnt = pa.cnt;
-  xa.off = pa.off;
-  xa.tok_slot = pa.tok_slot;
+  xa.n_active = reinterpret_cast<int*>(data + L.n_active);
+  xa.act = reinterpret_cast<int*>(data + L.act);
+  xa.cnt = reinterpret_cast<int*>(data + L.cnt);
+  xa.off = reinterpret_cast<int*>(data + L.off);
+  xa.tok_slot = reinterpret_cast<int32_t*>(data + L.tok_slot);
   xa.topk_w = topk_w;
-  xa.unit_ctr = pa.unit_ctr;
-  xa.gu_done = pa.gu_done;
-  xa.dn_done = pa.dn_done;
+  xa.topk_idx = topk_idx;
+  xa.xg = xg;
+  xa.xn = xg + static_cast<size_t>(MK) * H;  // the normed rows (also the shared expert's rows)
+  xa.bar_count = reinterpret_cast<unsigned long long*>(ctrl + kCtrlBarCount);
+  xa.out_idx = out_idx;
+  xa.out_w = out_w;
+  xa.unit_ctr = ctrl + kCtrlUnitCtr;
+  xa.gu_done = reinterpret_cast<int*>(data + L.gu_done);
+  xa.dn_done = reinterpret_cast<int*>(data + L.dn_done);
   xa.err = err;
   xa.M = M;
   xa.H = H;
@@ -424,6 +409,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     sa = used < budget ? static_cast<int>(std::min<size_t>(16, (budget - used) / a_stage)) : 0;
   }
   if (sa < 1 || sb < 1) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "expert pipeline does not fit in shared memory");
+  // The standalone kernel builds its permutation in the weight ring.
+  if (!fused && static_cast<size_t>(sa) * a_stage < perm_smem_bytes(M, K, E))
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "the permutation tables do not fit in the expert kernel's weight ring");
   const int smem_a = sa;
   xa.smem_a = smem_a;
   xa.stages_a = sa;
@@ -440,16 +428,13 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     xa.wr_next = reinterpret_cast<const bf16*>(next_router);
     xa.bias = layer.router_bias;
     xa.logits = reinterpret_cast<float*>(data + L.logits);
-    xa.xn = xg + static_cast<size_t>(MK) * H;
-    xa.bar_count = reinterpret_cast<unsigned long long*>(ctrl + kCtrlBarCount);
+
     xa.pub_idx = topk_idx;
     xa.pub_w = topk_w;
     xa.pub_p = reinterpret_cast<float*>(data + L.topk_p);
     xa.pub2_idx = reinterpret_cast<int32_t*>(data + L.rr_idx);
     xa.pub2_w = reinterpret_cast<float*>(data + L.rr_w);
     xa.coreset_top_p = d.coreset_top_p;
-    xa.out_idx = out_idx;
-    xa.out_w = out_w;
     xa.eps = d.rms_eps;
     xa.stamps = reinterpret_cast<unsigned long long*>(ctrl + kCtrlStamps);
     smem += layer_rt_bytes(M, K, E);

@@ -836,26 +836,6 @@ __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s,
 
 }  // namespace
 
-template <bool kQ4>
-__global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
-    k_expert(const __grid_constant__ ExpertArgs p) {
-  extern __shared__ uint8_t smem_raw[];
-  const Smem s = carve(smem_raw, p);
-  const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
-  pdl_wait();
-  pdl_trigger();
-  Rt rt;
-  rt.act = p.act;
-  rt.cnt = p.cnt;
-  rt.off = p.off;
-  rt.mask = nullptr;
-  rt.tok_slot = p.tok_slot;
-  rt.topk_w = p.topk_w;
-  rt.n_exp = *p.n_active + 1;
-  rt.dense = 0;
-  expert_roles<kQ4>(p, s, rt, tmem_base);
-}
-
 namespace {
 
 // Grid-wide barrier for a persistent launch (every CTA is resident: one per
@@ -893,6 +873,95 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 }
 
 }  // namespace
+
+template <bool kQ4>
+__global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
+    k_expert(const __grid_constant__ ExpertArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem s = carve(smem_raw, p);
+  const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
+  pdl_wait();
+  pdl_trigger();
+  const int M = p.M, K = p.K, E = p.E, MK = M * K;
+  // Every CTA builds the same permutation of the routing kernel's top-k in
+  // the (still idle) weight ring; CTA 0 publishes the unit tables; every
+  // CTA gathers its share of the normed rows into expert order; one grid
+  // barrier, then the units.
+  PermTables pt;
+  pt.idx = reinterpret_cast<int*>(s.a_ring);
+  pt.row_tok = pt.idx + MK;
+  pt.bm = reinterpret_cast<uint32_t*>(pt.row_tok + MK);
+  pt.off = reinterpret_cast<int*>(pt.bm + E * (kMaxTokens / 32));
+  pt.cnt = pt.off + E;
+  pt.tmp = pt.cnt + E;
+  const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
+  const int tid = threadIdx.x;
+  if (blockIdx.x == 0) {
+    if (tid < E) {
+      const int c = pt.cnt[tid];
+      p.cnt[tid] = c;
+      p.off[tid] = pt.off[tid];
+      if (c > 0) {
+        // Active experts heaviest first (ties: lower id first), so that the
+        // longest units are handed out first and do not end the launch.
+        int rank = 0;
+        for (int j = 0; j < E; ++j) {
+          const int cj = pt.cnt[j];
+          rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
+        }
+        p.act[rank] = tid;
+      }
+    }
+    if (tid == 0) {
+      *p.n_active = n_act;
+      *p.unit_ctr = 0;
+    }
+    for (int i = tid; i <= E; i += blockDim.x) p.gu_done[i] = 0;
+    for (int i = tid; i < (p.H >> 7); i += blockDim.x) p.dn_done[i] = 0;
+    if (p.out_idx)
+      for (int i = tid; i < MK; i += blockDim.x) p.out_idx[i] = pt.idx[i];
+    if (p.out_w)
+      for (int i = tid; i < MK; i += blockDim.x) p.out_w[i] = p.topk_w[i];
+  }
+  {  // gather: four consecutive rows per CTA pass, every thread's loads before its stores
+    const int per_row = p.H / 8;  // 16-byte pieces per row
+    const int span = 4 * per_row;
+    const int nt = blockDim.x;
+    for (int base = blockIdx.x * 4; base < MK; base += gridDim.x * 4) {
+      for (int i0 = tid; i0 < span; i0 += nt * 4) {
+        uint4 v[4];
+        int dst[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * nt;
+          const int r = base + i / per_row;
+          dst[j] = -1;
+          if (i < span && r < MK) {
+            const int c = i - (i / per_row) * per_row;
+            v[j] = __ldcg(reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(pt.row_tok[r]) * p.H) + c);
+            dst[j] = r * per_row + c;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (dst[j] >= 0) reinterpret_cast<uint4*>(p.xg)[dst[j]] = v[j];
+      }
+    }
+  }
+  fence_proxy_async_shared();  // the ring was used generically; TMA refills it
+  const bool ok = grid_barrier(p.bar_count, p.err);
+  Rt rt;
+  rt.act = p.act;
+  rt.cnt = p.cnt;
+  rt.off = p.off;
+  rt.mask = nullptr;
+  rt.tok_slot = p.tok_slot;
+  rt.topk_w = p.topk_w;
+  rt.n_exp = ok ? __ldcg(p.n_active) + 1 : 0;  // after a failed barrier no unit runs
+  rt.dense = 0;
+  expert_roles<kQ4>(p, s, rt, tmem_base);
+}
+
 
 // One MoE sublayer for M <= 32 tokens in one launch: routing, experts and
 // combine (see the file comment).
@@ -1190,6 +1259,10 @@ size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int
 // idx, w, slot, coreset probability [M*K] each; mask, count, offset, active,
 // coreset mass, sorted mass, sorted id [E] each; the active count and the
 // coreset's allowed-set words.
+size_t perm_smem_bytes(int M, int K, int E) {
+  return static_cast<size_t>(2 * M * K + E * (kMaxTokens / 32) + 2 * E + 17) * 4;
+}
+
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }
 
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {

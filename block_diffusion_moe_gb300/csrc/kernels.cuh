@@ -72,22 +72,6 @@ struct RouteArgs {
   float eps;
 };
 
-struct PermArgs {
-  const int32_t* topk_idx;  // [M][K]
-  const float* topk_w;      // [M][K]
-  int32_t* tok_slot;        // [M][K] -> row of the gathered buffer
-  int* cnt;                 // [E]
-  int* off;                 // [E]
-  int* act;                 // [E] active expert ids, heaviest first (ties: lower id)
-  int* n_active;            // scalar
-  int* unit_ctr;            // scalar, reset to 0
-  int* gu_done;             // [E+1], reset to 0
-  int* dn_done;             // [H/128], reset to 0
-  bf16* xg;                 // [M*K + M][H] gathered normed inputs
-  int32_t* out_idx;         // optional copies for the caller
-  float* out_w;
-  int M, H, E, K;
-};
 
 struct CombineArgs {
   const float* x_in;        // [M][H]
@@ -128,12 +112,14 @@ struct ExpertArgs {
   float* x_out;
   bf16* hbuf;          // [M*K+M][F]
   float* yslot;        // [M*K+M][H]
-  const int* n_active;
-  const int* act;
-  const int* cnt;
-  const int* off;
-  const int32_t* tok_slot;
+  int* n_active;
+  int* act;
+  int* cnt;
+  int* off;
+  int32_t* tok_slot;
   const float* topk_w;
+  const int32_t* topk_idx;  // standalone kernel: [M][K] selections to permute
+  bf16* xg;                 // standalone kernel: gathered rows [M*K][H] (normed rows follow at xn)
   int* unit_ctr;
   int* gu_done;
   int* dn_done;
@@ -209,12 +195,13 @@ cudaError_t launch_quantize_q4(const QuantArgs& a, cudaStream_t s);
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
-cudaError_t launch_perm(const PermArgs& a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 // (both launch the low-bit form when a.q4 != 0)
 size_t layer_rt_bytes(int M, int K, int E);
+// Shared memory the standalone expert kernel's permutation needs (in its weight ring).
+size_t perm_smem_bytes(int M, int K, int E);
 // Largest token count the fused layer kernel takes (one 32-bit mask per expert).
 constexpr int kLayerMaxTokens = 32;
 // Launches the unmask or the accept form of the head kernel.

@@ -1,5 +1,5 @@
-// Input assembly, RMSNorm, router with softmax top-k, and the token->expert
-// permutation with the gather of normed inputs.
+// Input assembly, RMSNorm, router with softmax top-k, and the parallel
+// combine of the standalone path.
 //
 // Follows "Clover-35B-A3B: how a diffusion model gets to 680 tokens a second,
 // read from its files": section "What Clover is" (256 routed experts, each
@@ -283,151 +283,6 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
   if (tid == 0) a.tg_ctr[blockIdx.y] = 0;
 }
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
-__device__ __forceinline__ int block_excl_scan_256(int v, int* s_tmp /*[8]*/, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) s_tmp[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int wv = lane < 8 ? s_tmp[lane] : 0;
-    int wi = wv;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    if (lane < 8) s_tmp[lane] = wi - wv;  // exclusive warp offsets
-    if (lane == 7) s_tmp[8] = wi;         // total
-  }
-  __syncthreads();
-  const int res = s_tmp[warp] + incl - v;
-  *total = s_tmp[8];
-  __syncthreads();
-  return res;
-}
-
-// ------------------------------------------------------------------- perm
-// Every CTA rebuilds the same token->expert permutation from the top-k ids
-// (cheap, and it avoids a grid-wide barrier): per-expert token bitmasks, a
-// scan over experts for the row offsets, and each (token, slot)'s row =
-// offset of its expert + number of lower tokens routed to that expert. Rows
-// of one expert are therefore in token order. CTA 0 publishes the metadata
-// and resets the expert kernel's counters; all CTAs gather rows of the
-// normed input into expert-grouped order.
-__global__ void __launch_bounds__(256) k_perm(PermArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  int* s_idx = reinterpret_cast<int*>(smem);  // [M*K]
-  int* s_row_tok = s_idx + a.M * a.K;         // [M*K]
-  __shared__ uint32_t s_bm[kMaxExperts][kMaxTokens / 32];
-  __shared__ int s_off[kMaxExperts];
-  __shared__ int s_cnt[kMaxExperts];
-  __shared__ int s_tmp[9];
-  const int tid = threadIdx.x;
-  const int MK = a.M * a.K;
-  const int nw = (a.M + 31) >> 5;
-
-  pdl_wait();
-  pdl_trigger();
-  for (int i = tid; i < MK; i += blockDim.x) {
-    const int e = a.topk_idx[i];
-    s_idx[i] = e < 0 ? 0 : (e >= a.E ? a.E - 1 : e);  // ids come from k_route; clamp keeps smem indexing safe
-  }
-  for (int i = tid; i < kMaxExperts * (kMaxTokens / 32); i += blockDim.x) (&s_bm[0][0])[i] = 0u;
-  __syncthreads();
-  // Word wd of every expert's token mask (tokens 32wd..32wd+31) is written
-  // by warp wd alone: per selection slot, the lanes that chose the same
-  // expert merge their bits and the lowest of them stores the word.
-  {
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int wd = warp; wd < nw; wd += blockDim.x >> 5) {
-      const int t = wd * 32 + lane;
-      for (int k = 0; k < a.K; ++k) {
-        const int e = t < a.M ? s_idx[t * a.K + k] : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) s_bm[e][wd] |= peers;
-        __syncwarp();
-      }
-    }
-  }
-  __syncthreads();
-  int c = 0;
-  if (tid < a.E)
-    for (int wd = 0; wd < nw; ++wd) c += __popc(s_bm[tid][wd]);
-  int total = 0;
-  const int off = block_excl_scan_256(c, s_tmp, &total);
-  const int n_act = __syncthreads_count(tid < a.E && c > 0);
-  if (tid < a.E) s_off[tid] = off;
-  s_cnt[tid] = tid < a.E ? c : 0;
-  __syncthreads();
-  for (int i = tid; i < MK; i += blockDim.x) {
-    const int e = s_idx[i], t = i / a.K;
-    const int wd = t >> 5, bit = t & 31;
-    int pre = __popc(s_bm[e][wd] & ((1u << bit) - 1u));
-    for (int j = 0; j < wd; ++j) pre += __popc(s_bm[e][j]);
-    const int row = s_off[e] + pre;
-    s_row_tok[row] = t;
-    if (blockIdx.x == 0) a.tok_slot[i] = row;
-  }
-  if (blockIdx.x == 0) {
-    if (tid < a.E) {
-      a.cnt[tid] = c;
-      a.off[tid] = off;
-      if (c > 0) {
-        // Active experts heaviest first (ties: lower id first), so that the
-        // longest units are handed out first and do not end the launch.
-        int rank = 0;
-        for (int j = 0; j < a.E; ++j) {
-          const int cj = s_cnt[j];
-          rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
-        }
-        a.act[rank] = tid;
-      }
-    }
-    if (tid == 0) {
-      *a.n_active = n_act;
-      *a.unit_ctr = 0;
-    }
-    for (int i = tid; i <= a.E; i += blockDim.x) a.gu_done[i] = 0;
-    for (int i = tid; i < a.H / 128; i += blockDim.x) a.dn_done[i] = 0;
-    if (a.out_idx)
-      for (int i = tid; i < MK; i += blockDim.x) a.out_idx[i] = s_idx[i];
-    if (a.out_w)
-      for (int i = tid; i < MK; i += blockDim.x) a.out_w[i] = a.topk_w[i];
-  }
-  __syncthreads();
-  const size_t H = a.H;
-  // Four consecutive rows per CTA pass, every thread's loads issued before
-  // its stores.
-  const int per_row = static_cast<int>(H / 8);
-  for (int base = blockIdx.x * 4; base < MK; base += gridDim.x * 4) {
-    const int span = 4 * per_row;
-    for (int i0 = tid; i0 < span; i0 += blockDim.x * 4) {
-      uint4 v[4];
-      int dst_i[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = i0 + j * blockDim.x;
-        const int r = base + i / per_row;
-        dst_i[j] = -1;
-        if (i < span && r < MK) {
-          const int c = i - (i / per_row) * per_row;
-          v[j] = reinterpret_cast<const uint4*>(a.xg + static_cast<size_t>(MK + s_row_tok[r]) * H)[c];
-          dst_i[j] = r * per_row + c;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (dst_i[j] >= 0) reinterpret_cast<uint4*>(a.xg)[dst_i[j]] = v[j];
-    }
-  }
-}
-
 // ---------------------------------------------------------------- combine
 // x_out = x_in + (sum_k w_tk y_{slot(t,k)}) + y_shared(t), one float4 of
 // outputs per thread; the sum runs in selection order, then the shared row,
@@ -509,11 +364,5 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl) {
   return launch_kernel(k_route, grid, dim3(256), smem, s, pdl, a);
 }
 
-cudaError_t launch_perm(const PermArgs& a, int grid, cudaStream_t s, bool pdl) {
-  const size_t smem = static_cast<size_t>(2) * a.M * a.K * sizeof(int);
-  cudaError_t e = cudaFuncSetAttribute(k_perm, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  return launch_kernel(k_perm, dim3(grid), dim3(256), smem, s, pdl, a);
-}
 
 }  // namespace clover

@@ -297,4 +297,97 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Block-wide exclusive scan of one int per thread (blockDim.x a multiple of
+// 32, at most 512). Returns the exclusive prefix; *total receives the sum.
+// s_tmp holds 17 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* s_tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = static_cast<int>(blockDim.x >> 5);
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_tmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int wv = lane < nw ? s_tmp[lane] : 0;
+    int wi = wv;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) s_tmp[lane] = wi - wv;  // exclusive warp offsets
+    if (lane == nw - 1) s_tmp[16] = wi;    // total
+  }
+  __syncthreads();
+  const int res = s_tmp[warp] + incl - v;
+  *total = s_tmp[16];
+  __syncthreads();
+  return res;
+}
+
+// Shared-memory tables of one CTA's token -> expert permutation.
+struct PermTables {
+  int* idx;       // [M*K] selections (clamped expert ids)
+  int* row_tok;   // [M*K] token of each gathered row
+  uint32_t* bm;   // [E][kMaxTokens / 32] token bitmask per expert
+  int* off;       // [E] first row of each expert
+  int* cnt;       // [E] tokens per expert
+  int* tmp;       // [17] scan scratch
+};
+
+// Builds, with every thread of the CTA (blockDim.x >= E), the permutation of
+// the M*K top-k selections: per-expert token bitmasks (word wd of an expert
+// written by warp wd alone: the lanes that chose the same expert in one
+// selection slot merge their bits), a scan over experts for the row offsets,
+// and each selection's row = its expert's offset + the number of lower
+// tokens routed to that expert, so rows of one expert are in token order.
+// Returns the number of active experts; `slot_out` (nullable) receives each
+// selection's row.
+__device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, int K, int E, const PermTables& t, int32_t* slot_out) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int MK = M * K, nw = (M + 31) >> 5;
+  constexpr int kW = kMaxTokens / 32;
+  for (int i = tid; i < MK; i += blockDim.x) {
+    const int e = __ldcg(topk_idx + i);
+    t.idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);  // ids come from another kernel; clamping keeps indexing safe
+  }
+  for (int i = tid; i < E * kW; i += blockDim.x) t.bm[i] = 0u;
+  __syncthreads();
+  for (int wd = warp; wd < nw; wd += blockDim.x >> 5) {
+    const int tk = wd * 32 + lane;
+    for (int k = 0; k < K; ++k) {
+      const int e = tk < M ? t.idx[tk * K + k] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) t.bm[e * kW + wd] |= peers;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  int c = 0;
+  if (tid < E)
+    for (int wd = 0; wd < nw; ++wd) c += __popc(t.bm[tid * kW + wd]);
+  int total = 0;
+  const int off = block_excl_scan(c, t.tmp, &total);
+  const int n_act = __syncthreads_count(tid < E && c > 0);
+  if (tid < E) {
+    t.off[tid] = off;
+    t.cnt[tid] = c;
+  }
+  __syncthreads();
+  for (int i = tid; i < MK; i += blockDim.x) {
+    const int e = t.idx[i], tk = i / K;
+    const int wd = tk >> 5, bit = tk & 31;
+    int pre = __popc(t.bm[e * kW + wd] & ((1u << bit) - 1u));
+    for (int j = 0; j < wd; ++j) pre += __popc(t.bm[e * kW + j]);
+    const int row = t.off[e] + pre;
+    t.row_tok[row] = tk;
+    if (slot_out != nullptr) slot_out[i] = row;
+  }
+  __syncthreads();
+  return n_act;
+}
+
 }  // namespace clover

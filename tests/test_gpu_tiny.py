@@ -236,3 +236,37 @@ def test_bad_token_id_is_clamped_and_reported():
         clover.workspace_status(ws)
     assert ei.value.code == clover.ERR_DEVICE_TIMEOUT and "token id" in str(ei.value)
     clover.workspace_status(ws)    # the status word was cleared
+
+
+@pytest.mark.parametrize("M", [8, 40])
+def test_router_exact_ties_take_the_lower_expert_id(M):
+    """Experts 2 and 5 (and 9 and 12) get identical router rows, scaled up so
+    that the pair wins wherever its dot product is positive: their logits tie
+    exactly and the rule takes the lower expert id first, with equal weights.
+    Both routing paths: the fused kernel (8 tokens) and the standalone router
+    (40 tokens)."""
+    d = synth.TINY
+    layer = synth.make_layer(d, 21, 0, DEV)
+    w = layer.router_w
+    w[2] = w[2] * 8.0
+    w[5] = w[2]
+    w[9] = w[9] * 8.0
+    w[12] = w[9]
+    x = synth.make_x(d, M, 22, DEV)
+    x_out, idx, wt = clover.moe_block_step(d, layer, x)
+    torch.cuda.synchronize()
+    ref = O.moe_layer(x.cpu().numpy(), layer_to_oracle(layer), d.top_k, d.rms_eps)
+    idx_g, w_g = idx.cpu().numpy(), wt.cpu().numpy()
+    pairs = [(2, 5), (9, 12)]
+    hits = 0
+    for t in range(M):
+        sel = tuple(int(e) for e in ref["idx"][t])
+        if sel in pairs:  # the oracle picked a tied pair: order and weights are fixed
+            assert tuple(int(e) for e in idx_g[t]) == sel, (t, idx_g[t], sel)
+            assert np.allclose(w_g[t], [0.5, 0.5], atol=1e-6), (t, w_g[t])
+            hits += 1
+        ps = np.sort(ref["p"][t])[::-1]
+        if ps[d.top_k - 1] == ps[d.top_k]:  # a planted tie at the cut: the lower id is kept
+            assert set(idx_g[t].tolist()) == set(sel), (t, idx_g[t], sel)
+    assert hits >= M // 4, hits  # the planted ties decide a good share of the tokens
+    compare_routing(idx_g, w_g, ref, d.top_k)
