@@ -395,12 +395,22 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   int sa, sb, sq = 0;
   if (q4) {
     // The staging ring carries the HBM stream (4 KiB of codes per K group,
-    // 4x the weights per byte); a few bf16 stages feed the MMA.
-    sa = kg == 2 ? 2 : 4;
+    // 4x the weights per byte); four bf16 stages (two slots' worth at two K
+    // groups per stage, one per converter team) feed the MMA.
+    sa = 4;
     sb = 3;
     const size_t used = static_cast<size_t>(sa) * a_stage + static_cast<size_t>(sb) * b_stage;
     sq = used < budget ? static_cast<int>(std::min<size_t>(24, (budget - used) / (kQSlotBytes + 16))) : 0;
     if (sq < 1) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "no shared memory left for the low-bit staging ring");
+    // Two converter teams take slots in turn when each can own its slots
+    // (an even slot count) and its bf16 stages (a multiple of twice the
+    // stages one slot fills, the same for both unit kinds).
+    const int per_slot_gu = xa.kq_gu / kg_gu, per_slot_dn = xa.kq_dn / kg_dn;
+    xa.q_teams = 1;
+    if (per_slot_gu == per_slot_dn && sa % (2 * per_slot_gu) == 0 && sq >= 2) {
+      sq &= ~1;
+      xa.q_teams = 2;
+    }
   } else if (nb <= 64) {
     sa = sb = static_cast<int>(std::min<size_t>(16, budget / (a_stage + b_stage)));
   } else {

@@ -142,6 +142,7 @@ struct Smem {
   volatile int* s_last;
   volatile int* s_unit;
   volatile int* s_ok;
+  volatile int* cvt_unit;  // converter teams' unit ids, double-buffered by iteration
   uint8_t* rt_region;  // k_layer's routing tables
   uint32_t a_stage_bytes;  // kg_stage A tiles of 16 KiB
   uint32_t b_stage_bytes;  // kg_stage B tiles of nb_max x 128 bytes
@@ -177,6 +178,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   s.s_last = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
   s.s_unit = s.s_last + 1;
   s.s_ok = s.s_last + 2;
+  s.cvt_unit = reinterpret_cast<volatile int*>(s.tmem_slot + 8);  // [2 teams][2] (bytes 32-47)
   s.rt_region = reinterpret_cast<uint8_t*>(s.tmem_slot) + 128;
   return s;
 }
@@ -312,70 +314,95 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
 // multiply by the scale gives bf16((u - 8) s). The row is written in the
 // 128-byte swizzle the TMA would have used, so the MMA is unchanged.
 __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
-  const int r = threadIdx.x - 8 * 32;  // 0..127
+  // With p.q_teams == 2 two teams of four warps take the staging slots in
+  // turn (team t: slots t, t + 2, ...). The host enables this only when the
+  // slot count is even and the bf16 stage count a multiple of twice the
+  // stages per slot, so each team owns its own slots and stages and never
+  // runs more than one ring round ahead of their consumer (a parity wait
+  // cannot tell two rounds apart). With one team, team 1 only takes part in
+  // the unit handshake. Both teams walk every unit and slot to keep the ring
+  // counters. Control flow stays uniform across a team: the unit id comes
+  // from the team leader through shared memory, and a failed wait only
+  // skips work, so no thread is left at a team barrier.
+  const int team = (threadIdx.x - 8 * 32) >> 7;  // 0 or 1
+  const int r = (threadIdx.x - 8 * 32) & 127;    // tile row
   const int lane = threadIdx.x & 31;
   const int SA = p.stages_a, SQ = p.stages_q;
   int sa = 0, sq = 0;
   uint32_t pha = 0, phq = 0;
+  uint32_t gslot = 0;  // slots of all units so far
   const __nv_bfloat162 k136 = __floats2bfloat162_rn(136.f, 136.f);
   for (int it = 0;; ++it) {
     const int us = it & (kExpertUnitRing - 1);
     const uint32_t upar = (it / kExpertUnitRing) & 1;
-    const bool got = mbar_wait(&s.ufull[us], upar, s.abort);
-    const int u = got ? s.unit_ids[us] : kUnitAbort;
-    named_bar_sync(2, 128);  // every converter thread has read the slot
+    volatile int* bcast = s.cvt_unit + team * 2 + (it & 1);
     if (r == 0) {
+      const bool got = mbar_wait(&s.ufull[us], upar, s.abort);
+      *bcast = got ? s.unit_ids[us] : kUnitAbort;
       if (got) mbar_arrive(&s.uempty[us]);
       else raise_abort(s, p.err, kErrMbarTimeout);
     }
+    named_bar_sync(2 + team, 128);  // the unit id is published to the team
+    const int u = *bcast;
     if (u < 0) break;
     const Unit w = decode_unit(u, rt, p);
     const int nk = (w.kind == 0) ? (p.H >> 6) : (p.F >> 6);
     const int kq = unit_kq(w, p);
     const int kg = unit_kg(w, p);  // kq is a multiple of kg
-    bool ok = true;
-    for (int kc0 = 0; kc0 < nk && ok; kc0 += kq) {
-      if (!mbar_wait(&s.full_q[sq], phq, s.abort)) {
-        raise_abort(s, p.err, kErrMbarTimeout);
-        ok = false;
-        break;
+    for (int kc0 = 0; kc0 < nk; kc0 += kq, ++gslot) {
+      const bool mine = (p.q_teams == 2) ? ((gslot & 1u) == static_cast<uint32_t>(team)) : (team == 0);
+      if (!mine) {  // another team's slot: step the counters
+        for (int st = 0; st < kq / kg; ++st) {
+          if (++sa == SA) {
+            sa = 0;
+            pha ^= 1u;
+          }
+        }
+        if (++sq == SQ) {
+          sq = 0;
+          phq ^= 1u;
+        }
+        continue;
       }
+      bool ok = mbar_wait(&s.full_q[sq], phq, s.abort);
+      if (!ok) raise_abort(s, p.err, kErrMbarTimeout);
       const uint8_t* slot = s.q_ring + static_cast<size_t>(sq) * kQSlotBytes;
       for (int g = 0; g < kq; ++g) {
         const int h = g % kg;  // half of the A stage this group fills
-        if (h == 0 && !mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
+        if (h == 0 && ok && !mbar_wait(&s.empty_a[sa], pha ^ 1u, s.abort)) {
           raise_abort(s, p.err, kErrMbarTimeout);
           ok = false;
-          break;
         }
-        // 128-byte code rows (kq = 4) arrive in the 128-byte swizzle
-        const uint8_t* src = slot + r * kq * 32;
-        const int ch0 = (kq == 4) ? ((2 * g) ^ (r & 7)) : 2 * g;
-        const int ch1 = (kq == 4) ? ((2 * g + 1) ^ (r & 7)) : 2 * g + 1;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(src + ch0 * 16);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(src + ch1 * 16);
-        const unsigned short sb = *reinterpret_cast<const unsigned short*>(slot + kq * 4096 + g * 256 + 2 * r);
-        const __nv_bfloat162 sc = __halves2bfloat162(__ushort_as_bfloat16(sb), __ushort_as_bfloat16(sb));
-        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t o[32];  // word 4j + i holds elements 8j + 2i (low half) and 8j + 2i + 1
+        if (ok) {
+          // 128-byte code rows (kq = 4) arrive in the 128-byte swizzle
+          const uint8_t* src = slot + r * kq * 32;
+          const int ch0 = (kq == 4) ? ((2 * g) ^ (r & 7)) : 2 * g;
+          const int ch1 = (kq == 4) ? ((2 * g + 1) ^ (r & 7)) : 2 * g + 1;
+          const uint4 c0 = *reinterpret_cast<const uint4*>(src + ch0 * 16);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(src + ch1 * 16);
+          const unsigned short sb = *reinterpret_cast<const unsigned short*>(slot + kq * 4096 + g * 256 + 2 * r);
+          const __nv_bfloat162 sc = __halves2bfloat162(__ushort_as_bfloat16(sb), __ushort_as_bfloat16(sb));
+          const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t o[32];  // word 4j + i holds elements 8j + 2i (low half) and 8j + 2i + 1
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 8; ++j) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t x = ((words[j] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-            const __nv_bfloat162 v = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&x), k136), sc);
-            o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t x = ((words[j] >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+              const __nv_bfloat162 v = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162*>(&x), k136), sc);
+              o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
+            }
           }
-        }
-        uint8_t* row = s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes + r * 128;
+          uint8_t* row = s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes + r * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) =
-              make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
         if (h == kg - 1) {
           fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
           __syncwarp();
-          if (lane == 0) mbar_arrive(&s.full_a[sa]);
+          if (lane == 0 && ok) mbar_arrive(&s.full_a[sa]);
           if (++sa == SA) {
             sa = 0;
             pha ^= 1u;
@@ -385,13 +412,12 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       // this thread's reads of the slot are done (the fence above ordered
       // them before any later copy into it)
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty_q[sq]);
+      if (lane == 0 && ok) mbar_arrive(&s.empty_q[sq]);
       if (++sq == SQ) {
         sq = 0;
         phq ^= 1u;
       }
     }
-    if (!ok) break;
   }
 }
 
@@ -782,7 +808,7 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
     }
     for (int i = 0; i < kExpertUnitRing; ++i) {
       mbar_init(&s.ufull[i], 1);
-      mbar_init(&s.uempty[i], kQ4 ? 4 : 3);  // B loader, MMA issuer, epilogue leader (+ converter leader)
+      mbar_init(&s.uempty[i], kQ4 ? 5 : 3);  // B loader, MMA issuer, epilogue leader (+ two converter team leaders)
     }
     mbar_init(s.drain, 1);
     *s.abort = 0u;

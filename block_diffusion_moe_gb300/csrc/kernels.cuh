@@ -26,8 +26,9 @@ constexpr int kMaxTopK = 32;
 // Expert kernel: 8 warps (A loads, MMA, B loads, 4 epilogue warps, and one
 // more that only takes part in the fused kernel's routing phase).
 constexpr int kExpertThreads = 256;
-// With low-bit expert weights four more warps expand the 4-bit codes.
-constexpr int kExpertThreadsQ4 = 384;
+// With low-bit expert weights eight more warps (two teams of four) expand
+// the 4-bit codes.
+constexpr int kExpertThreadsQ4 = 512;
 constexpr int kExpertUnitRing = 4;
 // Head kernel: 6 warps (loads, MMA, 4 epilogue warps).
 constexpr int kHeadThreads = 192;
@@ -103,6 +104,7 @@ struct ExpertArgs {
   const uint16_t* dn_s;   // [E][F/64][H]
   const uint16_t* sdn_s;  // [F/64][H]
   int q4, stages_q;
+  int q_teams;  // converter teams (1 or 2; 2 only when every team owns its stages and slots)
   int kq_gu, kq_dn;  // K groups per staging slot for gate/up and down units (1, 2 or 4)
   int smem_a;  // A stages in shared memory (= stages_a)
   // K groups of 64 per A/B stage (1 or 2) for gate/up and down units; a
