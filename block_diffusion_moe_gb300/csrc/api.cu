@@ -380,9 +380,12 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.K = K;
   const int nb = (M + 15) & ~15;
   // Two K groups per A/B stage (8 MMAs per pipeline step instead of 4) when
-  // the token tile is small; 256-token tiles keep one group per stage.
-  const int kg_gu = (nb <= 64 && (H / 64) % 2 == 0) ? 2 : 1;
-  const int kg_dn = (nb <= 64 && (F / 64) % 2 == 0) ? 2 : 1;
+  // the token tile is small; 256-token tiles keep one group per stage. The
+  // low-bit path, whose A stages are written by the converter warps rather
+  // than streamed, takes four (a whole staging slot, 16 MMAs per commit).
+  const bool g4 = q4 && nb <= 64 && (H / 64) % 4 == 0 && (F / 64) % 4 == 0 && xa.kq_gu == 4 && xa.kq_dn == 4;
+  const int kg_gu = g4 ? 4 : ((nb <= 64 && (H / 64) % 2 == 0) ? 2 : 1);
+  const int kg_dn = g4 ? 4 : ((nb <= 64 && (F / 64) % 2 == 0) ? 2 : 1);
   const int kg = std::max(kg_gu, kg_dn);
   xa.kg_gu = kg_gu;
   xa.kg_dn = kg_dn;
@@ -395,10 +398,10 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   int sa, sb, sq = 0;
   if (q4) {
     // The staging ring carries the HBM stream (4 KiB of codes per K group,
-    // 4x the weights per byte); four bf16 stages (two slots' worth at two K
-    // groups per stage, one per converter team) feed the MMA.
-    sa = 4;
-    sb = 3;
+    // 4x the weights per byte); the bf16 stages hold two slots' worth (one
+    // per converter team).
+    sa = kg == 4 ? 2 : 4;
+    sb = kg == 4 ? 2 : 3;
     const size_t used = static_cast<size_t>(sa) * a_stage + static_cast<size_t>(sb) * b_stage;
     sq = used < budget ? static_cast<int>(std::min<size_t>(24, (budget - used) / (kQSlotBytes + 16))) : 0;
     if (sq < 1) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "no shared memory left for the low-bit staging ring");

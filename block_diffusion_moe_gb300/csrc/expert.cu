@@ -117,7 +117,7 @@ __device__ __forceinline__ int unit_kq(const Unit& w, const ExpertArgs& p) {
   return p.q4 ? (w.kind == 0 ? p.kq_gu : p.kq_dn) : 1;
 }
 
-// K groups per A/B stage of a unit (1 or 2).
+// K groups per A/B stage of a unit (1, 2 or 4).
 __device__ __forceinline__ int unit_kg(const Unit& w, const ExpertArgs& p) { return w.kind == 0 ? p.kg_gu : p.kg_dn; }
 
 // Granularity of a unit's K walk: a low-bit slot (kq groups, a multiple of

@@ -107,8 +107,9 @@ struct ExpertArgs {
   int q_teams;  // converter teams (1 or 2; 2 only when every team owns its stages and slots)
   int kq_gu, kq_dn;  // K groups per staging slot for gate/up and down units (1, 2 or 4)
   int smem_a;  // A stages in shared memory (= stages_a)
-  // K groups of 64 per A/B stage (1 or 2) for gate/up and down units; a
-  // stage holds kg_stage groups of room (half h of a stage: group h).
+  // K groups of 64 per A/B stage (1, 2, or 4 on the low-bit path) for
+  // gate/up and down units; a stage holds kg_stage groups of room (part h
+  // of a stage: group h).
   int kg_gu, kg_dn, kg_stage;
   const float* x_in;
   float* x_out;
