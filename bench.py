@@ -258,6 +258,8 @@ WORKLOADS = {
             "bf16 scale per 64 weights: 1,671,168 B per expert instead of 6,291,456 B)",
     "zipf_layer": "one Clover-shaped MoE layer on 8 blocks x 32 positions (256 tokens), router biased to Zipf(1.2) "
                   "expert popularity (the standalone routing and expert kernels)",
+    "int4_layer": "one Clover-shaped MoE layer on a 32-position block with every expert's weights in the 4-bit "
+                  "format (the size ncu captures of the low-bit kernel use)",
 }
 CORESET_TOP_P = 0.9
 
@@ -273,17 +275,18 @@ def run_ours(args):
     kind = args.workload
     n_pos = 256 if kind in ("zipf", "zipf_layer") else M
     n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "int4": D.n_layers, "layer": 1,
-                "zipf_layer": 1,
+                "zipf_layer": 1, "int4_layer": 1,
                 "head": 0, "accept": 0}[kind]
     head_like = kind in ("head", "accept")
     if kind == "accept":
         n_pos = M + 1
-    one_layer = kind in ("layer", "zipf_layer")
+    one_layer = kind in ("layer", "zipf_layer", "int4_layer")
+    q4 = kind in ("int4", "int4_layer")
     full = kind in ("step", "zipf", "coreset", "int4")
     top_p = CORESET_TOP_P if kind == "coreset" else 0.0
     zipf = 1.2 if kind in ("zipf", "zipf_layer") else None
     layers = [synth.make_layer(D, seed, l, dev, zipf_s=zipf) for l in range(n_layers)]
-    if kind == "int4":
+    if q4:
         # the library's own quantizer; the bf16 expert weights are dropped after
         layers = [clover.quantize_layer_q4(L) for L in layers]
         torch.cuda.synchronize()
@@ -391,7 +394,7 @@ def run_ours(args):
     # ---- algorithmic bytes: replay the same steps layer by layer (the kernels
     # are deterministic) and count the experts each launch touched.
     # per expert: bf16 weights, or 4-bit codes + one bf16 scale per 64 weights
-    ebytes = D.expert_bytes if kind != "int4" else D.expert_params // 2 + D.expert_params // 64 * 2
+    ebytes = D.expert_bytes if not q4 else D.expert_params // 2 + D.expert_params // 64 * 2
     u_per_launch = []
     if head_like:
         alg = [D.head_bytes] * n_ev
@@ -485,10 +488,11 @@ def run_ours(args):
     if rank != 0:
         return
     csum = clk.summary()
-    # <= 32 positions: one fused launch per layer; more: route, perm, experts, combine
-    per_layer = 1 if n_pos <= 32 else 4
+    # <= 32 positions: one fused launch per layer; more: route, experts (with the permutation), combine
+    per_layer = 1 if n_pos <= 32 else 3
     launches_per_step = {"step": 1 + per_layer * n_layers + 2, "zipf": 1 + per_layer * n_layers + 2,
                          "coreset": 1 + per_layer * n_layers + 2, "int4": 1 + per_layer * n_layers + 2, "layer": per_layer, "zipf_layer": per_layer,
+                         "int4_layer": per_layer,
                          "head": 2, "accept": 2}[kind]
     roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
                    else "k_head<accept> + k_rmsnorm (head statistics, entropy and the accept test)"
@@ -508,7 +512,7 @@ def run_ours(args):
                    "step_roofline_frac": step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / peak},
         "roofline": {"kernel": roof_kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": _expert_traffic(u_mean, n_pos <= 32, kind == "int4") if not head_like else None,
+                     "traffic": _expert_traffic(u_mean, n_pos <= 32, q4) if not head_like else None,
                      "launches": len(durs),
                      "mean_launch_us": float(np.mean(durs)) * 1e3, "share_of_step": share,
                      "ms_per_step_with_events": ms_instr / args.steps},
