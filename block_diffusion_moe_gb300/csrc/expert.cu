@@ -207,7 +207,9 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
   int sa = 0;
   uint32_t pha = 0, issued = 0, parity_bits = 0;
   for (int it = 0;; ++it) {
-    int u = atomicAdd(p.unit_ctr, 1);
+    // A CTA that gave up (n_total == 0) draws no unit, so it never takes
+    // work away from the others.
+    int u = n_total > 0 ? atomicAdd(p.unit_ctr, 1) : n_total;
     if (u >= n_total) {
       u = kUnitEnd;
       if (p.wr_next != nullptr) {

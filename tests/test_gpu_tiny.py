@@ -270,3 +270,36 @@ def test_router_exact_ties_take_the_lower_expert_id(M):
             assert set(idx_g[t].tolist()) == set(sel), (t, idx_g[t], sel)
     assert hits >= M // 4, hits  # the planted ties decide a good share of the tokens
     compare_routing(idx_g, w_g, ref, d.top_k)
+
+
+@pytest.mark.parametrize("M", [8, 40])
+def test_grid_barrier_timeout_is_reported_and_cleared(M):
+    """Failure detection without a fault: the grid barrier's arrival count in
+    the workspace control block (bytes 24-31, a 64-bit count that only grows)
+    is set one past a multiple of the grid size, so the last CTA to arrive
+    waits for a count that no CTA will reach. Its bounded wait gives up after
+    about two seconds and sets the status word; the status call reports the
+    timeout and clears the control block, and the same workspace then gives
+    the oracle's result. Fused kernel (8 tokens) and standalone expert kernel
+    (40 tokens)."""
+    d = synth.TINY
+    layer = synth.make_layer(d, 31, 0, DEV)
+    x = synth.make_x(d, M, 32, DEV)
+    ws = clover.workspace(clover.moe_workspace_bytes(d, M), x.device)
+    ws[24:32].view(torch.int64).fill_(1)
+    clover.moe_block_step(d, layer, x, ws=ws)
+    torch.cuda.synchronize()
+    with pytest.raises(clover.CloverError) as ei:
+        clover.workspace_status(ws)
+    assert ei.value.code == clover.ERR_DEVICE_TIMEOUT and "dependency wait timed out" in str(ei.value)
+    clover.workspace_status(ws)  # cleared
+    x_out, idx, w = clover.moe_block_step(d, layer, x, ws=ws)
+    torch.cuda.synchronize()
+    clover.workspace_status(ws)
+    L = layer_to_oracle(layer)
+    xh = x.cpu().numpy()
+    ref = O.moe_layer(xh, L, d.top_k, d.rms_eps)
+    compare_routing(idx.cpu().numpy(), w.cpu().numpy(), ref, d.top_k)
+    forced = O.moe_layer(xh, L, d.top_k, d.rms_eps, force_idx=idx.cpu().numpy())
+    ok, worst = hidden_close(x_out.cpu().numpy() - xh, forced["x_out"] - xh)
+    assert ok, worst
