@@ -274,15 +274,6 @@ __device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], cons
   warp_topk_regs<NT>(v, E, K, lane, allowed, true, out);
 }
 
-// Single-token form of warp_topk_n.
-__device__ __forceinline__ TopkSel warp_topk(const float* logits_row, int E, int K, int lane,
-                                             const uint32_t* allowed = nullptr) {
-  const float* rows[1] = {logits_row};
-  const bool valid[1] = {true};
-  TopkSel out[1];
-  warp_topk_n<1>(rows, valid, E, K, lane, allowed, out);
-  return out[0];
-}
 
 // D (16x8, fp32) += A (16x16, bf16, row-major) * B (16x8, bf16, column-major)
 // on the warp's tensor cores. Fragment ownership (g = lane / 4, q = lane % 4):
