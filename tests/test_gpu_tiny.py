@@ -121,7 +121,7 @@ def _head_ref(d, head, x, alpha):
     return st
 
 
-@pytest.mark.parametrize("V,M", [(1024, 8), (1000, 37), (1024, 256)])
+@pytest.mark.parametrize("V,M", [(1024, 8), (1000, 37), (1024, 256), (1100, 200)])
 def test_head_unmask_matches_oracle(V, M):
     d = _dims(vocab=V, mask_id=V - 1)
     head = synth.make_head(d, 7, DEV)
