@@ -256,9 +256,9 @@ __device__ __forceinline__ void warp_topk_regs(const float (&v)[NT * 8], int E, 
   }
 }
 
-// As warp_topk_regs, reading token n's logits from the global row rows[n]
-// (written by other CTAs of this launch: loads bypass L1). Tokens with
-// valid[n] false read nothing.
+// As warp_topk_regs (without the full-softmax probabilities), reading token
+// n's logits from the global row rows[n] (written by other CTAs of this
+// launch: loads bypass L1). Tokens with valid[n] false read nothing.
 template <int NT>
 __device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], const bool (&valid)[NT], int E, int K,
                                             int lane, const uint32_t* allowed, TopkSel (&out)[NT]) {
@@ -271,7 +271,7 @@ __device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], cons
       v[n * 8 + i] = (valid[n] && e < E) ? __ldcg(rows[n] + e) : -INFINITY;
     }
   }
-  warp_topk_regs<NT>(v, E, K, lane, allowed, true, out);
+  warp_topk_regs<NT>(v, E, K, lane, allowed, false, out);
 }
 
 
