@@ -2,7 +2,8 @@
 shared, SwiGLU 2048->512->2048, vocabulary 248,320, blocks of 32), in the
 launch configuration the benchmark uses:
 
-* one MoE layer on a 32-position block (all outputs against the oracle);
+* one MoE layer on a 32-position block (all outputs against the oracle), and
+  on 1, 33 and 100 tokens (both routing paths, ragged tiles);
 * head + unmask on 32 positions with logit scales calibrated so ~40% of the
   positions clear 0.95;
 * the full 40-layer denoising step: the fused entry point equals the
@@ -58,6 +59,16 @@ def test_one_layer_block_of_32(model):
     assert ties <= 2
     u = len(np.unique(idx))
     assert 140 <= u <= 185          # ~163 experts touched under uniform routing
+
+
+@pytest.mark.parametrize("M", [1, 33, 100])
+def test_one_layer_ragged_token_counts(model, M):
+    """One token (the fused kernel's smallest block), 33 (the first count that
+    takes the standalone routing and expert kernels) and 100 (a ragged tile of
+    the standalone path) at full Clover size."""
+    x = synth.make_x(D, M, 40 + M, DEV)
+    idx, ties = _check_layer(model["layers"][2], x, M)
+    assert ties <= max(1, M // 16)
 
 
 def test_one_layer_256_tokens_zipf(model):
