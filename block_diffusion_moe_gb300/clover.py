@@ -71,6 +71,7 @@ EXPORTS = {
                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                             ctypes.c_size_t, ctypes.c_void_p]),
     "clover_denoise_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),
+    "clover_denoise_hidden_offset": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),
     "clover_denoise_step": (ctypes.c_int, [ctypes.POINTER(Dims), ctypes.POINTER(MoeLayer), ctypes.c_int32,
                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_float, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -197,6 +198,15 @@ def head_workspace_bytes(d: synth.Dims, max_tokens: int) -> int:
 
 def denoise_workspace_bytes(d: synth.Dims, max_tokens: int) -> int:
     return lib().clover_denoise_workspace_bytes(ctypes.byref(make_dims(d)), max_tokens)
+
+
+def denoise_hidden(d: synth.Dims, ws: torch.Tensor, M: int) -> torch.Tensor:
+    """The fp32 [M][H] residual stream the last denoise step left in `ws`
+    (a view into the workspace)."""
+    o = lib().clover_denoise_hidden_offset(ctypes.byref(make_dims(d)), M)
+    if o == 0:
+        raise CloverError(ERR_INVALID_ARG, last_error())
+    return ws[o:o + M * d.hidden * 4].view(torch.float32).view(M, d.hidden)
 
 
 def moe_block_step(d: synth.Dims, layer: synth.Layer, x_in: torch.Tensor, x_out: torch.Tensor | None = None,

@@ -54,8 +54,8 @@ enum CtrlWord : int {
 };
 
 struct MoeLayout {
-  size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, topk_p, rr_idx, rr_w, logits, xg,
-      hbuf, yslot, bytes;
+  size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, topk_p, rr_idx, rr_w, fin_w, logits,
+      xg, hbuf, yslot, bytes;
 };
 
 MoeLayout moe_layout(const clover_dims& d, int M) {
@@ -80,6 +80,7 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
   L.topk_p = take(M * K * 4);
   L.rr_idx = take(M * K * 4);
   L.rr_w = take(M * K * 4);
+  L.fin_w = take(M * K * 4);
   L.logits = take(static_cast<size_t>(M) * E * 4);
   L.xg = take(R * H * 2);
   L.hbuf = take(R * F * 2);
@@ -267,10 +268,12 @@ int record(cudaEvent_t ev, cudaStream_t s) {
 }
 
 // Route + permutation + experts for one layer. ctrl: this call's MoE control
-// block; err: status word to flag.
+// block; err: status word to flag. A chain of fused layers working in place
+// on one x may defer each layer's combine: `defer` leaves it to the next
+// launch on the same workspace (which takes `pend`) or to enqueue_combine.
 int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const float* x_in, float* x_out,
                       int32_t* out_idx, float* out_w, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
-                      cudaStream_t stream, const void* next_router = nullptr) {
+                      cudaStream_t stream, const void* next_router = nullptr, bool defer = false, bool pend = false) {
   const MoeLayout L = moe_layout(d, M);
   const int H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
   const int MK = M * K;
@@ -281,6 +284,8 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
 
   // The fused kernel gives each CTA at most kRouteExperts router rows.
   const bool fused = M <= kLayerMaxTokens && (E + plan.sms - 1) / plan.sms <= kRouteExperts;
+  if ((defer || pend) && (!fused || x_in != x_out))
+    return fail(CLOVER_ERR_INVALID_ARG, "a deferred combine needs the fused layer kernel working in place");
   if (d.coreset_top_p > 0.f && !fused)
     return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "the block coreset needs at most %d positions", kLayerMaxTokens);
   cudaError_t e = cudaSuccess;
@@ -434,7 +439,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   // Up to 32 tokens the down unit that completes a hidden slice combines it
   // (a few µs); with more tokens that serial walk would dominate, so a
   // parallel kernel does it.
-  xa.combine = fused ? 1 : 0;
+  xa.combine = fused ? (defer ? 2 : 1) : 0;
+  xa.pend = pend ? 1 : 0;
+  xa.fin_w = reinterpret_cast<float*>(data + L.fin_w);
   size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq, kg);
   if (fused) {
     xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
@@ -474,6 +481,24 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     if ((rc = record(g_prof.end[g_prof.count % g_prof.cap], stream))) return rc;
     ++g_prof.count;
   }
+  return CLOVER_OK;
+}
+
+// The combine a deferring fused layer left behind (tables in its workspace),
+// in place on x.
+int enqueue_combine(const clover_dims& d, float* x, int M, uint8_t* data, cudaStream_t stream) {
+  const MoeLayout L = moe_layout(d, M);
+  CombineArgs ca;
+  ca.x_in = x;
+  ca.x_out = x;
+  ca.yslot = reinterpret_cast<float*>(data + L.yslot);
+  ca.tok_slot = reinterpret_cast<int32_t*>(data + L.tok_slot);
+  ca.topk_w = reinterpret_cast<float*>(data + L.fin_w);
+  ca.M = M;
+  ca.H = d.hidden;
+  ca.K = d.top_k;
+  const cudaError_t e = launch_combine(ca, stream, kPdl);
+  if (e != cudaSuccess) return cuda_fail(e, "launch combine");
   return CLOVER_OK;
 }
 
@@ -617,12 +642,18 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
   ea.V = dims->vocab;
   cudaError_t e = launch_embed(ea, s, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch embed");
+  // With the fused layer kernel each layer's combine runs at the start of
+  // the next layer's launch, spread over all CTAs (one pass over the expert
+  // rows instead of a serial walk at the end of the launch); the last one is
+  // a combine kernel.
+  const bool defer = M <= kLayerMaxTokens && (dims->n_experts + plan.sms - 1) / plan.sms <= kRouteExperts;
   for (int l = 0; l < n_layers; ++l) {
     rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,
                            reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s,
-                           l + 1 < n_layers ? layers[l + 1].router_w : nullptr);
+                           l + 1 < n_layers ? layers[l + 1].router_w : nullptr, defer, defer && l > 0);
     if (rc) return rc;
   }
+  if (defer && n_layers > 0 && (rc = enqueue_combine(*dims, x, M, ws + L.moe, s))) return rc;
   rc = enqueue_head(*dims, head_w, x, logit_scale, threshold, block, tokens, masked, nullptr, nullptr, nullptr,
                     nullptr, ctrl + kCtrlCommitted, M, ws + L.head, reinterpret_cast<int*>(ws + L.head_ctrl), err,
                     plan, s);
@@ -761,6 +792,11 @@ int clover_lmhead_accept(const clover_dims* dims, const uint16_t* head_w, const 
 size_t clover_denoise_workspace_bytes(const clover_dims* dims, int32_t max_tokens) {
   if (check_dims(dims) || check_tokens(max_tokens)) return 0;
   return denoise_layout(*dims, max_tokens).bytes;
+}
+
+size_t clover_denoise_hidden_offset(const clover_dims* dims, int32_t max_tokens) {
+  if (check_dims(dims) || check_tokens(max_tokens)) return 0;
+  return denoise_layout(*dims, max_tokens).x;
 }
 
 int clover_denoise_step(const clover_dims* dims, const clover_moe_layer* layers, int32_t n_layers,

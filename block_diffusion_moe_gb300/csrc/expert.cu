@@ -654,6 +654,24 @@ __device__ void combine_slice(const ExpertArgs& p, const Rt& rt, int j, int t0, 
   }
 }
 
+// Combines token t's 128-wide hidden slice j with one warp (lane l takes
+// columns 4l..4l+3), in the same order as combine_slice.
+__device__ void combine_token(const ExpertArgs& p, const Rt& rt, int j, int t, int lane) {
+  const size_t col = static_cast<size_t>(j) * 128 + lane * 4;
+  const int MK = p.M * p.K;
+  const float4 ys = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t) * p.H + col));
+  const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * p.H + col);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < p.K; k0 += 8) {
+    int r[8];
+    float wk[8];
+    float4 y[8];
+    combine_loads(p, rt, t, col, k0, r, wk, y);
+    combine_accumulate(acc, wk, y, k0, p.K);
+  }
+  combine_store(p, t, col, acc, ys, xi);
+}
+
 __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;             // TMEM lane quarter this warp may read
@@ -766,13 +784,13 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
         }
       }
       tc_fence_before();
-      if (p.combine) __threadfence();  // otherwise the rows are read by a later kernel
+      if (p.combine == 1) __threadfence();  // otherwise the rows are read by a later kernel
       named_bar_sync(1, 128);
       if (etid == 0 && p.stamps != nullptr) atomicMax(p.stamps + 6, global_ns());
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
         int last = 0;
-        if (p.combine) last = (atomicAdd(&p.dn_done[w.slice], 1) == rt.n_exp - 1) ? 1 : 0;
+        if (p.combine == 1) last = (atomicAdd(&p.dn_done[w.slice], 1) == rt.n_exp - 1) ? 1 : 0;
         *s.s_last = last;
       }
       named_bar_sync(1, 128);
@@ -1055,7 +1073,20 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pdl_wait();
   pdl_trigger();
   if (st) st[1] = global_ns();
-  if (threadIdx.x == 0 && x_staged) {  // written by the previous kernel
+  if (p.pend) {
+    // The previous layer left its combine to this launch: every CTA combines
+    // its share of (token, 128-wide slice) pieces from the previous layer's
+    // expert rows and published tables, one warp per piece, then a grid
+    // barrier before any CTA reads the combined rows.
+    Rt prev;
+    prev.tok_slot = p.tok_slot;
+    prev.topk_w = p.fin_w;
+    const int SH = H >> 7, n_pieces = M * SH, nw = blockDim.x >> 5;
+    for (int pc = blockIdx.x + G * warp; pc < n_pieces; pc += G * nw)
+      combine_token(p, prev, pc % SH, pc / SH, lane);
+    if (!grid_barrier(p.bar_count, p.err)) *s.abort = 1u;
+  }
+  if (threadIdx.x == 0 && x_staged) {  // written by the previous kernel (or just combined)
     mbar_arrive_expect_tx(xbar, x_bytes);
     bulk_load(smem_u32(s.a_ring) + x_off, p.x_in + static_cast<size_t>(xt0) * H, x_bytes, xbar);
   }
@@ -1259,6 +1290,12 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
       for (int i = threadIdx.x; i < MK; i += blockDim.x) p.out_idx[i] = s_idx[i];
     if (p.out_w)
       for (int i = threadIdx.x; i < MK; i += blockDim.x) p.out_w[i] = s_w[i];
+    if (p.combine == 2) {  // the next launch (or the combine kernel) combines from these
+      for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+        p.tok_slot[i] = s_slot[i];
+        p.fin_w[i] = s_w[i];
+      }
+    }
   }
   __syncthreads();
 

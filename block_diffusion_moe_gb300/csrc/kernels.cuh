@@ -129,7 +129,10 @@ struct ExpertArgs {
   int* err;
   int M, H, F, E, K;
   int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
-  int combine;  // 1: the down unit that completes a hidden slice combines it; 0: k_combine does
+  int combine;  // 1: the down unit that completes a hidden slice combines it; 0: k_combine does;
+                // 2 (fused kernel): no combine here, the final tables are published for a later one
+  int pend;     // fused kernel: first combine the previous launch's deferred output (same workspace)
+  float* fin_w; // [M][K] final selection weights published for a deferred combine
   // fused-layer launches only (k_layer)
   const bf16* wr;      // [E][H] router
   const bf16* wr_next; // [E][H] the next layer's router (nullable): its slices are prefetched into L2

@@ -200,6 +200,13 @@ int clover_lmhead_accept(const clover_dims* dims, const uint16_t* head_w, const 
 /* Bytes of workspace the denoise entry points need. Host-only. */
 size_t clover_denoise_workspace_bytes(const clover_dims* dims, int32_t max_tokens);
 
+/* Byte offset, within a denoise workspace sized for max_tokens, of the
+ * residual stream that the last clover_denoise_step left there: fp32 [M][H],
+ * the output of the last MoE sublayer (the input of the final RMSNorm and
+ * the head). Host-only. Returns 0 for invalid dims or max_tokens (the offset
+ * itself is never 0). */
+size_t clover_denoise_hidden_offset(const clover_dims* dims, int32_t max_tokens);
+
 /* One block-diffusion denoising step over M positions (Files, "How it
  * writes", steps 1-3): x_p = E[tokens_p] + ctx_p (the mask token's embedding
  * while masked), n_layers MoE sublayers as in clover_moe_block_step, a final

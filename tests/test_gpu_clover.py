@@ -7,7 +7,7 @@ launch configuration the benchmark uses:
 * head + unmask on 32 positions with logit scales calibrated so ~40% of the
   positions clear 0.95;
 * the full 40-layer denoising step: the fused entry point equals the
-  layer-by-layer composition bit for bit, sampled layers match the oracle
+  layer-by-layer composition bit for bit (hidden state and decisions), sampled layers match the oracle
   under teacher forcing, and the block-level invariants hold over a whole
   block (never re-masks, progresses every step, every slot ends with the
   token it predicted while masked, commits in descending confidence);
@@ -126,12 +126,15 @@ def test_full_step_composition_and_sampled_layers(model):
     ctx = synth.make_ctx(D, M, 5, DEV)
     cmodel = clover.Model(D, model["layers"], model["embed"], model["head"])
     t1, m1 = synth.masked_block(D, M, DEV)
-    clover.denoise_step(cmodel, ctx, t1, m1, block=32)
+    ws = clover.denoise_step(cmodel, ctx, t1, m1, block=32)
     t2, m2 = synth.masked_block(D, M, DEV)
     xs, idxs, xf, out = _compose_step(model, model["layers"], ctx, t2, m2)
     torch.cuda.synchronize()
     assert torch.equal(t1, t2) and torch.equal(m1, m2)
     assert int(m1.sum()) == M - 1
+    # the step's own residual stream (each layer's combine deferred into the
+    # next launch) equals the composition's, bit for bit
+    assert torch.equal(clover.denoise_hidden(D, ws, M), xf)
     # teacher-forced oracle checks of sampled layers
     for l in (0, 19, 39):
         L = layer_to_oracle(model["layers"][l], lazy=True)

@@ -199,6 +199,34 @@ def test_tiny_denoise_four_steps():
     clover.workspace_status(ws)
 
 
+@pytest.mark.parametrize("M", [8, 32, 40])
+def test_multi_layer_step_hidden_equals_composition(M):
+    """Three layers: the denoise step's residual stream (up to 32 positions
+    each layer's combine runs at the start of the next layer's launch, the
+    last in a combine kernel) equals per-layer calls bit for bit, and every
+    layer of the composition matches the oracle under its own routing."""
+    d = synth.TINY
+    layers = [synth.make_layer(d, 5, l, DEV) for l in range(3)]
+    embed = synth.make_embed(d, 5, DEV)
+    head = synth.make_head(d, 5, DEV)
+    ctx = synth.make_ctx(d, M, 5, DEV)
+    model = clover.Model(d, layers, embed, head)
+    tokens, masked = synth.masked_block(d, M, DEV)
+    t0 = tokens.clone()
+    ws = clover.denoise_step(model, ctx, tokens, masked, block=d.block)
+    x = embed[t0.long()].float() + ctx
+    for layer in layers:
+        xi = x
+        x, idx, _ = clover.moe_block_step(d, layer, xi)
+        torch.cuda.synchronize()
+        L = layer_to_oracle(layer)
+        ref = O.moe_layer(xi.cpu().numpy(), L, d.top_k, d.rms_eps, force_idx=idx.cpu().numpy())
+        ok, worst = hidden_close(x.cpu().numpy(), ref["x_out"])
+        assert ok, worst
+    assert torch.equal(clover.denoise_hidden(d, ws, M), x)
+    clover.workspace_status(ws)
+
+
 def test_denoise_block_runs_to_completion_and_reports():
     d = synth.TINY
     n = 16
