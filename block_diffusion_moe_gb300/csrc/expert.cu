@@ -1119,7 +1119,9 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
                                               : p.wr + static_cast<size_t>(e0) * H;
       __nv_bfloat16* xn_out = eg == 0 ? p.xn + static_cast<size_t>(t) * H : nullptr;
       float lg;
-      if (H <= 128 * 16) {
+      if (x_staged && wr_staged && H == 2048 && ne == kRouteExperts) {
+        lg = warp_router_row_smem<kRouteExperts, 2048>(smem_u32(xr), p.eps, smem_u32(w_rows), lane, xn_out);
+      } else if (H <= 128 * 16) {
         lg = warp_router_row_reg<kRouteExperts, 16>(xr, p.eps, w_rows, ne, H, lane, xn_out);
       } else {
         const float rstd = row_rstd(xr, H, p.eps, lane);

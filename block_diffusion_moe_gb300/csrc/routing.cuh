@@ -85,6 +85,69 @@ __device__ __forceinline__ float warp_router_row_reg(const float* xr, float eps,
   return mine;
 }
 
+// warp_router_row_reg for the common shape, with both operands staged in
+// shared memory (32-bit shared addresses) and the hidden size and expert
+// count fixed at compile time: explicit shared loads, no per-element guards
+// and constant offsets let every load of a chunk issue ahead of its FMAs.
+// The same expressions in the same order, so the results are identical.
+template <int kE, int kH>
+__device__ __forceinline__ float warp_router_row_smem(uint32_t xr, float eps, uint32_t w_rows, int lane,
+                                                      __nv_bfloat16* xn_out) {
+  constexpr int kChunks = kH / 128;
+  static_assert(kH % 128 == 0, "hidden size must be a multiple of 128");
+  float4 xv[kChunks];
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const uint32_t a = xr + static_cast<uint32_t>(lane * 4 + 128 * j) * 4u;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(xv[j].x), "=f"(xv[j].y), "=f"(xv[j].z), "=f"(xv[j].w)
+                 : "r"(a));
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) ss += xv[j].x * xv[j].x + xv[j].y * xv[j].y + xv[j].z * xv[j].z + xv[j].w * xv[j].w;
+  ss = warp_sum_f(ss);
+  const float rstd = 1.0f / sqrtf(ss / static_cast<float>(kH) + eps);
+  float acc[kE];
+#pragma unroll
+  for (int e = 0; e < kE; ++e) acc[e] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) {
+    const int c = lane * 4 + 128 * j;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(xv[j].x * rstd, xv[j].y * rstd);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(xv[j].z * rstd, xv[j].w * rstd);
+    if (xn_out != nullptr) {
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(xn_out + c) = pk;
+    }
+    const float x0 = __low2float(lo), x1 = __high2float(lo), x2 = __low2float(hi), x3 = __high2float(hi);
+    uint2 wb[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      const uint32_t a = w_rows + static_cast<uint32_t>(e * kH + c) * 2u;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(wb[e].x), "=r"(wb[e].y) : "r"(a));
+    }
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      const __nv_bfloat162 w01 = *reinterpret_cast<const __nv_bfloat162*>(&wb[e].x);
+      const __nv_bfloat162 w23 = *reinterpret_cast<const __nv_bfloat162*>(&wb[e].y);
+      acc[e] = fmaf(x0, __low2float(w01), acc[e]);
+      acc[e] = fmaf(x1, __high2float(w01), acc[e]);
+      acc[e] = fmaf(x2, __low2float(w23), acc[e]);
+      acc[e] = fmaf(x3, __high2float(w23), acc[e]);
+    }
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < kE; ++e) {
+    const float sm = warp_sum_f(acc[e]);
+    if (lane == e) mine = sm;
+  }
+  return mine;
+}
+
 // One warp, one token row xr: xn = bf16(xr * rstd) (stored to xn_out when
 // non-null) and the router logits of experts w_rows[0..ne) (ne <= 8), each a
 // bf16 row of H. Lane e (< ne) receives logit e (without bias).
