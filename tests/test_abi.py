@@ -66,6 +66,14 @@ def test_workspace_sizes(lib):
     assert lib.clover_moe_workspace_bytes(ctypes.byref(d), 0) == 0
     assert lib.clover_moe_workspace_bytes(ctypes.byref(d), 257) == 0
     assert lib.clover_moe_workspace_bytes(None, 32) == 0
+    # the residual stream the denoise step leaves: an fp32 [M][H] block that
+    # lies inside the workspace for every M up to the size it was built for
+    for m in (1, 32):
+        o = lib.clover_denoise_hidden_offset(ctypes.byref(d), m)
+        assert o > 0 and o % 16 == 0
+        assert o + m * 2048 * 4 <= lib.clover_denoise_workspace_bytes(ctypes.byref(d), m)
+    assert lib.clover_denoise_hidden_offset(ctypes.byref(d), 0) == 0
+    assert lib.clover_denoise_hidden_offset(None, 32) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
