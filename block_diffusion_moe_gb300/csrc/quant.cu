@@ -3,8 +3,8 @@
 //
 // The pages name INT4 for one deployment of the model ("Clover-35B-A3B: how a
 // diffusion model gets to 680 tokens a second, read from its files", section
-// "What 680 tokens a second has to be") but give no format; this one is the
-// build's own. Per group: s = bf16(float32(max |w|) / 7) (IEEE fp32 division,
+// "What 680 tokens a second has to be") but give no format; this one is
+// this library's own. Per group: s = bf16(float32(max |w|) / 7) (IEEE fp32 division,
 // round to nearest even); per element u = clamp(rint(w / s), -8, 7) + 8
 // (u = 8 where s = 0); the weight a product uses is bf16((u - 8) s). Eight
 // codes fill a 32-bit word in the nibble order e0 e2 e4 e6 e1 e3 e5 e7, so

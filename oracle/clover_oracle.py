@@ -25,7 +25,7 @@ diffusion model gets to 680 tokens a second, read from its files"):
   "What DiffuSpace actually shipped": block of 32 masked positions resolved
   by a 0.95 confidence threshold.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 
 * Top-k routing is softmax over all routed experts, then the top-k
   probabilities renormalised to sum to one. Ties go to the lower expert id.
@@ -68,8 +68,8 @@ Readings where the pages are silent (each is listed in the design doc):
   probability zero, so it is never accepted; a draft id outside the
   vocabulary is never accepted either.
 
-* Low-bit expert weights (SURVEY's NEXT 4; the pages name INT4 for one
-  deployment but give no format, so this format is the build's own): each
+* Low-bit expert weights (the pages name INT4 for one deployment but give
+  no format, so this format is this implementation's own): each
   expert matrix [R][K] keeps one bf16 scale per row and group of 64
   consecutive K elements, s = bf16(float32(max |w|) / 7) (fp32 IEEE division,
   then round to nearest even), and per element the 4-bit code

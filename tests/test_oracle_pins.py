@@ -548,7 +548,7 @@ def test_accept_invariants():
 
 
 # ---------------------------------------------------------------------------
-# Low-bit expert weight format (SURVEY's NEXT 4; the build's own format)
+# Low-bit expert weight format (this implementation's own; the pages give none)
 
 
 def _bf16_bits(x):
