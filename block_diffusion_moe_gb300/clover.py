@@ -61,6 +61,7 @@ EXPORTS = {
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                    ctypes.c_int32, ctypes.c_void_p]),
+    "clover_lmhead_unmask_static_status": (ctypes.c_int, [ctypes.c_void_p]),
     "clover_quantize_q4": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "clover_accept_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Dims), ctypes.c_int32]),

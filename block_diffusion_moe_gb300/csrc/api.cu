@@ -9,10 +9,15 @@
 #include <mutex>
 
 #include "../../include/clover.h"
+#include "internal.h"
 #include "kernels.cuh"
+#include "plan.h"
 #include "sm100.cuh"
 
 using namespace clover;
+
+static_assert(plan::kFusedMaxTokens == kLayerMaxTokens && plan::kFusedRouterRowsPerCta == kRouteExperts,
+              "the launch plan and the fused layer kernel must agree on its limits");
 
 namespace {
 
@@ -267,6 +272,35 @@ int record(cudaEvent_t ev, cudaStream_t s) {
   return CLOVER_OK;
 }
 
+// Occupancy of an expert kernel at a shared-memory size, cached per
+// (device, kernel, size): the query runs once per configuration.
+int resident_per_sm(bool fused, bool q4, size_t smem, int* out) {
+  struct Entry {
+    int dev, kind;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int n_cached = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const int kind = (fused ? 2 : 0) + (q4 ? 1 : 0);
+  std::lock_guard<std::mutex> g(mu);
+  for (int i = 0; i < n_cached; ++i)
+    if (cache[i].dev == dev && cache[i].kind == kind && cache[i].smem == smem) {
+      *out = cache[i].n;
+      return CLOVER_OK;
+    }
+  int n = 0;
+  e = expert_resident_per_sm(fused, q4, smem, &n);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy of the expert kernel");
+  if (n_cached < 64) cache[n_cached++] = Entry{dev, kind, smem, n};
+  *out = n;
+  return CLOVER_OK;
+}
+
 // Route + permutation + experts for one layer. ctrl: this call's MoE control
 // block; err: status word to flag. A chain of fused layers working in place
 // on one x may defer each layer's combine: `defer` leaves it to the next
@@ -282,8 +316,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   int32_t* topk_idx = reinterpret_cast<int32_t*>(data + L.topk_idx);
   float* topk_w = reinterpret_cast<float*>(data + L.topk_w);
 
-  // The fused kernel gives each CTA at most kRouteExperts router rows.
-  const bool fused = M <= kLayerMaxTokens && (E + plan.sms - 1) / plan.sms <= kRouteExperts;
+  const bool fused = plan::moe_fused(M, E, plan.sms);
   if ((defer || pend) && (!fused || x_in != x_out))
     return fail(CLOVER_ERR_INVALID_ARG, "a deferred combine needs the fused layer kernel working in place");
   if (d.coreset_top_p > 0.f && !fused)
@@ -456,13 +489,25 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     xa.pub2_w = reinterpret_cast<float*>(data + L.rr_w);
     xa.coreset_top_p = d.coreset_top_p;
     xa.eps = d.rms_eps;
+#if CLOVER_PHASE_STAMPS
     xa.stamps = reinterpret_cast<unsigned long long*>(ctrl + kCtrlStamps);
+#else
+    xa.stamps = nullptr;
+#endif
     smem += layer_rt_bytes(M, K, E);
   }
+  // Every CTA of the persistent kernel waits at grid barriers, so the whole
+  // grid must be resident at once: check it before launching.
+  int resident = 0;
+  if ((rc = resident_per_sm(fused, q4, smem, &resident))) return rc;
+  const int grid = plan::persistent_grid(plan.sms, resident);
+  if (grid == 0)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "the %s expert kernel cannot be resident on an SM (%zu bytes of shared "
+                "memory, occupancy %d)", fused ? "fused" : "standalone", smem, resident);
   if (g_prof.begin && g_prof.cap > 0) {
     if ((rc = record(g_prof.begin[g_prof.count % g_prof.cap], stream))) return rc;
   }
-  e = fused ? launch_layer(xa, plan.sms, smem, stream, kPdl) : launch_expert(xa, plan.sms, smem, stream, kPdl);
+  e = fused ? launch_layer(xa, grid, smem, stream, kPdl) : launch_expert(xa, grid, smem, stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, fused ? "launch layer" : "launch expert");
   if (!xa.combine) {
     CombineArgs ca;
@@ -646,7 +691,7 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
   // the next layer's launch, spread over all CTAs (one pass over the expert
   // rows instead of a serial walk at the end of the launch); the last one is
   // a combine kernel.
-  const bool defer = M <= kLayerMaxTokens && (dims->n_experts + plan.sms - 1) / plan.sms <= kRouteExperts;
+  const bool defer = plan::moe_fused(M, dims->n_experts, plan.sms);
   for (int l = 0; l < n_layers; ++l) {
     rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,
                            reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s,
@@ -672,6 +717,67 @@ namespace clover {
 // Lets other translation units of the library report through
 // clover_last_error().
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+// clover_lmhead_unmask with one option: clear_ctrl zeroes the workspace's
+// control words on the stream (after every argument check, so a rejected
+// call enqueues nothing) for scratch memory whose previous contents are not
+// known.
+int lmhead_unmask_check(const clover_dims* dims, const uint16_t* head_w, const float* x, float threshold,
+                        int32_t block, const int32_t* tokens, const uint8_t* masked, int32_t M) {
+  int rc;
+  if ((rc = check_dims(dims))) return rc;
+  if ((rc = check_tokens(M))) return rc;
+  if (!head_w || !x || !tokens || !masked) return fail(CLOVER_ERR_INVALID_ARG, "NULL head_w/x/tokens/masked");
+  if (!aligned16(head_w) || !aligned16(x)) return fail(CLOVER_ERR_INVALID_ARG, "head_w/x not 16-byte aligned");
+  if (block < 1) return fail(CLOVER_ERR_INVALID_ARG, "block=%d < 1", block);
+  if (!(threshold == threshold)) return fail(CLOVER_ERR_INVALID_ARG, "threshold is NaN");
+  return CLOVER_OK;
+}
+
+int lmhead_unmask_impl(const clover_dims* dims, const uint16_t* head_w, const float* x, const float* logit_scale,
+                       float threshold, int32_t block, int32_t* tokens, uint8_t* masked, int32_t* argmax,
+                       float* max_logit, float* lse, float* max_prob, int32_t* n_committed, int32_t M,
+                       void* workspace, size_t workspace_bytes, clover_stream_t stream, bool clear_ctrl) {
+  int rc;
+  if ((rc = lmhead_unmask_check(dims, head_w, x, threshold, block, tokens, masked, M))) return rc;
+  if ((rc = check_ws(workspace, workspace_bytes, kCtrlBytes + head_layout(*dims, M).bytes))) return rc;
+  if ((rc = get_encoder())) return rc;
+  DevInfo di;
+  if ((rc = device_info(&di))) return rc;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* ctrl = reinterpret_cast<int*>(ws);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (clear_ctrl) {
+    const cudaError_t e = cudaMemsetAsync(ws, 0, kCtrlBytes, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the control words");
+  }
+  rc = enqueue_head(*dims, head_w, x, logit_scale, threshold, block, tokens, masked, argmax, max_logit, lse, max_prob,
+                    n_committed, M, ws + kCtrlBytes, ctrl, ctrl + kCtrlErr, Plan{di.sms}, s);
+  if (rc) return rc;
+  return check_launch_errors("lmhead unmask");
+}
+
+// Synchronises the stream, reads the status word of the control block at
+// `workspace`, and if it is set clears the control block and reports it.
+int workspace_status_impl(void* workspace, size_t workspace_bytes, clover_stream_t stream) {
+  if (workspace == nullptr || workspace_bytes < kCtrlBytes) return fail(CLOVER_ERR_INVALID_ARG, "bad workspace");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
+  if (word == 0) return CLOVER_OK;
+  // Clear the status word and the arrival counters a failed kernel may have
+  // left behind, so the workspace is usable again.
+  e = cudaMemset(workspace, 0, kCtrlBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
+  char what[160] = {0};
+  snprintf(what, sizeof(what), "%s%s%s%s", (word & kErrMbarTimeout) ? "pipeline wait timed out; " : "",
+           (word & kErrDepTimeout) ? "cross-CTA dependency wait timed out; " : "",
+           (word & kErrBadToken) ? "token id out of range; " : "",
+           (word & kErrBadRoute) ? "expert id out of range; " : "");
+  return fail(CLOVER_ERR_DEVICE_TIMEOUT, "device status 0x%x: %s", word, what);
+}
 }  // namespace clover
 
 extern "C" {
@@ -715,24 +821,8 @@ int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const 
                          float threshold, int32_t block, int32_t* tokens, uint8_t* masked, int32_t* argmax,
                          float* max_logit, float* lse, float* max_prob, int32_t* n_committed, int32_t M,
                          void* workspace, size_t workspace_bytes, clover_stream_t stream) {
-  int rc;
-  if ((rc = check_dims(dims))) return rc;
-  if ((rc = check_tokens(M))) return rc;
-  if (!head_w || !x || !tokens || !masked) return fail(CLOVER_ERR_INVALID_ARG, "NULL head_w/x/tokens/masked");
-  if (!aligned16(head_w) || !aligned16(x)) return fail(CLOVER_ERR_INVALID_ARG, "head_w/x not 16-byte aligned");
-  if (block < 1) return fail(CLOVER_ERR_INVALID_ARG, "block=%d < 1", block);
-  if (!(threshold == threshold)) return fail(CLOVER_ERR_INVALID_ARG, "threshold is NaN");
-  if ((rc = check_ws(workspace, workspace_bytes, kCtrlBytes + head_layout(*dims, M).bytes))) return rc;
-  if ((rc = get_encoder())) return rc;
-  DevInfo di;
-  if ((rc = device_info(&di))) return rc;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int* ctrl = reinterpret_cast<int*>(ws);
-  rc = enqueue_head(*dims, head_w, x, logit_scale, threshold, block, tokens, masked, argmax, max_logit, lse, max_prob,
-                    n_committed, M, ws + kCtrlBytes, ctrl, ctrl + kCtrlErr, Plan{di.sms},
-                    reinterpret_cast<cudaStream_t>(stream));
-  if (rc) return rc;
-  return check_launch_errors("lmhead unmask");
+  return clover::lmhead_unmask_impl(dims, head_w, x, logit_scale, threshold, block, tokens, masked, argmax, max_logit,
+                                    lse, max_prob, n_committed, M, workspace, workspace_bytes, stream, false);
 }
 
 int clover_quantize_q4(const uint16_t* w, int32_t n_mats, int32_t rows, int32_t cols, uint8_t* q, uint16_t* s,
@@ -845,23 +935,7 @@ int clover_denoise_block(const clover_dims* dims, const clover_moe_layer* layers
 }
 
 int clover_workspace_status(void* workspace, size_t workspace_bytes, clover_stream_t stream) {
-  if (workspace == nullptr || workspace_bytes < kCtrlBytes) return fail(CLOVER_ERR_INVALID_ARG, "bad workspace");
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  int word = 0;
-  cudaError_t e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess) e = cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "reading the workspace status");
-  if (word == 0) return CLOVER_OK;
-  // Clear the status word and the arrival counters a failed kernel may have
-  // left behind, so the workspace is usable again.
-  e = cudaMemset(workspace, 0, kCtrlBytes);
-  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
-  char what[160] = {0};
-  snprintf(what, sizeof(what), "%s%s%s%s", (word & kErrMbarTimeout) ? "pipeline wait timed out; " : "",
-           (word & kErrDepTimeout) ? "cross-CTA dependency wait timed out; " : "",
-           (word & kErrBadToken) ? "token id out of range (clamped); " : "",
-           (word & kErrBadRoute) ? "expert id out of range; " : "");
-  return fail(CLOVER_ERR_DEVICE_TIMEOUT, "device status 0x%x: %s", word, what);
+  return clover::workspace_status_impl(workspace, workspace_bytes, stream);
 }
 
 int32_t clover_profile_expert_events(clover_event_t* begin, clover_event_t* end, int32_t capacity) {

@@ -786,7 +786,7 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
       tc_fence_before();
       if (p.combine == 1) __threadfence();  // otherwise the rows are read by a later kernel
       named_bar_sync(1, 128);
-      if (etid == 0 && p.stamps != nullptr) atomicMax(p.stamps + 6, global_ns());
+      if (kPhaseStamps && etid == 0 && p.stamps != nullptr) atomicMax(p.stamps + 6, global_ns());
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
         int last = 0;
@@ -1068,7 +1068,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
       bulk_load(smem_u32(s.a_ring) + j * wslice, p.wr + static_cast<size_t>(eg) * kRouteExperts * H, ne * H * 2, wbar);
     }
   }
-  unsigned long long* st = (blockIdx.x == 0 && threadIdx.x == 0) ? p.stamps : nullptr;
+  unsigned long long* st = (kPhaseStamps && blockIdx.x == 0 && threadIdx.x == 0) ? p.stamps : nullptr;
   if (st) st[0] = global_ns();
   pdl_wait();
   pdl_trigger();
@@ -1134,7 +1134,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     }
   }
   fence_proxy_async_shared();  // the ring was read generically; TMA refills it later
-  if (p.stamps != nullptr) {
+  if (kPhaseStamps && p.stamps != nullptr) {
     __syncthreads();
     if (threadIdx.x == 0) atomicMax(p.stamps + 2, global_ns());
   }
@@ -1312,7 +1312,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.dense = 1;
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
-  if (p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
+  if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
 }
 
 // smem_a: A stages in shared memory; stages_a: A barriers; kg: K groups of
@@ -1331,6 +1331,13 @@ size_t perm_smem_bytes(int M, int K, int E) {
 }
 
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }
+
+cudaError_t expert_resident_per_sm(bool fused, bool q4, size_t smem, int* n) {
+  auto* k = fused ? (q4 ? k_layer<true> : k_layer<false>) : (q4 ? k_expert<true> : k_expert<false>);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k, q4 ? kExpertThreadsQ4 : kExpertThreads, smem);
+}
 
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl) {
   auto* k = a.q4 ? k_layer<true> : k_layer<false>;

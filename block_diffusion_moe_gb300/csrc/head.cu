@@ -485,8 +485,14 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
     const int p0 = b * p.block, p1 = min(p.M, p0 + p.block);
     int n_commit = 0, best = -1;
     float best_p = 0.f;
+    bool bad = false;
     for (int i = p0; i < p1; ++i) {
-      if (!p.masked[i]) continue;
+      if (!p.masked[i]) {
+        // a committed slot must hold a vocabulary id; report one that does not
+        const int tk = p.tokens[i];
+        bad |= (tk < 0 || tk >= p.V);
+        continue;
+      }
       const float pm = s.run_m[i];
       if (pm > p.threshold) ++n_commit;
       if (best < 0 || pm > best_p) {
@@ -508,6 +514,7 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
     }
     atomicAdd(&s.s_counts[0], done);
     atomicAdd(&s.s_counts[1], still);
+    if (bad) atomicOr(p.err, kErrBadToken);
   }
   named_bar_sync(1, 128);
   if (etid == 0) {

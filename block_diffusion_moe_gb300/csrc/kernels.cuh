@@ -43,6 +43,13 @@ constexpr int kQSlotGroups = 4;
 constexpr int kQSlotBytes = kQSlotGroups * kQGroupBytes;
 constexpr int kSmemBudget = 227 * 1024;
 
+// Phase timestamps of the fused layer kernel (a diagnostic: a barrier and
+// global atomics per launch). Off unless built with -DCLOVER_PHASE_STAMPS=1.
+#ifndef CLOVER_PHASE_STAMPS
+#define CLOVER_PHASE_STAMPS 0
+#endif
+constexpr bool kPhaseStamps = CLOVER_PHASE_STAMPS != 0;
+
 struct EmbedArgs {
   const int32_t* tokens;
   const bf16* embed;  // [V][H]
@@ -205,6 +212,9 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 // (both launch the low-bit form when a.q4 != 0)
+// CTAs of the fused (k_layer) or standalone (k_expert) expert kernel that
+// can be resident on one SM at the given dynamic shared memory size.
+cudaError_t expert_resident_per_sm(bool fused, bool q4, size_t smem, int* n);
 size_t layer_rt_bytes(int M, int K, int E);
 // Shared memory the standalone expert kernel's permutation needs (in its weight ring).
 size_t perm_smem_bytes(int M, int K, int E);

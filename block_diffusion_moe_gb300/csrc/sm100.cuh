@@ -13,7 +13,7 @@ namespace clover {
 enum : int {
   kErrMbarTimeout = 1,   // an mbarrier wait ran past its time limit
   kErrDepTimeout = 2,    // a wait on another CTA's progress flag timed out
-  kErrBadToken = 4,      // a token id outside [0, V) was clamped
+  kErrBadToken = 4,      // a token id outside [0, V) was seen (the embedding lookup clamps it)
   kErrBadRoute = 8,      // an expert id outside [0, E) was seen
 };
 

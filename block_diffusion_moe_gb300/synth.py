@@ -103,14 +103,20 @@ def make_router(d: Dims, seed: int, layer: int, device="cpu") -> torch.Tensor:
     return normal((d.n_experts, d.hidden), WEIGHT_STD, _seed(seed, layer, "router"), device)
 
 
+def make_expert(d: Dims, seed: int, layer: int, e: int, device="cpu"):
+    """Routed expert e of a layer: (gate_up bf16 [2F][H], down bf16 [H][F]),
+    the same values make_layer draws for it on the same device."""
+    return (normal((2 * d.d_ff, d.hidden), WEIGHT_STD, _seed(seed, layer, "gate_up", e), device),
+            normal((d.hidden, d.d_ff), WEIGHT_STD, _seed(seed, layer, "down", e), device))
+
+
 def make_layer(d: Dims, seed: int, layer: int, device="cpu", zipf_s: float | None = None) -> Layer:
     E, H, F = d.n_experts, d.hidden, d.d_ff
     router_w = make_router(d, seed, layer, device)
     gate_up = torch.empty((E, 2 * F, H), dtype=torch.bfloat16, device=device)
     down = torch.empty((E, H, F), dtype=torch.bfloat16, device=device)
     for e in range(E):
-        gate_up[e] = normal((2 * F, H), WEIGHT_STD, _seed(seed, layer, "gate_up", e), device)
-        down[e] = normal((H, F), WEIGHT_STD, _seed(seed, layer, "down", e), device)
+        gate_up[e], down[e] = make_expert(d, seed, layer, e, device)
     sh_gate_up = normal((2 * F, H), WEIGHT_STD, _seed(seed, layer, "sh_gate_up"), device)
     sh_down = normal((H, F), WEIGHT_STD, _seed(seed, layer, "sh_down"), device)
     bias = zipf_router_bias(d, seed, layer, zipf_s, device) if zipf_s else None

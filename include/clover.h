@@ -151,7 +151,9 @@ size_t clover_head_workspace_bytes(const clover_dims* dims, int32_t max_tokens);
  * NULL (= 1). tokens int32 [M], masked uint8 [M]: in/out. argmax int32 [M],
  * max_logit, lse, max_prob fp32 [M]: out. n_committed: device int32 scalar,
  * out (number committed by this call). M % block == 0 is not required; the
- * last group may be shorter. */
+ * last group may be shorter. A committed slot (masked_p == 0) whose token id
+ * lies outside [0, V) is left as it is and reported through the workspace
+ * status word (clover_workspace_status). */
 int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const float* x,
                          const float* logit_scale, float threshold, int32_t block,
                          int32_t* tokens, uint8_t* masked,
@@ -259,16 +261,28 @@ int32_t clover_last_error(char* buf, size_t n);
  * every GPU loading the library keeps until the process exits; it fits up to
  * 102 positions at hidden 2048 (the rule: clover_head_workspace_bytes(dims, M)
  * <= 1 MiB). Larger sizes return CLOVER_ERR_WORKSPACE_TOO_SMALL and nothing
- * runs. The first call on each device looks up the array's device address;
- * make that first call before any stream capture. The call allocates nothing
- * and clears the array's control words itself. All calls share the one
- * array: calls that may overlap on the GPU (other streams, other threads)
- * race and must be serialised by the caller. */
+ * runs. Every call looks up the array's device address in the current
+ * context; the first call on a device also loads the library's kernels
+ * there, so make that first call before any stream capture. The call
+ * allocates nothing. It checks every argument before it enqueues anything,
+ * then clears the array's control words on the stream, so the status of a
+ * call must be read (clover_lmhead_unmask_static_status) before the next
+ * call. All calls share the one array: calls that may overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller. */
 int clover_lmhead_unmask_static(const clover_dims* dims, const uint16_t* head_w, const float* x,
                                 const float* logit_scale, float threshold, int32_t block,
                                 int32_t* tokens, uint8_t* masked,
                                 int32_t* argmax, float* max_logit, float* lse, float* max_prob,
                                 int32_t* n_committed, int32_t M, clover_stream_t stream);
+
+/* The device status of the last clover_lmhead_unmask_static call, which has
+ * no workspace to pass to clover_workspace_status: synchronises `stream`,
+ * reads the status word of the library's static scratch array, and if it is
+ * set clears the array's control words and returns
+ * CLOVER_ERR_DEVICE_TIMEOUT (a wait that gave up, or a committed slot whose
+ * token id lies outside [0, V); the message names which); else CLOVER_OK.
+ * (The pages have no counterpart.) */
+int clover_lmhead_unmask_static_status(clover_stream_t stream);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int32_t clover_version(void);

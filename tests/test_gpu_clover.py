@@ -6,12 +6,16 @@ launch configuration the benchmark uses:
   on 1, 33 and 100 tokens (both routing paths, ragged tiles);
 * head + unmask on 32 positions with logit scales calibrated so ~40% of the
   positions clear 0.95;
+* head + unmask on 256 positions (8 blocks of 32; the widest token tile);
 * the full 40-layer denoising step: the fused entry point equals the
-  layer-by-layer composition bit for bit (hidden state and decisions), sampled layers match the oracle
-  under teacher forcing, and the block-level invariants hold over a whole
-  block (never re-masks, progresses every step, every slot ends with the
-  token it predicted while masked, commits in descending confidence);
-* 8 blocks x 32 positions with Zipf(1.2)-biased routing.
+  layer-by-layer composition bit for bit (hidden state and decisions), every
+  one of the 40 layers matches the oracle under teacher forcing, and the
+  block-level invariants hold over a whole block (never re-masks, progresses
+  every step, every slot ends with the token it predicted while masked,
+  commits in descending confidence), both step by step and through the
+  clover_denoise_block loop itself;
+* 8 blocks x 32 positions with Zipf(1.2)-biased routing, all 40 layers
+  teacher-forced against the oracle.
 """
 import numpy as np
 import pytest
@@ -107,6 +111,57 @@ def test_head_unmask_32_positions(model):
     assert np.array_equal(masked.cpu().numpy(), rm)
 
 
+def test_head_unmask_256_positions(model):
+    """Eight blocks of 32 in one head call: the 256-column token tile, with
+    logit scales calibrated so that about 40% of the positions clear 0.95
+    (the unmask rule then runs per block of 32)."""
+    M = 256
+    x = synth.make_x(D, M, 8, DEV)
+    xh = x.cpu().numpy()
+    hb = bits(model["head"])
+    z_raw = O.head_logits(xh, hb, D.rms_eps)
+    alpha = calibrate_alpha(z_raw, D.mask_id, synth.confidence_targets(M, 9).numpy(), O, iters=40)
+    tokens, masked = synth.masked_block(D, M, DEV)
+    masked[5::7] = 0                       # some slots committed earlier
+    tokens[5::7] = 11
+    t0, m0 = tokens.cpu().numpy(), masked.cpu().numpy()
+    out = clover.lmhead_unmask(D, model["head"], x, tokens, masked, logit_scale=torch.from_numpy(alpha).to(DEV),
+                               threshold=0.95, block=32)
+    torch.cuda.synchronize()
+    z = z_raw * alpha.astype(np.float64)[:, None]
+    ref = O.head_stats(z, D.mask_id)
+    z[:, D.mask_id] = -np.inf
+    ref["z"] = z
+    got = {k: v.cpu().numpy() for k, v in out.items()}
+    compare_head(got, ref)
+    assert decisions_clear(ref["max_prob"], m0, 0.95, 32)
+    rt, rm, rc = O.unmask(t0, m0, ref["argmax"], ref["max_prob"], 0.95, 32)
+    assert np.array_equal(tokens.cpu().numpy(), rt)
+    assert np.array_equal(masked.cpu().numpy(), rm)
+    assert int(out["n_committed"][0]) == int(np.sum(rc))
+
+
+def _teacher_forced(layers, xs, idxs, xf, ties_allowed):
+    """Every layer l: the oracle on the GPU's own input x_l and (where the
+    routing is a near-tie) the GPU's selection, against the GPU's output
+    x_(l+1). Returns the number of tokens whose routing was a near-tie."""
+    ties = 0
+    for l, layer in enumerate(layers):
+        L = layer_to_oracle(layer, lazy=True)
+        xh = xs[l].cpu().numpy()
+        ig = idxs[l].cpu().numpy()
+        free = O.moe_layer(xh, L, D.top_k, D.rms_eps)
+        ref = O.moe_layer(xh, L, D.top_k, D.rms_eps, force_idx=ig)
+        ties += compare_routing(ig, ref["w"], free, D.top_k)
+        g = (xs[l + 1] if l + 1 < len(xs) else xf).cpu().numpy()
+        ok, worst = hidden_close(g - xh, ref["x_out"] - xh)
+        assert ok, (l, worst)
+        ok, worst = hidden_close(g, ref["x_out"])
+        assert ok, (l, worst)
+    assert ties <= ties_allowed, ties
+    return ties
+
+
 def _compose_step(model, layers, ctx, tokens, masked, alpha=None, block=32):
     """The denoising step as separate entry-point calls; returns the inputs of
     every layer and its routing."""
@@ -121,7 +176,7 @@ def _compose_step(model, layers, ctx, tokens, masked, alpha=None, block=32):
     return xs, idxs, x, out
 
 
-def test_full_step_composition_and_sampled_layers(model):
+def test_full_step_composition_and_every_layer(model):
     M = 32
     ctx = synth.make_ctx(D, M, 5, DEV)
     cmodel = clover.Model(D, model["layers"], model["embed"], model["head"])
@@ -135,16 +190,8 @@ def test_full_step_composition_and_sampled_layers(model):
     # the step's own residual stream (each layer's combine deferred into the
     # next launch) equals the composition's, bit for bit
     assert torch.equal(clover.denoise_hidden(D, ws, M), xf)
-    # teacher-forced oracle checks of sampled layers
-    for l in (0, 19, 39):
-        L = layer_to_oracle(model["layers"][l], lazy=True)
-        xh = xs[l].cpu().numpy()
-        ref = O.moe_layer(xh, L, D.top_k, D.rms_eps, force_idx=idxs[l].cpu().numpy())
-        free = O.moe_layer(xh, L, D.top_k, D.rms_eps)
-        compare_routing(idxs[l].cpu().numpy(), ref["w"], free, D.top_k)
-        g = (xs[l + 1] if l + 1 < len(xs) else xf).cpu().numpy()
-        ok, worst = hidden_close(g - xh, ref["x_out"] - xh)
-        assert ok, (l, worst)
+    # every layer against the oracle under teacher forcing (40 x 32 tokens)
+    _teacher_forced(model["layers"], xs, idxs, xf, ties_allowed=40)
     # head statistics on the final residual stream
     z = O.head_logits(xf.cpu().numpy(), bits(model["head"]), D.rms_eps)
     ref = O.head_stats(z, D.mask_id)
@@ -185,6 +232,34 @@ def test_full_block_invariants(model):
     assert order == want
 
 
+def test_denoise_block_loop_entry_point(model):
+    """clover_denoise_block itself on one Clover block at logit scale 1: it
+    must run exactly 32 steps (one commit per step), leave no slot masked,
+    and leave every slot with the token it predicted at step 1. With a step
+    cap of 5 it stops early and reports NOT_CONVERGED with 27 slots left."""
+    M = 32
+    ctx = synth.make_ctx(D, M, 10, DEV)
+    cmodel = clover.Model(D, model["layers"], model["embed"], model["head"])
+    t2, m2 = synth.masked_block(D, M, DEV)
+    _, _, _, first = _compose_step(model, model["layers"], ctx, t2, m2)
+    torch.cuda.synchronize()
+    arg1 = first["argmax"].cpu().numpy()
+    ws = clover.workspace(clover.denoise_workspace_bytes(D, M))
+    tokens, masked = synth.masked_block(D, M, DEV)
+    steps = clover.denoise_block(cmodel, ctx, tokens, masked, block=32, max_steps=32, ws=ws)
+    clover.workspace_status(ws)
+    assert steps == 32
+    assert int(masked.sum()) == 0
+    assert np.array_equal(tokens.cpu().numpy(), arg1)
+    tokens, masked = synth.masked_block(D, M, DEV)
+    with pytest.raises(clover.CloverError) as ei:
+        clover.denoise_block(cmodel, ctx, tokens, masked, block=32, max_steps=5, ws=ws)
+    assert ei.value.code == clover.ERR_NOT_CONVERGED
+    assert int(masked.sum()) == 27
+    m = masked.cpu().numpy()
+    assert np.array_equal(tokens.cpu().numpy()[m == 0], arg1[m == 0])
+
+
 def test_batched_zipf_8_blocks(model):
     B, M = 8, 256
     layers = [synth.Layer(L.router_w, L.gate_up, L.down, L.sh_gate_up, L.sh_down,
@@ -199,8 +274,7 @@ def test_batched_zipf_8_blocks(model):
     assert torch.equal(t1, t2) and torch.equal(m1, m2)
     m = m1.cpu().numpy().reshape(B, 32)
     assert np.all(m.sum(axis=1) == 31)             # one commit per block
-    L = layer_to_oracle(layers[20], lazy=True)
-    xh = xs[20].cpu().numpy()
-    ref = O.moe_layer(xh, L, D.top_k, D.rms_eps, force_idx=idxs[20].cpu().numpy())
-    ok, worst = hidden_close(xs[21].cpu().numpy() - xh, ref["x_out"] - xh)
-    assert ok, worst
+    # every layer against the oracle under teacher forcing (40 x 256 tokens)
+    _teacher_forced(layers, xs, idxs, xf, ties_allowed=320)
+    counts = np.bincount(idxs[20].cpu().numpy().ravel(), minlength=D.n_experts)
+    assert counts.max() >= 100                     # hot experts carry a large share of the batch

@@ -36,6 +36,25 @@ def test_bf16_rounding_matches_torch():
     assert np.array_equal(got, want)
 
 
+def test_bf16_rounding_goes_through_float32():
+    """The oracle rounds a float64 value to bf16 in two steps, first to the
+    float32 the kernels hold and then to bf16, each to nearest even. The two
+    steps differ from one direct rounding only where the float32 step lands
+    exactly on a bf16 tie: 1 + 2^-8 + 2^-30 is above the tie between 1 and
+    1 + 2^-7, but its float32 rounding is the tie itself, which then goes to
+    the even neighbour 1. With 2^-20 instead of 2^-30 the excess survives in
+    float32 and the value rounds up."""
+    x = np.array([1.0 + 2.0 ** -8 + 2.0 ** -30, 1.0 + 2.0 ** -8 + 2.0 ** -20, -(1.0 + 2.0 ** -8 + 2.0 ** -30),
+                  1.0 + 3 * 2.0 ** -8 - 2.0 ** -31])
+    got = O.round_to_bf16(x)
+    assert got[0] == 1.0
+    assert got[1] == 1.0 + 2.0 ** -7
+    assert got[2] == -1.0
+    # 1 + 3 * 2^-8 is the tie between 1 + 2^-7 and 1 + 2^-6 (odd and even
+    # last bits); just below it float32 rounds onto the tie, which goes up
+    assert got[3] == 1.0 + 2.0 ** -6
+
+
 def test_bf16_decode_matches_torch():
     g = torch.Generator().manual_seed(2)
     t = torch.randn(10_000, generator=g).to(torch.bfloat16)
