@@ -66,6 +66,8 @@ WORKLOADS = {
               "2,048) into the untied 248,320-row head",
     "zipf": "batched and skewed routing: 8 blocks x 32 positions (256 tokens) through 40 Clover-shaped MoE "
             "layers + head, router biased to Zipf(1.2) expert popularity",
+    "zipf512": "batching beyond 8 blocks: 16 blocks x 32 positions (512 tokens) through 40 Clover-shaped MoE "
+               "layers + head, router biased to Zipf(1.2) expert popularity (hot experts take more than 256 tokens)",
     "coreset": "full block denoising step as 'step' with the block coreset expert selection (top_p 0.9) in every "
                "MoE layer",
     "int4": "full block denoising step as 'step' with every expert's weights in the 4-bit format (4-bit codes, one "
@@ -83,15 +85,16 @@ class Spec:
 
     def __init__(self, kind: str):
         self.kind = kind
-        self.n_pos = 256 if kind in ("zipf", "zipf_layer") else (M + 1 if kind == "accept" else M)
-        self.n_layers = {"step": D.n_layers, "zipf": D.n_layers, "coreset": D.n_layers, "int4": D.n_layers,
+        self.n_pos = {"zipf": 256, "zipf_layer": 256, "zipf512": 512, "accept": M + 1}.get(kind, M)
+        self.n_layers = {"step": D.n_layers, "zipf": D.n_layers, "zipf512": D.n_layers, "coreset": D.n_layers,
+                         "int4": D.n_layers,
                          "layer": 1, "zipf_layer": 1, "int4_layer": 1, "head": 0, "accept": 0}[kind]
         self.head_like = kind in ("head", "accept")
         self.one_layer = kind in ("layer", "zipf_layer", "int4_layer")
         self.q4 = kind in ("int4", "int4_layer")
-        self.full = kind in ("step", "zipf", "coreset", "int4")
+        self.full = kind in ("step", "zipf", "zipf512", "coreset", "int4")
         self.top_p = CORESET_TOP_P if kind == "coreset" else 0.0
-        self.zipf = 1.2 if kind in ("zipf", "zipf_layer") else None
+        self.zipf = 1.2 if kind in ("zipf", "zipf_layer", "zipf512") else None
 
 
 def base_config(kind: str, n_gpus: int) -> dict:
@@ -679,7 +682,8 @@ def run_ours(args):
     fused = n_pos <= 32
     per_layer = 1 if fused else 3         # fused layer kernel, or route + experts + combine
     if sp.full:
-        launches_per_step = 1 + per_layer * n_layers + (1 if fused else 0) + 2   # embed, layers, last combine, norm + head
+        # embed, layers, the last deferred combine, norm + one head launch per 256 positions
+        launches_per_step = 1 + per_layer * n_layers + (1 if fused else 0) + 1 + (n_pos + 255) // 256
     elif sp.one_layer:
         launches_per_step = per_layer
     else:

@@ -54,14 +54,22 @@ enum CtrlWord : int {
   kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
   kCtrlCommitted = 4,    // positions committed by the last head call
   kCtrlBarCount = 6,     // [u64, words 6-7] fused-layer grid barrier arrivals (only grows)
-  kCtrlTokenGroups = 8,  // [32] routing arrival counters (reset by their last CTA)
   kCtrlStamps = 40,      // [8 x u64] phase timestamps of the last fused-layer launch (diagnostics)
 };
 
 struct MoeLayout {
   size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, topk_p, rr_idx, rr_w, fin_w, logits,
-      xg, hbuf, yslot, bytes;
+      xg, hbuf, yslot, tg_ctr, bytes;
 };
+
+// Most units tables a call can need: the standalone expert kernel cuts each
+// expert's rows (and the shared expert's) into chunks of at most
+// kTileTokens, so there are at most E + ceil(M K / kTileTokens) routed chunks
+// and ceil(M / kTileTokens) shared ones.
+size_t max_chunks(const clover_dims& d, int M) {
+  const size_t MK = static_cast<size_t>(M) * d.top_k;
+  return d.n_experts + (MK + kTileTokens - 1) / kTileTokens + (M + kTileTokens - 1) / kTileTokens + 1;
+}
 
 MoeLayout moe_layout(const clover_dims& d, int M) {
   MoeLayout L;
@@ -73,12 +81,13 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
   };
   const size_t H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
   const size_t R = static_cast<size_t>(M) * K + M;
-  L.gu_done = take((E + 1) * 4);
+  const size_t NC = max_chunks(d, M);
+  L.gu_done = take(NC * 4);
   L.dn_done = take((H / 128) * 4);
   L.n_active = take(4);
-  L.act = take(E * 4);
-  L.cnt = take(E * 4);
-  L.off = take(E * 4);
+  L.act = take(NC * 4);
+  L.cnt = take(std::max(NC, E) * 4);
+  L.off = take(std::max(NC, E) * 4);
   L.tok_slot = take(M * K * 4);
   L.topk_idx = take(M * K * 4);
   L.topk_w = take(M * K * 4);
@@ -90,6 +99,7 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
   L.xg = take(R * H * 2);
   L.hbuf = take(R * F * 2);
   L.yslot = take(R * H * 4);
+  L.tg_ctr = take(((M + kRouteTileTokens - 1) / kRouteTileTokens) * 4);  // routing arrival counters (kept zero)
   L.bytes = o;
   return L;
 }
@@ -107,12 +117,13 @@ HeadLayout head_layout(const clover_dims& d, int M, bool accept = false) {
     o = align_up(o + b, 256);
     return r;
   };
+  const size_t ms = static_cast<size_t>(std::min(M, kTileTokens));  // positions of one head sub-call
   L.xn = take(static_cast<size_t>(M) * d.hidden * 2);
-  L.part_m = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
-  L.part_s = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
-  L.part_a = take(static_cast<size_t>(kHeadMaxCtas) * M * 4);
-  L.part_t = accept ? take(static_cast<size_t>(kHeadMaxCtas) * M * 4) : 0;
-  L.part_zd = accept ? take(static_cast<size_t>(kHeadMaxCtas) * M * 4) : 0;
+  L.part_m = take(static_cast<size_t>(kHeadMaxCtas) * ms * 4);
+  L.part_s = take(static_cast<size_t>(kHeadMaxCtas) * ms * 4);
+  L.part_a = take(static_cast<size_t>(kHeadMaxCtas) * ms * 4);
+  L.part_t = accept ? take(static_cast<size_t>(kHeadMaxCtas) * ms * 4) : 0;
+  L.part_zd = accept ? take(static_cast<size_t>(kHeadMaxCtas) * ms * 4) : 0;
   L.bytes = o;
   return L;
 }
@@ -329,7 +340,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     ra.bias = layer.router_bias;
     ra.logits = reinterpret_cast<float*>(data + L.logits);
     ra.xn_rows = xg + static_cast<size_t>(MK) * H;
-    ra.tg_ctr = ctrl + kCtrlTokenGroups;
+    ra.tg_ctr = reinterpret_cast<int*>(data + L.tg_ctr);
     ra.err = ctrl + kCtrlErr;
     ra.topk_idx = topk_idx;
     ra.topk_w = topk_w;
@@ -377,7 +388,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   }
   // B tiles move in boxes of up to 64 rows (one TMA instruction each), with
   // 16-row boxes for the rest; fewer, larger copies stream faster.
-  const int nb_rows = (M + 15) & ~15;
+  const int nb_rows = std::min((M + 15) & ~15, kTileTokens);
   if (fused) {  // the gate/up B operand is the dense block of normed rows
     const bf16* xn_rows = xg + static_cast<size_t>(MK) * H;
     if ((rc = encode_bf16_2d(&xa.tm_xg, xn_rows, M, H, 16, "normed rows"))) return rc;
@@ -416,7 +427,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.F = F;
   xa.E = E;
   xa.K = K;
-  const int nb = (M + 15) & ~15;
+  const int nb = std::min((M + 15) & ~15, kTileTokens);  // B-tile rows: one chunk at most
   // Two K groups per A/B stage (8 MMAs per pipeline step instead of 4) when
   // the token tile is small; 256-token tiles keep one group per stage. The
   // low-bit path, whose A stages are written by the converter warps rather
@@ -558,11 +569,20 @@ struct AcceptCfg {
   int32_t* out_tokens;
 };
 
+// Head statistics and the unmask rule (or the accept test) on M positions.
+// The positions are normalised once; the head kernel then takes them in
+// sub-calls of at most kTileTokens positions made of whole blocks (one
+// accumulator's width), each streaming the head once.
 int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, const float* alpha, float threshold,
                  int block, int32_t* tokens, uint8_t* masked, int32_t* argmax, float* max_logit, float* lse,
                  float* max_prob, int32_t* n_committed, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
                  cudaStream_t stream, const AcceptCfg* acc = nullptr) {
-  const HeadLayout L = head_layout(d, M, acc != nullptr);
+  const bool accept = acc != nullptr;
+  const HeadLayout L = head_layout(d, M, accept);
+  const int sub = M <= kTileTokens ? M : (kTileTokens / block) * block;
+  if (sub < 1)
+    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "block=%d: blocks wider than %d positions need M <= %d", block,
+                kTileTokens, kTileTokens);
   bf16* xn = reinterpret_cast<bf16*>(data + L.xn);
   NormArgs na;
   na.x = x;
@@ -573,62 +593,67 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
   cudaError_t e = launch_rmsnorm(na, stream, kPdl);
   if (e != cudaSuccess) return cuda_fail(e, "launch rmsnorm");
 
-  HeadArgs ha;
-  memset(&ha, 0, sizeof(ha));
   int rc;
-  if ((rc = encode_bf16_2d(&ha.tm_w, head_w, d.vocab, d.hidden, 128, "head"))) return rc;
-  // One box carries a K group of all positions (rows past M read as zeros).
-  const int nb = (M + 15) & ~15;
-  if ((rc = encode_bf16_2d(&ha.tm_x, xn, M, d.hidden, static_cast<uint32_t>(nb), "normed positions"))) return rc;
-  ha.x_box = nb;
-  ha.alpha = alpha;
-  ha.part_m = reinterpret_cast<float*>(data + L.part_m);
-  ha.part_s = reinterpret_cast<float*>(data + L.part_s);
-  ha.part_a = reinterpret_cast<int*>(data + L.part_a);
-  ha.done_ctr = ctrl + kCtrlHeadDone;
-  ha.tokens = tokens;
-  ha.masked = masked;
-  ha.argmax = argmax;
-  ha.max_logit = max_logit;
-  ha.lse = lse;
-  ha.max_prob = max_prob;
-  ha.n_committed = n_committed ? n_committed : ctrl + kCtrlCommitted;
-  ha.n_masked_left = ctrl + kCtrlMaskedLeft;
-  ha.err = err;
-  ha.M = M;
-  ha.H = d.hidden;
-  ha.V = d.vocab;
-  ha.mask_id = d.mask_id;
-  ha.block = block;
-  ha.n_tiles = (d.vocab + 127) / 128;
-  ha.threshold = threshold;
-  const bool accept = acc != nullptr;
-  if (accept) {
-    ha.draft = acc->draft;
-    ha.part_t = reinterpret_cast<float*>(data + L.part_t);
-    ha.part_zd = reinterpret_cast<float*>(data + L.part_zd);
-    ha.entropy = acc->entropy;
-    ha.p_draft = acc->p_draft;
-    ha.accept_len = acc->accept_len;
-    ha.out_tokens = acc->out_tokens;
-    ha.rule = acc->rule;
-    ha.ratio = acc->ratio;
-    ha.delta = acc->delta;
+  for (int p0 = 0; p0 < M; p0 += sub) {
+    const int m = std::min(sub, M - p0);
+    HeadArgs ha;
+    memset(&ha, 0, sizeof(ha));
+    if ((rc = encode_bf16_2d(&ha.tm_w, head_w, d.vocab, d.hidden, 128, "head"))) return rc;
+    // One box carries a K group of all positions (rows past m read as zeros).
+    const int nb = (m + 15) & ~15;
+    if ((rc = encode_bf16_2d(&ha.tm_x, xn + static_cast<size_t>(p0) * d.hidden, m, d.hidden, static_cast<uint32_t>(nb),
+                             "normed positions")))
+      return rc;
+    ha.x_box = nb;
+    ha.alpha = alpha ? alpha + p0 : nullptr;
+    ha.part_m = reinterpret_cast<float*>(data + L.part_m);
+    ha.part_s = reinterpret_cast<float*>(data + L.part_s);
+    ha.part_a = reinterpret_cast<int*>(data + L.part_a);
+    ha.done_ctr = ctrl + kCtrlHeadDone;
+    ha.tokens = tokens ? tokens + p0 : nullptr;
+    ha.masked = masked ? masked + p0 : nullptr;
+    ha.argmax = argmax ? argmax + p0 : nullptr;
+    ha.max_logit = max_logit ? max_logit + p0 : nullptr;
+    ha.lse = lse ? lse + p0 : nullptr;
+    ha.max_prob = max_prob ? max_prob + p0 : nullptr;
+    ha.n_committed = n_committed ? n_committed : ctrl + kCtrlCommitted;
+    ha.n_masked_left = ctrl + kCtrlMaskedLeft;
+    ha.accumulate = p0 > 0 ? 1 : 0;
+    ha.err = err;
+    ha.M = m;
+    ha.H = d.hidden;
+    ha.V = d.vocab;
+    ha.mask_id = d.mask_id;
+    ha.block = block;
+    ha.n_tiles = (d.vocab + 127) / 128;
+    ha.threshold = threshold;
+    if (accept) {
+      ha.draft = acc->draft + p0;
+      ha.part_t = reinterpret_cast<float*>(data + L.part_t);
+      ha.part_zd = reinterpret_cast<float*>(data + L.part_zd);
+      ha.entropy = acc->entropy ? acc->entropy + p0 : nullptr;
+      ha.p_draft = acc->p_draft ? acc->p_draft + p0 : nullptr;
+      ha.accept_len = acc->accept_len + p0 / block;
+      ha.out_tokens = acc->out_tokens + p0;
+      ha.rule = acc->rule;
+      ha.ratio = acc->ratio;
+      ha.delta = acc->delta;
+    }
+    // Two K groups per stage at up to 64 positions (half the pipeline steps);
+    // 8 groups of weights (128 KiB) in flight per SM streamed best on GB300.
+    const int kg = (nb <= 64 && (d.hidden / 64) % 2 == 0) ? 2 : 1;
+    ha.kg = kg;
+    const size_t fixed = head_smem_bytes(0, nb, accept, kg) + 16 * 2 * 8;
+    ha.stages = static_cast<int>(std::min<size_t>(
+        8 / kg, (static_cast<size_t>(kSmemBudget) - fixed) / (kg * (kATileBytes + static_cast<size_t>(nb) * 128))));
+    const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
+    // The final merge reuses the ring for 12 (accept: 20) bytes x 32 positions x grid.
+    if (ha.stages < 1 || static_cast<size_t>(ha.stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) <
+                             static_cast<size_t>(grid) * 32 * (accept ? 20 : 12))
+      return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
+    e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept, kg), stream, kPdl);
+    if (e != cudaSuccess) return cuda_fail(e, "launch head");
   }
-  // Two K groups per stage at up to 64 positions (half the pipeline steps);
-  // 8 groups of weights (128 KiB) in flight per SM streamed best on GB300.
-  const int kg = (nb <= 64 && (d.hidden / 64) % 2 == 0) ? 2 : 1;
-  ha.kg = kg;
-  const size_t fixed = head_smem_bytes(0, nb, accept, kg) + 16 * 2 * 8;
-  ha.stages = static_cast<int>(std::min<size_t>(
-      8 / kg, (static_cast<size_t>(kSmemBudget) - fixed) / (kg * (kATileBytes + static_cast<size_t>(nb) * 128))));
-  const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
-  // The final merge reuses the ring for 12 (accept: 20) bytes x 32 positions x grid.
-  if (ha.stages < 1 || static_cast<size_t>(ha.stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) <
-                           static_cast<size_t>(grid) * 32 * (accept ? 20 : 12))
-    return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
-  e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept, kg), stream, kPdl);
-  if (e != cudaSuccess) return cuda_fail(e, "launch head");
   return CLOVER_OK;
 }
 
@@ -909,7 +934,7 @@ int clover_denoise_block(const clover_dims* dims, const clover_moe_layer* layers
   if ((rc = check_tokens(M))) return rc;
   if (masked == nullptr) return fail(CLOVER_ERR_INVALID_ARG, "masked is NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t host_masked[kMaxTokens];
+  uint8_t host_masked[kMaxTokens];  // M <= kMaxTokens (checked above)
   cudaError_t e = cudaMemcpyAsync(host_masked, masked, M, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "reading the mask");

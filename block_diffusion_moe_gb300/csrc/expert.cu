@@ -56,24 +56,25 @@ constexpr int kUnitAbort = -2;
 
 struct Unit {
   int kind;   // 0 gate/up, 1 down
-  int a;      // active-expert index; 0 is the shared expert
+  int a;      // index of the active expert (fused kernel; 0 is the shared expert) or chunk (standalone)
   int e;      // expert id (E for the shared expert)
   int slice;  // F/64 slice (gate/up) or H/128 slice (down)
-  int cnt;    // tokens routed to the expert
-  int off;    // first row of the expert in the gathered buffers
+  int cnt;    // tokens of the expert (chunk)
+  int off;    // first row of the expert (chunk) in the gathered buffers
 };
 
-// Where a launch finds its routing: global tables written by k_perm
-// (k_expert) or shared-memory tables built by the launch itself (k_layer).
+// Where a launch finds its routing: global tables written in the prologue
+// of k_expert, or shared-memory tables built by k_layer itself.
 struct Rt {
-  const int* act;           // active routed expert ids (standalone kernel: heaviest first)
-  const int* cnt;           // [E] tokens per expert
-  const int* off;           // [E] first row per expert
+  const int* act;           // fused: active routed expert ids; standalone: expert id of each chunk
+  const int* cnt;           // fused: [E] tokens per expert; standalone: rows of each chunk
+  const int* off;           // fused: [E] first row per expert; standalone: first row of each chunk
   const uint32_t* mask;     // [E] token bitmask (dense mode)
   const int32_t* tok_slot;  // [M][K] row of each selection
   const float* topk_w;      // [M][K] weight of each selection
-  int n_exp;                // active routed experts + the shared expert
+  int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
   int dense;                // gate/up B operand = all M normed rows
+  int chunked;              // standalone: units index chunks of at most kTileTokens rows
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArgs& p) {
@@ -90,7 +91,11 @@ __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArg
     w.a = v / SH;
     w.slice = v - w.a * SH;
   }
-  if (w.a == 0) {
+  if (rt.chunked) {
+    w.e = rt.act[w.a];
+    w.cnt = rt.cnt[w.a];
+    w.off = rt.off[w.a];
+  } else if (w.a == 0) {
     w.e = p.E;
     w.cnt = p.M;
     w.off = p.M * p.K;
@@ -238,12 +243,12 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
     const CUtensorMap* m;
     int row, nk;
     if (w.kind == 0) {
-      m = (w.a == 0) ? &p.tm_sgu : &p.tm_gu;
-      row = (w.a == 0 ? 0 : w.e * 2 * p.F) + w.slice * 64;
+      m = (w.e == p.E) ? &p.tm_sgu : &p.tm_gu;
+      row = (w.e == p.E ? 0 : w.e * 2 * p.F) + w.slice * 64;
       nk = p.H >> 6;
     } else {
-      m = (w.a == 0) ? &p.tm_sdn : &p.tm_dn;
-      row = (w.a == 0 ? 0 : w.e * p.H) + w.slice * 128;
+      m = (w.e == p.E) ? &p.tm_sdn : &p.tm_dn;
+      row = (w.e == p.E ? 0 : w.e * p.H) + w.slice * 128;
       nk = p.F >> 6;
     }
     const int kq = kQ4 ? unit_kq(w, p) : 1;
@@ -266,19 +271,19 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
         mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(kq * kQGroupBytes));
         const uint32_t sdst = dst + kq * 4096;
         if (w.kind == 0) {
-          const CUtensorMap* mq = (w.a == 0) ? &p.tm_sgu_q : &p.tm_gu_q;
+          const CUtensorMap* mq = (w.e == p.E) ? &p.tm_sgu_q : &p.tm_gu_q;
           tma_load_2d(dst, mq, &full[sa], kc * 32, row, pol);
           tma_load_2d(dst + kq * 2048, mq, &full[sa], kc * 32, row + p.F, pol);
-          const uint16_t* sc = (w.a == 0 ? p.sgu_s : p.gu_s + static_cast<size_t>(w.e) * (p.H >> 6) * 2 * p.F) +
+          const uint16_t* sc = (w.e == p.E ? p.sgu_s : p.gu_s + static_cast<size_t>(w.e) * (p.H >> 6) * 2 * p.F) +
                                static_cast<size_t>(kc) * 2 * p.F + w.slice * 64;
           for (int g = 0; g < kq; ++g) {
             bulk_load(sdst + g * 256, sc + static_cast<size_t>(g) * 2 * p.F, 128, &full[sa]);
             bulk_load(sdst + g * 256 + 128, sc + static_cast<size_t>(g) * 2 * p.F + p.F, 128, &full[sa]);
           }
         } else {
-          const CUtensorMap* mq = (w.a == 0) ? &p.tm_sdn_q : &p.tm_dn_q;
+          const CUtensorMap* mq = (w.e == p.E) ? &p.tm_sdn_q : &p.tm_dn_q;
           tma_load_2d(dst, mq, &full[sa], kc * 32, row, pol);
-          const uint16_t* sc = (w.a == 0 ? p.sdn_s : p.dn_s + static_cast<size_t>(w.e) * (p.F >> 6) * p.H) +
+          const uint16_t* sc = (w.e == p.E ? p.sdn_s : p.dn_s + static_cast<size_t>(w.e) * (p.F >> 6) * p.H) +
                                static_cast<size_t>(kc) * p.H + w.slice * 128;
           for (int g = 0; g < kq; ++g) bulk_load(sdst + g * 256, sc + static_cast<size_t>(g) * p.H, 256, &full[sa]);
         }
@@ -716,7 +721,7 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
       bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + w.slice * 64 + r64;
       float* x_up = s.xch;              // [64][20] up values of columns 0..15
       float* x_gate = s.xch + 64 * 20;  // [64][20] gate values of columns 16..31
-      const uint32_t tm = (rt.dense && w.a != 0) ? rt.mask[w.e] : 0xffffffffu;
+      const uint32_t tm = (rt.dense && w.e != p.E) ? rt.mask[w.e] : 0xffffffffu;
       for (int c0 = 0; c0 < n; c0 += 32) {
         float v[32];
         __syncwarp();
@@ -758,7 +763,7 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
           bool keep = c < w.cnt;
           if (rt.dense) {
             keep = c < p.M && ((tm >> c) & 1u);
-            slot = (w.a == 0) ? c : __popc(tm & ((1u << c) - 1u));
+            slot = (w.e == p.E) ? c : __popc(tm & ((1u << c) - 1u));
           }
           if (keep) hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(hv[j]);
         }
@@ -940,29 +945,49 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pt.off = reinterpret_cast<int*>(pt.bm + E * (kMaxTokens / 32));
   pt.cnt = pt.off + E;
   pt.tmp = pt.cnt + E;
+  int* by_rank = pt.tmp + 32;  // [E] active expert ids, heaviest first
   const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
   const int tid = threadIdx.x;
   if (blockIdx.x == 0) {
+    // Unit tables: the expert's tokens in chunks of at most kTileTokens rows
+    // (one accumulator's width): the shared expert's chunks first, then the
+    // routed experts heaviest first (ties: lower id first), so that the
+    // longest units are handed out first and do not end the launch; an
+    // expert's chunks are adjacent, so its weight tiles are asked for at
+    // nearly the same time by the CTAs that take them.
+    const int n_sh = (M + kTileTokens - 1) / kTileTokens;
     if (tid < E) {
       const int c = pt.cnt[tid];
-      p.cnt[tid] = c;
-      p.off[tid] = pt.off[tid];
       if (c > 0) {
-        // Active experts heaviest first (ties: lower id first), so that the
-        // longest units are handed out first and do not end the launch.
         int rank = 0;
         for (int j = 0; j < E; ++j) {
           const int cj = pt.cnt[j];
           rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
         }
-        p.act[rank] = tid;
+        by_rank[rank] = tid;
       }
     }
+    if (tid < n_sh) {
+      p.act[tid] = E;
+      p.off[tid] = MK + tid * kTileTokens;
+      p.cnt[tid] = min(kTileTokens, M - tid * kTileTokens);
+    }
+    __syncthreads();
+    const int e = tid < n_act ? by_rank[tid] : 0;
+    const int ce = tid < n_act ? pt.cnt[e] : 0;
+    const int nch = (ce + kTileTokens - 1) / kTileTokens;
+    int n_chunks = 0;
+    const int first = n_sh + block_excl_scan(nch, pt.tmp, &n_chunks);
+    for (int c = 0; c < nch; ++c) {
+      p.act[first + c] = e;
+      p.off[first + c] = pt.off[e] + c * kTileTokens;
+      p.cnt[first + c] = min(kTileTokens, ce - c * kTileTokens);
+    }
     if (tid == 0) {
-      *p.n_active = n_act;
+      *p.n_active = n_sh + n_chunks;
       *p.unit_ctr = 0;
     }
-    for (int i = tid; i <= E; i += blockDim.x) p.gu_done[i] = 0;
+    for (int i = tid; i < n_sh + n_chunks; i += blockDim.x) p.gu_done[i] = 0;
     for (int i = tid; i < (p.H >> 7); i += blockDim.x) p.dn_done[i] = 0;
     if (p.out_idx)
       for (int i = tid; i < MK; i += blockDim.x) p.out_idx[i] = pt.idx[i];
@@ -1003,8 +1028,9 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.mask = nullptr;
   rt.tok_slot = p.tok_slot;
   rt.topk_w = p.topk_w;
-  rt.n_exp = ok ? __ldcg(p.n_active) + 1 : 0;  // after a failed barrier no unit runs
+  rt.n_exp = ok ? __ldcg(p.n_active) : 0;  // after a failed barrier no unit runs
   rt.dense = 0;
+  rt.chunked = 1;
   expert_roles<kQ4>(p, s, rt, tmem_base);
 }
 
@@ -1310,6 +1336,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.topk_w = s_w;
   rt.n_exp = (*s.abort) ? 0 : *s_nact + 1;  // after a failed barrier no unit runs
   rt.dense = 1;
+  rt.chunked = 0;
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
   if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
@@ -1327,7 +1354,7 @@ size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int
 // coreset mass, sorted mass, sorted id [E] each; the active count and the
 // coreset's allowed-set words.
 size_t perm_smem_bytes(int M, int K, int E) {
-  return static_cast<size_t>(2 * M * K + E * (kMaxTokens / 32) + 2 * E + 17) * 4;
+  return static_cast<size_t>(2 * M * K + E * (kMaxTokens / 32) + 2 * E + 32 + E) * 4;
 }
 
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }

@@ -236,7 +236,7 @@ __device__ void head_mma(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t 
 // out of the transposed tile.
 template <bool kAccept>
 __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint32_t tmem_base) {
-  constexpr int kMaxChunks = kMaxTokens / 32;
+  constexpr int kMaxChunks = kTileTokens / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;
   const int row = q * 32 + lane;
@@ -518,8 +518,8 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   }
   named_bar_sync(1, 128);
   if (etid == 0) {
-    if (p.n_committed) *p.n_committed = s.s_counts[0];
-    if (p.n_masked_left) *p.n_masked_left = s.s_counts[1];
+    if (p.n_committed) *p.n_committed = (p.accumulate ? *p.n_committed : 0) + s.s_counts[0];
+    if (p.n_masked_left) *p.n_masked_left = (p.accumulate ? *p.n_masked_left : 0) + s.s_counts[1];
     *p.done_ctr = 0;
   }
 }

@@ -19,7 +19,11 @@ constexpr int kRouteTokens = 8;
 constexpr int kRouteTileTokens = 16;
 constexpr int kRouteTileExperts = 32;
 constexpr int kRouteChunk = 2048;
-constexpr int kMaxTokens = 256;
+// Tokens per call, and per token tile: an expert's tokens and the head's
+// positions are processed in tiles of at most kTileTokens (the N side of a
+// tcgen05.mma and of one TMEM accumulator).
+constexpr int kMaxTokens = 1024;
+constexpr int kTileTokens = 256;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 
@@ -180,6 +184,7 @@ struct HeadArgs {
   int* n_masked_left;  // scalar out (nullable)
   int* err;
   int M, H, V, mask_id, block, n_tiles, stages;
+  int accumulate;  // 1: add this call's counts to *n_committed / *n_masked_left (a later sub-call of a split call)
   int kg;     // K groups of 64 per pipeline stage (1 or 2)
   int x_box;  // rows per TMA box of the normed positions (a multiple of 16)
   float threshold;

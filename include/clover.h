@@ -28,9 +28,13 @@
  *     records a flag in the workspace and the kernel returns;
  *     clover_workspace_status() reports it as CLOVER_ERR_DEVICE_TIMEOUT.
  *   - Shapes: hidden % 128 == 0, d_ff % 64 == 0, 1 <= top_k <= 32,
- *     top_k <= n_experts <= 256, hidden <= 8192, 1 <= tokens <= 256, vocab >= 2,
- *     0 <= mask_id < vocab. Other shapes return CLOVER_ERR_UNSUPPORTED_SHAPE;
- *     there is no fallback path.
+ *     top_k <= n_experts <= 256, hidden <= 8192, 1 <= tokens <= 1024,
+ *     vocab >= 2, 0 <= mask_id < vocab. Other shapes return
+ *     CLOVER_ERR_UNSUPPORTED_SHAPE; there is no fallback path. Tokens are
+ *     processed in tiles of at most 256: an expert that more than 256 tokens
+ *     select is streamed once per tile of its tokens (the tiles run side by
+ *     side, so the repeat reads mostly come from L2), and the head streams
+ *     once per 256 positions.
  */
 #ifndef CLOVER_H_
 #define CLOVER_H_
@@ -113,7 +117,8 @@ size_t clover_moe_workspace_bytes(const clover_dims* dims, int32_t max_tokens);
  * x_in, x_out: fp32 [M][H]; x_out may equal x_in (in place), other overlap is
  * not allowed. topk_idx (int32 [M][K]) and topk_w (fp32 [M][K]) receive the
  * selection in descending probability order; either may be NULL.
- * Each selected expert's weights are read from HBM once per call. */
+ * Each selected expert's weights are read from HBM once per call (once per
+ * tile of 256 of its tokens when more than 256 tokens select it). */
 int clover_moe_block_step(const clover_dims* dims, const clover_moe_layer* layer,
                           const float* x_in, float* x_out,
                           int32_t* topk_idx, float* topk_w, int32_t M,
@@ -151,7 +156,8 @@ size_t clover_head_workspace_bytes(const clover_dims* dims, int32_t max_tokens);
  * NULL (= 1). tokens int32 [M], masked uint8 [M]: in/out. argmax int32 [M],
  * max_logit, lse, max_prob fp32 [M]: out. n_committed: device int32 scalar,
  * out (number committed by this call). M % block == 0 is not required; the
- * last group may be shorter. A committed slot (masked_p == 0) whose token id
+ * last group may be shorter. Above 256 positions, block must be at most 256
+ * (the head then runs on whole blocks, at most 256 positions at a time). A committed slot (masked_p == 0) whose token id
  * lies outside [0, V) is left as it is and reported through the workspace
  * status word (clover_workspace_status). */
 int clover_lmhead_unmask(const clover_dims* dims, const uint16_t* head_w, const float* x,

@@ -64,7 +64,8 @@ def test_workspace_sizes(lib):
     dn = lib.clover_denoise_workspace_bytes(ctypes.byref(d), 32)
     assert dn >= m32 + h - 2 * 256
     assert lib.clover_moe_workspace_bytes(ctypes.byref(d), 0) == 0
-    assert lib.clover_moe_workspace_bytes(ctypes.byref(d), 257) == 0
+    assert lib.clover_moe_workspace_bytes(ctypes.byref(d), 1025) == 0
+    assert lib.clover_moe_workspace_bytes(ctypes.byref(d), 1024) > m256
     assert lib.clover_moe_workspace_bytes(None, 32) == 0
     # the residual stream the denoise step leaves: an fp32 [M][H] block that
     # lies inside the workspace for every M up to the size it was built for
@@ -167,7 +168,7 @@ def test_accept_arg_checks(lib):
     need = lib.clover_accept_workspace_bytes(ctypes.byref(d), 33)
     assert need > lib.clover_head_workspace_bytes(ctypes.byref(d), 33)
     assert lib.clover_accept_workspace_bytes(ctypes.byref(d), 0) == 0
-    assert lib.clover_accept_workspace_bytes(ctypes.byref(d), 257) == 0
+    assert lib.clover_accept_workspace_bytes(ctypes.byref(d), 1025) == 0
     f = lib.clover_lmhead_accept
     #      dims          head_w   x        scale draft   rule ratio delta block
     base = [ctypes.byref(d), 0x10000, 0x20000, None, 0x30000, 1, 0.9, 0.6, 33,
@@ -188,5 +189,5 @@ def test_accept_arg_checks(lib):
     assert call(delta=float("inf")) == C.ERR_INVALID_ARG
     assert call(draft=None) == C.ERR_INVALID_ARG
     assert call(accept_len=None) == C.ERR_INVALID_ARG
-    assert call(M=300, block=30) == C.ERR_UNSUPPORTED_SHAPE
+    assert call(M=1100, block=50) == C.ERR_UNSUPPORTED_SHAPE
     assert call(ws_bytes=need - 1) == C.ERR_WORKSPACE_TOO_SMALL

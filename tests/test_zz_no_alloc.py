@@ -122,6 +122,6 @@ def test_static_call_checks_arguments_before_any_cuda_call():
     assert f(ctypes.byref(dims), 0x10000, 0x20000, None, 0.95, 0, 0x30000, 0x40000, None, None, None, None, None,
              32, None) == clover.ERR_INVALID_ARG
     assert f(ctypes.byref(dims), 0x10000, 0x20000, None, 0.95, 32, 0x30000, 0x40000, None, None, None, None, None,
-             300, None) == clover.ERR_UNSUPPORTED_SHAPE
+             1100, None) == clover.ERR_UNSUPPORTED_SHAPE
     assert f(ctypes.byref(dims), 0x10000, 0x20000, None, 0.95, 32, 0x30000, 0x40000, None, None, None, None, None,
              103, None) == clover.ERR_WORKSPACE_TOO_SMALL
