@@ -53,13 +53,14 @@ enum CtrlWord : int {
   kCtrlMaskedLeft = 2,   // positions still masked after the last head call
   kCtrlHeadDone = 3,     // head kernel arrival counter (reset by its last CTA)
   kCtrlCommitted = 4,    // positions committed by the last head call
+  kCtrlExitCtr = 5,      // expert kernel CTAs that finished (reset by the last one)
   kCtrlBarCount = 6,     // [u64, words 6-7] fused-layer grid barrier arrivals (only grows)
   kCtrlStamps = 40,      // [8 x u64] phase timestamps of the last fused-layer launch (diagnostics)
 };
 
 struct MoeLayout {
   size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, topk_p, rr_idx, rr_w, fin_w, logits,
-      xg, hbuf, yslot, tg_ctr, bytes;
+      xg, hbuf, yslot, tg_ctr, gathered, bytes;
 };
 
 // Most units tables a call can need: the standalone expert kernel cuts each
@@ -100,6 +101,7 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
   L.hbuf = take(R * F * 2);
   L.yslot = take(R * H * 4);
   L.tg_ctr = take(((M + kRouteTileTokens - 1) / kRouteTileTokens) * 4);  // routing arrival counters (kept zero)
+  L.gathered = take(NC * 4);  // rows gathered per chunk (reset by the last CTA of each launch)
   L.bytes = o;
   return L;
 }
@@ -328,6 +330,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   float* topk_w = reinterpret_cast<float*>(data + L.topk_w);
 
   const bool fused = plan::moe_fused(M, E, plan.sms);
+  const int n_chunks = static_cast<int>(max_chunks(d, M));
   if ((defer || pend) && (!fused || x_in != x_out))
     return fail(CLOVER_ERR_INVALID_ARG, "a deferred combine needs the fused layer kernel working in place");
   if (d.coreset_top_p > 0.f && !fused)
@@ -421,6 +424,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.unit_ctr = ctrl + kCtrlUnitCtr;
   xa.gu_done = reinterpret_cast<int*>(data + L.gu_done);
   xa.dn_done = reinterpret_cast<int*>(data + L.dn_done);
+  xa.gathered = reinterpret_cast<int*>(data + L.gathered);
+  xa.exit_ctr = ctrl + kCtrlExitCtr;
+  xa.max_chunks = n_chunks;
   xa.err = err;
   xa.M = M;
   xa.H = H;
@@ -441,8 +447,8 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.kg_stage = kg;
   const size_t a_stage = static_cast<size_t>(kg) * kATileBytes;
   const size_t b_stage = static_cast<size_t>(kg) * nb * 128;
-  const size_t fixed = expert_smem_bytes(0, 0, 0, nb, 0, kg) + static_cast<size_t>(4 * 16) * 8 +
-                       (fused ? layer_rt_bytes(M, K, E) : 0);
+  const size_t tables = fused ? layer_rt_bytes(M, K, E) : expert_tables_bytes(M, K, n_chunks);
+  const size_t fixed = expert_smem_bytes(0, 0, 0, nb, 0, kg) + static_cast<size_t>(4 * 16) * 8 + tables;
   const size_t budget = static_cast<size_t>(kSmemBudget) - fixed;
   int sa, sb, sq = 0;
   if (q4) {
@@ -505,10 +511,11 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
 #else
     xa.stamps = nullptr;
 #endif
-    smem += layer_rt_bytes(M, K, E);
   }
-  // Every CTA of the persistent kernel waits at grid barriers, so the whole
-  // grid must be resident at once: check it before launching.
+  smem += tables;
+  // Every CTA of the persistent kernel waits on other CTAs (grid barriers,
+  // the chunk and unit counters), so the whole grid must be resident at
+  // once: check it before launching.
   int resident = 0;
   if ((rc = resident_per_sm(fused, q4, smem, &resident))) return rc;
   const int grid = plan::persistent_grid(plan.sms, resident);
@@ -796,11 +803,12 @@ int workspace_status_impl(void* workspace, size_t workspace_bytes, clover_stream
   // left behind, so the workspace is usable again.
   e = cudaMemset(workspace, 0, kCtrlBytes);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace status");
-  char what[160] = {0};
-  snprintf(what, sizeof(what), "%s%s%s%s", (word & kErrMbarTimeout) ? "pipeline wait timed out; " : "",
+  char what[200] = {0};
+  snprintf(what, sizeof(what), "%s%s%s%s%s", (word & kErrMbarTimeout) ? "pipeline wait timed out; " : "",
            (word & kErrDepTimeout) ? "cross-CTA dependency wait timed out; " : "",
            (word & kErrBadToken) ? "token id out of range; " : "",
-           (word & kErrBadRoute) ? "expert id out of range; " : "");
+           (word & kErrBadRoute) ? "expert id out of range; " : "",
+           (word & kErrState) ? "work counters inconsistent (workspace changed between calls?); " : "");
   return fail(CLOVER_ERR_DEVICE_TIMEOUT, "device status 0x%x: %s", word, what);
 }
 }  // namespace clover

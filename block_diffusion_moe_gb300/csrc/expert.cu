@@ -215,6 +215,10 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
     // A CTA that gave up (n_total == 0) draws no unit, so it never takes
     // work away from the others.
     int u = n_total > 0 ? atomicAdd(p.unit_ctr, 1) : n_total;
+    if (u < 0) {  // a counter left negative: take no unit, report it
+      atomicOr(p.err, kErrState);
+      u = n_total;
+    }
     if (u >= n_total) {
       u = kUnitEnd;
       if (p.wr_next != nullptr) {
@@ -455,6 +459,26 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       mb = &p.tm_xg_big;
       box = p.xg_box;
       nk = p.H >> 6;
+      if (rt.chunked && w.e != p.E) {
+        // The chunk's token rows are gathered by the CTAs' spare warps at
+        // the start of the launch: wait (bounded) until all of them are in.
+        const unsigned long long t0 = global_ns();
+        bool ok = true;
+        while (ld_acquire_gpu(&p.gathered[w.a]) < w.cnt) {
+          if (*s.abort) {
+            ok = false;
+            break;
+          }
+          if (global_ns() - t0 > kWaitLimitNs) {
+            raise_abort(s, p.err, kErrDepTimeout);
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+        if (!ok) break;
+        fence_proxy_async_global();
+      }
     } else {
       m = &p.tm_h;
       mb = &p.tm_h_big;
@@ -925,6 +949,81 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 
 }  // namespace
 
+// Copies the normed rows of the routed chunks' tokens into expert order
+// (row r of the gathered buffer = normed row of token row_tok[r]). Work is
+// cut into pieces of four rows; piece q of chunk a belongs to CTA
+// (7 a + q) mod G, so every CTA takes a share of the hottest chunks first.
+// After a piece's rows are stored, the chunk's counter grows by its rows
+// (release); a gate/up unit of the chunk loads them once the counter reaches
+// the chunk's row count. Run by n_thr threads of the CTA (named barrier bar).
+__device__ void gather_chunks(const ExpertArgs& p, const Rt& rt, const uint16_t* row_tok, int n_thr, int tid,
+                              uint32_t bar) {
+  const int G = gridDim.x;
+  const int per_row = p.H / 8;  // 16-byte pieces per row
+  for (int a = 0; a < rt.n_exp; ++a) {
+    if (rt.act[a] == p.E) continue;  // the shared expert reads the normed rows in place
+    const int off = rt.off[a], cnt = rt.cnt[a];
+    const int n_q = (cnt + 3) >> 2;
+    for (int q = static_cast<int>((static_cast<unsigned>(G) - (7u * a) % G + blockIdx.x) % G); q < n_q; q += G) {
+      const int r0 = q * 4, nr = min(4, cnt - r0);
+      const int span = nr * per_row;
+      for (int i0 = tid; i0 < span; i0 += 4 * n_thr) {
+        uint4 v[4];
+        int dst[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * n_thr;
+          dst[j] = -1;
+          if (i < span) {
+            const int rr = i / per_row, c = i - rr * per_row;
+            const int r = off + r0 + rr;
+            v[j] = __ldcg(reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(row_tok[r]) * p.H) + c);
+            dst[j] = r * per_row + c;
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (dst[j] >= 0) reinterpret_cast<uint4*>(p.xg)[dst[j]] = v[j];
+      }
+      fence_proxy_async_global();  // the rows are read by TMA
+      __threadfence();
+      named_bar_sync(bar, n_thr);
+      if (tid == 0) red_release_gpu_add(&p.gathered[a], nr);
+    }
+  }
+}
+
+// Every CTA calls this last. The CTA that finishes last resets the unit
+// counter and the per-unit-table counters the launch used, so that the next
+// launch on the workspace finds them at zero without a barrier of its own
+// (the next kernel reads them only after its dependency wait, which sees
+// this grid complete). A clean launch leaves the unit counter at n_total
+// plus one failed draw per CTA; anything else (units skipped or never
+// drawn) is reported.
+__device__ void exit_reset(const ExpertArgs& p, int n_entries, int n_total, bool gathered) {
+  __shared__ int s_lastx;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(p.exit_ctr, 1);
+    s_lastx = (old == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (s_lastx) {
+    __threadfence();
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
+      p.gu_done[i] = 0;
+      if (gathered) p.gathered[i] = 0;
+    }
+    if (threadIdx.x == 0) {
+      if (n_total > 0 && *reinterpret_cast<volatile int*>(p.unit_ctr) != n_total + static_cast<int>(gridDim.x))
+        atomicOr(p.err, kErrState);
+      *p.unit_ctr = 0;
+      *p.exit_ctr = 0;
+    }
+  }
+}
+
 template <bool kQ4>
 __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     k_expert(const __grid_constant__ ExpertArgs p) {
@@ -934,104 +1033,87 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pdl_wait();
   pdl_trigger();
   const int M = p.M, K = p.K, E = p.E, MK = M * K;
-  // Every CTA builds the same permutation of the routing kernel's top-k in
-  // the (still idle) weight ring; CTA 0 publishes the unit tables; every
-  // CTA gathers its share of the normed rows into expert order; one grid
-  // barrier, then the units.
+  // Every CTA builds the same permutation of the routing kernel's top-k (its
+  // scratch in the still idle weight ring) and keeps the token of every row
+  // and the unit tables in its own shared memory, so no CTA waits for
+  // another before its units: the weight stream starts right after the
+  // permutation, while the spare warps gather the token rows chunk by chunk
+  // and each gate/up unit waits only for its own chunk's rows.
+  uint16_t* row_tok = reinterpret_cast<uint16_t*>(s.rt_region);
+  const int NC = p.max_chunks;
+  int* c_act = reinterpret_cast<int*>(s.rt_region + ((2 * MK + 15) & ~15));
+  int* c_off = c_act + NC;
+  int* c_cnt = c_off + NC;
   PermTables pt;
   pt.idx = reinterpret_cast<int*>(s.a_ring);
-  pt.row_tok = pt.idx + MK;
-  pt.bm = reinterpret_cast<uint32_t*>(pt.row_tok + MK);
+  pt.row_tok = row_tok;
+  pt.bm = reinterpret_cast<uint32_t*>(pt.idx + MK);
   pt.off = reinterpret_cast<int*>(pt.bm + E * (kMaxTokens / 32));
   pt.cnt = pt.off + E;
   pt.tmp = pt.cnt + E;
   int* by_rank = pt.tmp + 32;  // [E] active expert ids, heaviest first
   const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
   const int tid = threadIdx.x;
-  if (blockIdx.x == 0) {
-    // Unit tables: the expert's tokens in chunks of at most kTileTokens rows
-    // (one accumulator's width): the shared expert's chunks first, then the
-    // routed experts heaviest first (ties: lower id first), so that the
-    // longest units are handed out first and do not end the launch; an
-    // expert's chunks are adjacent, so its weight tiles are asked for at
-    // nearly the same time by the CTAs that take them.
-    const int n_sh = (M + kTileTokens - 1) / kTileTokens;
-    if (tid < E) {
-      const int c = pt.cnt[tid];
-      if (c > 0) {
-        int rank = 0;
-        for (int j = 0; j < E; ++j) {
-          const int cj = pt.cnt[j];
-          rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
-        }
-        by_rank[rank] = tid;
+  // Unit tables: the expert's tokens in chunks of at most kTileTokens rows
+  // (one accumulator's width): the shared expert's chunks first, then the
+  // routed experts heaviest first (ties: lower id first), so that the
+  // longest units are handed out first and do not end the launch; an
+  // expert's chunks are adjacent, so its weight tiles are asked for at
+  // nearly the same time by the CTAs that take them.
+  const int n_sh = (M + kTileTokens - 1) / kTileTokens;
+  if (tid < E) {
+    const int c = pt.cnt[tid];
+    if (c > 0) {
+      int rank = 0;
+      for (int j = 0; j < E; ++j) {
+        const int cj = pt.cnt[j];
+        rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
       }
+      by_rank[rank] = tid;
     }
-    if (tid < n_sh) {
-      p.act[tid] = E;
-      p.off[tid] = MK + tid * kTileTokens;
-      p.cnt[tid] = min(kTileTokens, M - tid * kTileTokens);
-    }
-    __syncthreads();
-    const int e = tid < n_act ? by_rank[tid] : 0;
-    const int ce = tid < n_act ? pt.cnt[e] : 0;
-    const int nch = (ce + kTileTokens - 1) / kTileTokens;
-    int n_chunks = 0;
-    const int first = n_sh + block_excl_scan(nch, pt.tmp, &n_chunks);
-    for (int c = 0; c < nch; ++c) {
-      p.act[first + c] = e;
-      p.off[first + c] = pt.off[e] + c * kTileTokens;
-      p.cnt[first + c] = min(kTileTokens, ce - c * kTileTokens);
-    }
-    if (tid == 0) {
-      *p.n_active = n_sh + n_chunks;
-      *p.unit_ctr = 0;
-    }
-    for (int i = tid; i < n_sh + n_chunks; i += blockDim.x) p.gu_done[i] = 0;
-    for (int i = tid; i < (p.H >> 7); i += blockDim.x) p.dn_done[i] = 0;
+  }
+  if (tid < n_sh) {
+    c_act[tid] = E;
+    c_off[tid] = MK + tid * kTileTokens;
+    c_cnt[tid] = min(kTileTokens, M - tid * kTileTokens);
+  }
+  __syncthreads();
+  const int e = tid < n_act ? by_rank[tid] : 0;
+  const int ce = tid < n_act ? pt.cnt[e] : 0;
+  const int nch = (ce + kTileTokens - 1) / kTileTokens;
+  int n_chunks = 0;
+  const int first = n_sh + block_excl_scan(nch, pt.tmp, &n_chunks);
+  const bool fits = n_sh + n_chunks <= NC;  // the host sized the tables for the worst case
+  for (int c = 0; c < nch && first + c < NC; ++c) {
+    c_act[first + c] = e;
+    c_off[first + c] = pt.off[e] + c * kTileTokens;
+    c_cnt[first + c] = min(kTileTokens, ce - c * kTileTokens);
+  }
+  if (blockIdx.x == 0) {
+    if (!fits && tid == 0) atomicOr(p.err, kErrBadRoute);
     if (p.out_idx)
       for (int i = tid; i < MK; i += blockDim.x) p.out_idx[i] = pt.idx[i];
     if (p.out_w)
       for (int i = tid; i < MK; i += blockDim.x) p.out_w[i] = p.topk_w[i];
   }
-  {  // gather: four consecutive rows per CTA pass, every thread's loads before its stores
-    const int per_row = p.H / 8;  // 16-byte pieces per row
-    const int span = 4 * per_row;
-    const int nt = blockDim.x;
-    for (int base = blockIdx.x * 4; base < MK; base += gridDim.x * 4) {
-      for (int i0 = tid; i0 < span; i0 += nt * 4) {
-        uint4 v[4];
-        int dst[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = i0 + j * nt;
-          const int r = base + i / per_row;
-          dst[j] = -1;
-          if (i < span && r < MK) {
-            const int c = i - (i / per_row) * per_row;
-            v[j] = __ldcg(reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(pt.row_tok[r]) * p.H) + c);
-            dst[j] = r * per_row + c;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (dst[j] >= 0) reinterpret_cast<uint4*>(p.xg)[dst[j]] = v[j];
-      }
-    }
-  }
   fence_proxy_async_shared();  // the ring was used generically; TMA refills it
-  const bool ok = grid_barrier(p.bar_count, p.err);
+  __syncthreads();
   Rt rt;
-  rt.act = p.act;
-  rt.cnt = p.cnt;
-  rt.off = p.off;
+  rt.act = c_act;
+  rt.cnt = c_cnt;
+  rt.off = c_off;
   rt.mask = nullptr;
   rt.tok_slot = p.tok_slot;
   rt.topk_w = p.topk_w;
-  rt.n_exp = ok ? __ldcg(p.n_active) : 0;  // after a failed barrier no unit runs
+  rt.n_exp = fits ? n_sh + n_chunks : 0;
   rt.dense = 0;
   rt.chunked = 1;
+  // Warps 3-7 (the epilogue warps and the spare one) gather first: no
+  // accumulator is ready before the first unit's rows are in anyway.
+  const int warp = tid >> 5;
+  if (warp >= 3 && warp < 8) gather_chunks(p, rt, row_tok, 160, tid - 96, 4);
   expert_roles<kQ4>(p, s, rt, tmem_base);
+  exit_reset(p, rt.n_exp, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), true);
 }
 
 
@@ -1340,6 +1422,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
   if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
+  exit_reset(p, E + 1, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), false);
 }
 
 // smem_a: A stages in shared memory; stages_a: A barriers; kg: K groups of
@@ -1350,11 +1433,15 @@ size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int
          static_cast<size_t>(2 * stages_a + 2 * stages_b + 2 * stages_q + 5 + 2 * kExpertUnitRing) * 8 + 256;
 }
 
-// idx, w, slot, coreset probability [M*K] each; mask, count, offset, active,
+// (k_layer) idx, w, slot, coreset probability [M*K] each; mask, count, offset, active,
 // coreset mass, sorted mass, sorted id [E] each; the active count and the
 // coreset's allowed-set words.
 size_t perm_smem_bytes(int M, int K, int E) {
-  return static_cast<size_t>(2 * M * K + E * (kMaxTokens / 32) + 2 * E + 32 + E) * 4;
+  return static_cast<size_t>(M * K + E * (kMaxTokens / 32) + 2 * E + 32 + E) * 4;
+}
+
+size_t expert_tables_bytes(int M, int K, int max_chunks) {
+  return ((static_cast<size_t>(2) * M * K + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(3) * max_chunks * 4;
 }
 
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }

@@ -137,6 +137,9 @@ struct ExpertArgs {
   int* unit_ctr;
   int* gu_done;
   int* dn_done;
+  int* gathered;   // standalone kernel: [max_chunks] rows of each chunk gathered so far
+  int* exit_ctr;   // CTAs that finished this launch; the last one resets the unit counters
+  int max_chunks;  // standalone kernel: room of the chunk tables
   int* err;
   int M, H, F, E, K;
   int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
@@ -223,6 +226,9 @@ cudaError_t expert_resident_per_sm(bool fused, bool q4, size_t smem, int* n);
 size_t layer_rt_bytes(int M, int K, int E);
 // Shared memory the standalone expert kernel's permutation needs (in its weight ring).
 size_t perm_smem_bytes(int M, int K, int E);
+// Shared memory the standalone expert kernel keeps for its whole run: the
+// token of every gathered row and the chunk tables.
+size_t expert_tables_bytes(int M, int K, int max_chunks);
 // Largest token count the fused layer kernel takes (one 32-bit mask per expert).
 constexpr int kLayerMaxTokens = 32;
 // Launches the unmask or the accept form of the head kernel.

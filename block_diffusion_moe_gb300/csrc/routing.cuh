@@ -385,7 +385,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_tmp, int* total) {
 // Shared-memory tables of one CTA's token -> expert permutation.
 struct PermTables {
   int* idx;       // [M*K] selections (clamped expert ids)
-  int* row_tok;   // [M*K] token of each gathered row
+  uint16_t* row_tok;  // [M*K] token of each gathered row (tokens < 65536)
   uint32_t* bm;   // [E][kMaxTokens / 32] token bitmask per expert
   int* off;       // [E] first row of each expert
   int* cnt;       // [E] tokens per expert
@@ -437,7 +437,7 @@ __device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, i
     int pre = __popc(t.bm[e * kW + wd] & ((1u << bit) - 1u));
     for (int j = 0; j < wd; ++j) pre += __popc(t.bm[e * kW + j]);
     const int row = t.off[e] + pre;
-    t.row_tok[row] = tk;
+    t.row_tok[row] = static_cast<uint16_t>(tk);
     if (slot_out != nullptr) slot_out[i] = row;
   }
   __syncthreads();

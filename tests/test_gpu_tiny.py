@@ -302,20 +302,26 @@ def test_router_exact_ties_take_the_lower_expert_id(M):
 
 
 @pytest.mark.parametrize("M", [8, 40])
-def test_grid_barrier_timeout_is_reported_and_cleared(M):
-    """Failure detection without a fault: the grid barrier's arrival count in
-    the workspace control block (bytes 24-31, a 64-bit count that only grows)
-    is set one past a multiple of the grid size, so the last CTA to arrive
-    waits for a count that no CTA will reach. Its bounded wait gives up after
-    about two seconds and sets the status word; the status call reports the
+def test_dependency_timeout_is_reported_and_cleared(M):
+    """Failure detection without a fault. Fused kernel (8 tokens): the grid
+    barrier's arrival count in the workspace control block (bytes 24-31, a
+    64-bit count that only grows) is set one past a multiple of the grid
+    size, so the last CTA to arrive waits for a count that no CTA will reach.
+    Standalone expert kernel (40 tokens, no grid barrier): the unit counter
+    (bytes 4-7) is set to 1, so unit 0 (the first gate/up slice of the
+    shared expert) is never drawn and the shared expert's down units wait
+    for a slice that never comes. Either bounded wait gives up after about
+    two seconds and sets the status word; the status call reports the
     timeout and clears the control block, and the same workspace then gives
-    the oracle's result. Fused kernel (8 tokens) and standalone expert kernel
-    (40 tokens)."""
+    the oracle's result."""
     d = synth.TINY
     layer = synth.make_layer(d, 31, 0, DEV)
     x = synth.make_x(d, M, 32, DEV)
     ws = clover.workspace(clover.moe_workspace_bytes(d, M), x.device)
-    ws[24:32].view(torch.int64).fill_(1)
+    if M <= 32:
+        ws[24:32].view(torch.int64).fill_(1)
+    else:
+        ws[4:8].view(torch.int32).fill_(1)
     clover.moe_block_step(d, layer, x, ws=ws)
     torch.cuda.synchronize()
     with pytest.raises(clover.CloverError) as ei:
