@@ -952,44 +952,75 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 // Copies the normed rows of the routed chunks' tokens into expert order
 // (row r of the gathered buffer = normed row of token row_tok[r]). Work is
 // cut into pieces of four rows; piece q of chunk a belongs to CTA
-// (7 a + q) mod G, so every CTA takes a share of the hottest chunks first.
-// After a piece's rows are stored, the chunk's counter grows by its rows
-// (release); a gate/up unit of the chunk loads them once the counter reaches
-// the chunk's row count. Run by n_thr threads of the CTA (named barrier bar).
-__device__ void gather_chunks(const ExpertArgs& p, const Rt& rt, const uint16_t* row_tok, int n_thr, int tid,
-                              uint32_t bar) {
-  const int G = gridDim.x;
-  const int per_row = p.H / 8;  // 16-byte pieces per row
-  for (int a = 0; a < rt.n_exp; ++a) {
-    if (rt.act[a] == p.E) continue;  // the shared expert reads the normed rows in place
-    const int off = rt.off[a], cnt = rt.cnt[a];
-    const int n_q = (cnt + 3) >> 2;
-    for (int q = static_cast<int>((static_cast<unsigned>(G) - (7u * a) % G + blockIdx.x) % G); q < n_q; q += G) {
-      const int r0 = q * 4, nr = min(4, cnt - r0);
-      const int span = nr * per_row;
-      for (int i0 = tid; i0 < span; i0 += 4 * n_thr) {
-        uint4 v[4];
-        int dst[4];
+// (7 a + q) mod G (a chunk has at most 64 pieces, fewer than the CTAs, so a
+// CTA owns at most one piece of each chunk). The first warp lists the CTA's
+// rows, hottest chunks first, in `list` (shared memory of n_list entries);
+// then all n_thr threads copy them with eight 16-byte loads in flight each,
+// fence once, and publish per chunk how many rows this CTA gathered
+// (release); a gate/up unit of the chunk loads them once the chunk's
+// counter reaches its row count. Run by the n_thr threads of named barrier
+// `bar` (tid 0..n_thr-1, the first warp being tid 0..31).
+__device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G, int* first) {
+  const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
+  const int q0 = static_cast<int>((static_cast<unsigned>(blockIdx.x) + static_cast<unsigned>(G) -
+                                   (7u * static_cast<unsigned>(a)) % static_cast<unsigned>(G)) %
+                                  static_cast<unsigned>(G));
+  *first = rt.off[a] + 4 * q0;
+  return q0 < n_q ? min(4, cnt - 4 * q0) : 0;
+}
+
+__device__ void gather_chunks(const ExpertArgs& p, const Rt& rt, const uint16_t* row_tok, uint16_t* list, int n_list,
+                              int n_thr, int tid, uint32_t bar) {
+  const int G = gridDim.x, lane = tid & 31;
+  __shared__ int s_n;
+  if (tid < 32) {
+    int base = 0;
+    for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
+      const int a = a0 + lane;
+      int first = 0, nr = 0;
+      if (a < rt.n_exp && rt.act[a] != p.E) nr = owned_rows(rt, a, G, &first);
+      int incl = nr;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = i0 + j * n_thr;
-          dst[j] = -1;
-          if (i < span) {
-            const int rr = i / per_row, c = i - rr * per_row;
-            const int r = off + r0 + rr;
-            v[j] = __ldcg(reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(row_tok[r]) * p.H) + c);
-            dst[j] = r * per_row + c;
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (dst[j] >= 0) reinterpret_cast<uint4*>(p.xg)[dst[j]] = v[j];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      fence_proxy_async_global();  // the rows are read by TMA
-      __threadfence();
-      named_bar_sync(bar, n_thr);
-      if (tid == 0) red_release_gpu_add(&p.gathered[a], nr);
+      for (int j = 0; j < nr; ++j)
+        if (base + incl - nr + j < n_list) list[base + incl - nr + j] = static_cast<uint16_t>(first + j);
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) s_n = min(base, n_list);
+  }
+  named_bar_sync(bar, n_thr);
+  const int n_rows = s_n;
+  const int per_row = p.H / 8;  // 16-byte pieces per row
+  const int total = n_rows * per_row;
+  for (int i0 = tid; i0 < total; i0 += 8 * n_thr) {
+    uint4 v[8];
+    int dst[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * n_thr;
+      dst[j] = -1;
+      if (i < total) {
+        const int li = i / per_row, c = i - li * per_row;
+        const int r = list[li];
+        v[j] = __ldcg(reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(row_tok[r]) * p.H) + c);
+        dst[j] = r * per_row + c;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (dst[j] >= 0) reinterpret_cast<uint4*>(p.xg)[dst[j]] = v[j];
+  }
+  fence_proxy_async_global();  // the rows are read by TMA
+  __threadfence();
+  named_bar_sync(bar, n_thr);
+  for (int a = tid; a < rt.n_exp; a += n_thr) {
+    if (rt.act[a] == p.E) continue;
+    int first = 0;
+    const int nr = owned_rows(rt, a, G, &first);
+    if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
   }
 }
 
@@ -1045,13 +1076,17 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   int* c_off = c_act + NC;
   int* c_cnt = c_off + NC;
   PermTables pt;
-  pt.idx = reinterpret_cast<int*>(s.a_ring);
-  pt.row_tok = row_tok;
-  pt.bm = reinterpret_cast<uint32_t*>(pt.idx + MK);
-  pt.off = reinterpret_cast<int*>(pt.bm + E * (kMaxTokens / 32));
-  pt.cnt = pt.off + E;
-  pt.tmp = pt.cnt + E;
+  const int ws = perm_stride(M);
+  // (every table starts on a 16-byte boundary of the 1 KiB-aligned ring)
+  const int E4 = (E + 3) & ~3;
+  pt.bm = reinterpret_cast<uint32_t*>(s.a_ring);
+  pt.off = reinterpret_cast<int*>(pt.bm + ((E * ws + 3) & ~3));
+  pt.cnt = pt.off + E4;
+  pt.tmp = pt.cnt + E4;
   int* by_rank = pt.tmp + 32;  // [E] active expert ids, heaviest first
+  pt.pre = reinterpret_cast<uint16_t*>(by_rank + E4);
+  pt.idx = reinterpret_cast<uint8_t*>(pt.pre + ((E * ws + 7) & ~7));
+  pt.row_tok = row_tok;
   const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
   const int tid = threadIdx.x;
   // Unit tables: the expert's tokens in chunks of at most kTileTokens rows
@@ -1065,7 +1100,15 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     const int c = pt.cnt[tid];
     if (c > 0) {
       int rank = 0;
-      for (int j = 0; j < E; ++j) {
+      const int4* c4 = reinterpret_cast<const int4*>(pt.cnt);  // 16-byte aligned; the tail past E / 4 is read below
+      const int e4 = E >> 2;
+      for (int j = 0; j < e4; ++j) {
+        const int4 v = c4[j];
+        const int b = 4 * j;
+        rank += (v.x > c || (v.x == c && b < tid)) + (v.y > c || (v.y == c && b + 1 < tid)) +
+                (v.z > c || (v.z == c && b + 2 < tid)) + (v.w > c || (v.w == c && b + 3 < tid));
+      }
+      for (int j = e4 * 4; j < E; ++j) {
         const int cj = pt.cnt[j];
         rank += (cj > c || (cj == c && j < tid)) ? 1 : 0;
       }
@@ -1111,7 +1154,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   // Warps 3-7 (the epilogue warps and the spare one) gather first: no
   // accumulator is ready before the first unit's rows are in anyway.
   const int warp = tid >> 5;
-  if (warp >= 3 && warp < 8) gather_chunks(p, rt, row_tok, 160, tid - 96, 4);
+  // (the list lives in the SwiGLU exchange buffer, unused until the first
+  // gate/up epilogue, which these same warps run after the gather)
+  if (warp >= 3 && warp < 8)
+    gather_chunks(p, rt, row_tok, reinterpret_cast<uint16_t*>(s.xch), 2 * 64 * 20 * 2, 160, tid - 96, 4);
   expert_roles<kQ4>(p, s, rt, tmem_base);
   exit_reset(p, rt.n_exp, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), true);
 }
@@ -1437,7 +1483,9 @@ size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int
 // coreset mass, sorted mass, sorted id [E] each; the active count and the
 // coreset's allowed-set words.
 size_t perm_smem_bytes(int M, int K, int E) {
-  return static_cast<size_t>(M * K + E * (kMaxTokens / 32) + 2 * E + 32 + E) * 4;
+  const size_t ws = static_cast<size_t>(perm_stride(M)), e4 = (static_cast<size_t>(E) + 3) & ~static_cast<size_t>(3);
+  return (((E * ws + 3) & ~static_cast<size_t>(3)) + 3 * e4 + 32) * 4 + ((E * ws + 7) & ~static_cast<size_t>(7)) * 2 +
+         static_cast<size_t>(M) * K;
 }
 
 size_t expert_tables_bytes(int M, int K, int max_chunks) {

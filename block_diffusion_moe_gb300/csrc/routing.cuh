@@ -384,45 +384,54 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_tmp, int* total) {
 
 // Shared-memory tables of one CTA's token -> expert permutation.
 struct PermTables {
-  int* idx;       // [M*K] selections (clamped expert ids)
+  uint8_t* idx;       // [M*K] selections (clamped expert ids; E <= 256)
   uint16_t* row_tok;  // [M*K] token of each gathered row (tokens < 65536)
-  uint32_t* bm;   // [E][kMaxTokens / 32] token bitmask per expert
-  int* off;       // [E] first row of each expert
-  int* cnt;       // [E] tokens per expert
-  int* tmp;       // [17] scan scratch
+  uint32_t* bm;       // [E][perm_stride(M)] token bitmask per expert
+  uint16_t* pre;      // [E][perm_stride(M)] tokens of the expert in the words before each word
+  int* off;           // [E] first row of each expert
+  int* cnt;           // [E] tokens per expert
+  int* tmp;           // [32] scan scratch
 };
+
+// Words per expert in the bitmask and prefix tables: one per 32 tokens,
+// rounded up to an odd count so that the rows of different experts start in
+// different shared-memory banks (warps read one word of many experts at once).
+__host__ __device__ constexpr int perm_stride(int M) { return ((M + 31) >> 5) | 1; }
 
 // Builds, with every thread of the CTA (blockDim.x >= E), the permutation of
 // the M*K top-k selections: per-expert token bitmasks (word wd of an expert
 // written by warp wd alone: the lanes that chose the same expert in one
-// selection slot merge their bits), a scan over experts for the row offsets,
-// and each selection's row = its expert's offset + the number of lower
-// tokens routed to that expert, so rows of one expert are in token order.
-// Returns the number of active experts; `slot_out` (nullable) receives each
-// selection's row.
-__device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, int K, int E, const PermTables& t, int32_t* slot_out) {
+// selection slot merge their bits), per-expert counts and a prefix count per
+// word, a scan over experts for the row offsets, and each selection's row =
+// its expert's offset + the number of lower tokens routed to that expert, so
+// rows of one expert are in token order. Returns the number of active
+// experts; `slot_out` (nullable) receives each selection's row.
+__device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, int K, int E, const PermTables& t,
+                                               int32_t* slot_out) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int MK = M * K, nw = (M + 31) >> 5;
-  constexpr int kW = kMaxTokens / 32;
+  const int MK = M * K, nw = (M + 31) >> 5, ws = perm_stride(M);
   for (int i = tid; i < MK; i += blockDim.x) {
     const int e = __ldcg(topk_idx + i);
-    t.idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);  // ids come from another kernel; clamping keeps indexing safe
+    t.idx[i] = static_cast<uint8_t>(e < 0 ? 0 : (e >= E ? E - 1 : e));  // ids come from another kernel; clamping keeps indexing safe
   }
-  for (int i = tid; i < E * kW; i += blockDim.x) t.bm[i] = 0u;
+  for (int i = tid; i < E * ws; i += blockDim.x) t.bm[i] = 0u;
   __syncthreads();
   for (int wd = warp; wd < nw; wd += blockDim.x >> 5) {
     const int tk = wd * 32 + lane;
     for (int k = 0; k < K; ++k) {
       const int e = tk < M ? t.idx[tk * K + k] : -1;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(peers) - 1) t.bm[e * kW + wd] |= peers;
+      if (e >= 0 && lane == __ffs(peers) - 1) t.bm[e * ws + wd] |= peers;
       __syncwarp();
     }
   }
   __syncthreads();
   int c = 0;
   if (tid < E)
-    for (int wd = 0; wd < nw; ++wd) c += __popc(t.bm[tid * kW + wd]);
+    for (int wd = 0; wd < nw; ++wd) {
+      t.pre[tid * ws + wd] = static_cast<uint16_t>(c);
+      c += __popc(t.bm[tid * ws + wd]);
+    }
   int total = 0;
   const int off = block_excl_scan(c, t.tmp, &total);
   const int n_act = __syncthreads_count(tid < E && c > 0);
@@ -434,9 +443,7 @@ __device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, i
   for (int i = tid; i < MK; i += blockDim.x) {
     const int e = t.idx[i], tk = i / K;
     const int wd = tk >> 5, bit = tk & 31;
-    int pre = __popc(t.bm[e * kW + wd] & ((1u << bit) - 1u));
-    for (int j = 0; j < wd; ++j) pre += __popc(t.bm[e * kW + j]);
-    const int row = t.off[e] + pre;
+    const int row = t.off[e] + t.pre[e * ws + wd] + __popc(t.bm[e * ws + wd] & ((1u << bit) - 1u));
     t.row_tok[row] = static_cast<uint16_t>(tk);
     if (slot_out != nullptr) slot_out[i] = row;
   }
