@@ -137,6 +137,21 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), cached
+// in L2 only; completion is tracked per thread with commit/wait groups.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's committed groups are in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Asks for `bytes` (a multiple of 16) at src (16-byte aligned) to be brought
 // into L2; nothing waits for it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
