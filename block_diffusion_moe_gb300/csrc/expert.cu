@@ -1303,10 +1303,14 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   if (static_cast<int>(blockIdx.x) < M && warp == 0) route_token(blockIdx.x, nullptr, coreset, p.pub_idx, p.pub_w, p.pub_p);
   if (!grid_barrier(p.bar_count, p.err)) *s.abort = 1u;
   for (int i = threadIdx.x; i < MK; i += blockDim.x) {
+    // all loads before the stores (shared and global through generic
+    // pointers would otherwise keep each load behind the previous store)
     const int e = __ldcg(p.pub_idx + i);
+    const float wv = __ldcg(p.pub_w + i);
+    const float pv = coreset ? __ldcg(p.pub_p + i) : 0.f;
     s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-    s_w[i] = __ldcg(p.pub_w + i);
-    if (coreset) s_p[i] = __ldcg(p.pub_p + i);
+    s_w[i] = wv;
+    if (coreset) s_p[i] = pv;
   }
   if (coreset) {
     // Block coreset (the M tokens are one block): every CTA computes the
@@ -1373,8 +1377,9 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     if (!grid_barrier(p.bar_count, p.err)) *s.abort = 1u;
     for (int i = threadIdx.x; i < MK; i += blockDim.x) {
       const int e = __ldcg(p.pub2_idx + i);
+      const float wv = __ldcg(p.pub2_w + i);
       s_idx[i] = e < 0 ? 0 : (e >= E ? E - 1 : e);
-      s_w[i] = __ldcg(p.pub2_w + i);
+      s_w[i] = wv;
     }
   }
 

@@ -410,9 +410,22 @@ __device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, i
                                                int32_t* slot_out) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int MK = M * K, nw = (M + 31) >> 5, ws = perm_stride(M);
-  for (int i = tid; i < MK; i += blockDim.x) {
-    const int e = __ldcg(topk_idx + i);
-    t.idx[i] = static_cast<uint8_t>(e < 0 ? 0 : (e >= E ? E - 1 : e));  // ids come from another kernel; clamping keeps indexing safe
+  // Eight loads in flight per thread before any store: the loads read global
+  // memory and the stores shared memory through generic pointers, so the
+  // compiler would otherwise keep every load behind the previous store.
+  for (int i0 = tid; i0 < MK; i0 += 8 * blockDim.x) {
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * blockDim.x;
+      v[j] = i < MK ? __ldcg(topk_idx + i) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + j * blockDim.x;
+      const int e = v[j];
+      if (i < MK) t.idx[i] = static_cast<uint8_t>(e < 0 ? 0 : (e >= E ? E - 1 : e));  // ids come from another kernel; clamping keeps indexing safe
+    }
   }
   for (int i = tid; i < E * ws; i += blockDim.x) t.bm[i] = 0u;
   __syncthreads();
