@@ -60,7 +60,7 @@ enum CtrlWord : int {
 
 struct MoeLayout {
   size_t gu_done, dn_done, n_active, act, cnt, off, tok_slot, topk_idx, topk_w, topk_p, rr_idx, rr_w, fin_w, logits,
-      xg, hbuf, yslot, tg_ctr, bytes;
+      xg, hbuf, yslot, tg_ctr, gathered, bytes;
 };
 
 // Most units tables a call can need: the standalone expert kernel cuts each
@@ -101,6 +101,7 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
   L.hbuf = take(R * F * 2);
   L.yslot = take(R * H * 4);
   L.tg_ctr = take(((M + kRouteTileTokens - 1) / kRouteTileTokens) * 4);  // routing arrival counters (kept zero)
+  L.gathered = take(NC * 4);  // rows gathered per chunk (reset by the last CTA of each launch)
   L.bytes = o;
   return L;
 }
@@ -423,6 +424,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.unit_ctr = ctrl + kCtrlUnitCtr;
   xa.gu_done = reinterpret_cast<int*>(data + L.gu_done);
   xa.dn_done = reinterpret_cast<int*>(data + L.dn_done);
+  xa.gathered = reinterpret_cast<int*>(data + L.gathered);
   xa.exit_ctr = ctrl + kCtrlExitCtr;
   xa.max_chunks = n_chunks;
   xa.err = err;

@@ -75,8 +75,6 @@ struct Rt {
   int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
   int dense;                // gate/up B operand = all M normed rows
   int chunked;              // standalone: units index chunks of at most kTileTokens rows
-  const uint16_t* row_tok;  // standalone: token of every routed row
-  uint32_t* rowoff;         // standalone: [kTileTokens] byte offsets of a unit's token rows (B producer's)
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArgs& p) {
@@ -434,77 +432,52 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
   }
 }
 
-// Activation producer (all 32 lanes of warp 2). B tiles are the expert's
-// token rows. Most units load them with TMA boxes (lane 0): the dense normed
-// rows (fused kernel), the shared expert's rows, and the SwiGLU rows of down
-// units. A routed gate/up unit of the standalone kernel fetches its chunk's
-// token rows straight from the normed rows with 16-byte asynchronous copies
-// (eight lanes per row, one row's 128 contiguous bytes, written in the
-// 128-byte swizzle the MMA descriptor expects), so no CTA waits for rows
-// gathered by another. Up to two such stages stay in flight; each is
-// released to the MMA once this lane's copies landed and were fenced for the
-// async proxy. All pending stages are released before any wait that the MMA
-// could be needed to satisfy (a down unit's dependency, the end).
 __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
-  const int lane = threadIdx.x & 31;
   const uint64_t pol = l2_policy_evict_last();
   const int SB = p.stages_b;
   const int SF = p.F >> 6;
-  const int lag = min(2, SB - 1);  // released stages must include every stage the next empty-wait depends on
   int sb = 0;
   uint32_t phb = 0, issued = 0, parity_bits = 0;
-  int pend0 = 0, pend1 = 0, pend2 = 0;  // pending stages, oldest first (registers, not an array)
-  int n_pend = 0;
-  auto release_to = [&](int keep) {
-    while (n_pend > keep) {
-      if (n_pend - 1 >= 2)
-        cp_async_wait<2>();
-      else if (n_pend - 1 == 1)
-        cp_async_wait<1>();
-      else
-        cp_async_wait<0>();
-      fence_proxy_async_shared();  // the MMA reads the rows through the async proxy
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s.full_b[pend0]);
-      pend0 = pend1;
-      pend1 = pend2;
-      --n_pend;
-    }
-  };
-  bool failed = false;
   for (int it = 0;; ++it) {
     const int us = it & (kExpertUnitRing - 1);
     const uint32_t upar = (it / kExpertUnitRing) & 1;
-    int u = kUnitAbort;
-    if (lane == 0) {
-      if (mbar_wait(&s.ufull[us], upar, s.abort)) {
-        u = s.unit_ids[us];
-        mbar_arrive(&s.uempty[us]);
-      } else {
-        raise_abort(s, p.err, kErrMbarTimeout);
-      }
-    }
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if (u < 0) {
-      failed = (u == kUnitAbort);
+    if (!mbar_wait(&s.ufull[us], upar, s.abort)) {
+      raise_abort(s, p.err, kErrMbarTimeout);
       break;
     }
+    const int u = s.unit_ids[us];
+    mbar_arrive(&s.uempty[us]);
+    if (u < 0) break;
     const Unit w = decode_unit(u, rt, p);
     const int nrows = unit_rows(w, rt, p);
     const int row0 = (w.kind == 0 && rt.dense) ? 0 : w.off;
-    const bool sw = rt.chunked && w.kind == 0 && w.e != p.E;
     const CUtensorMap* m;
     const CUtensorMap* mb;
     int nk, box;
-    if (!sw) release_to(0);
     if (w.kind == 0) {
       m = &p.tm_xg;
       mb = &p.tm_xg_big;
       box = p.xg_box;
       nk = p.H >> 6;
-      if (sw) {
-        for (int j = lane; j < w.cnt; j += 32) rt.rowoff[j] = static_cast<uint32_t>(rt.row_tok[w.off + j]) * (p.H * 2u);
-        __syncwarp();
+      if (rt.chunked && w.e != p.E) {
+        // The chunk's token rows are gathered by the CTAs' spare warps at
+        // the start of the launch: wait (bounded) until all of them are in.
+        const unsigned long long t0 = global_ns();
+        bool ok = true;
+        while (ld_acquire_gpu(&p.gathered[w.a]) < w.cnt) {
+          if (*s.abort) {
+            ok = false;
+            break;
+          }
+          if (global_ns() - t0 > kWaitLimitNs) {
+            raise_abort(s, p.err, kErrDepTimeout);
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+        }
+        if (!ok) break;
+        fence_proxy_async_global();
       }
     } else {
       m = &p.tm_h;
@@ -512,91 +485,53 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       box = p.h_box;
       nk = p.F >> 6;
       // The expert's SwiGLU rows must be complete before they are loaded.
-      int ok = 1;
-      if (lane == 0) {
-        const unsigned long long t0 = global_ns();
-        while (ld_acquire_gpu(&p.gu_done[w.a]) < SF) {
-          if (*s.abort) {
-            ok = 0;
-            break;
-          }
-          if (global_ns() - t0 > kWaitLimitNs) {
-            raise_abort(s, p.err, kErrDepTimeout);
-            ok = 0;
-            break;
-          }
-          __nanosleep(64);
+      const unsigned long long t0 = global_ns();
+      bool ok = true;
+      while (ld_acquire_gpu(&p.gu_done[w.a]) < SF) {
+        if (*s.abort) {
+          ok = false;
+          break;
         }
-        fence_proxy_async_global();
+        if (global_ns() - t0 > kWaitLimitNs) {
+          raise_abort(s, p.err, kErrDepTimeout);
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
       }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) {
-        failed = true;
-        break;
-      }
+      if (!ok) break;
+      fence_proxy_async_global();
     }
     const int kg = unit_kg(w, p);
     const int rot = unit_rot(w, nk, unit_kstep(w, p));
     bool ok = true;
     for (int kc0 = 0; kc0 < nk; kc0 += kg) {
       const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
-      int good = 1;
-      if (lane == 0 && !mbar_wait(&s.empty_b[sb], phb ^ 1u, s.abort)) {
+      if (!mbar_wait(&s.empty_b[sb], phb ^ 1u, s.abort)) {
         raise_abort(s, p.err, kErrMbarTimeout);
-        good = 0;
-      }
-      if (!__shfl_sync(0xffffffffu, good, 0)) {
         ok = false;
         break;
       }
       const uint32_t dst0 = smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes);
-      if (sw) {
-        const int c = lane & 7;
-        for (int h = 0; h < kg; ++h) {
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.xn) + (kc + h) * 128 + c * 16;
-          const uint32_t dst = dst0 + h * s.b_half_bytes;
-          for (int i = lane >> 3; i < w.cnt; i += 4) cp_async_16(dst + i * 128 + ((c ^ (i & 7)) << 4), src + rt.rowoff[i]);
+      mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(kg * nrows) * 128u);
+      for (int h = 0; h < kg; ++h) {
+        const uint32_t dst = dst0 + h * s.b_half_bytes;
+        for (int i = 0; i < nrows;) {
+          const bool big = nrows - i >= box;
+          tma_load_2d(dst + i * 128, big ? mb : m, &s.full_b[sb], (kc + h) * 64, row0 + i, pol);
+          i += big ? box : 16;
         }
-        cp_async_commit();
-        if (n_pend == 0)
-          pend0 = sb;
-        else if (n_pend == 1)
-          pend1 = sb;
-        else
-          pend2 = sb;
-        ++n_pend;
-        release_to(lag);
-      } else if (lane == 0) {
-        mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(kg * nrows) * 128u);
-        for (int h = 0; h < kg; ++h) {
-          const uint32_t dst = dst0 + h * s.b_half_bytes;
-          for (int i = 0; i < nrows;) {
-            const bool big = nrows - i >= box;
-            tma_load_2d(dst + i * 128, big ? mb : m, &s.full_b[sb], (kc + h) * 64, row0 + i, pol);
-            i += big ? box : 16;
-          }
-        }
-        issued |= 1u << sb;
-        parity_bits = (parity_bits & ~(1u << sb)) | (phb << sb);
       }
+      issued |= 1u << sb;
+      parity_bits = (parity_bits & ~(1u << sb)) | (phb << sb);
       if (++sb == SB) {
         sb = 0;
         phb ^= 1u;
       }
     }
-    if (!ok) {
-      failed = true;
-      break;
-    }
+    if (!ok) break;
   }
-  // Copies still in flight land before the CTA may exit; when nothing failed
-  // their stages are released to the MMA as usual.
-  if (failed) {
-    cp_async_wait<0>();
-    n_pend = 0;
-  } else {
-    release_to(0);
-  }
-  if (lane == 0 && *s.abort) drain_ring(s.full_b, SB, issued, parity_bits);
+  if (*s.abort) drain_ring(s.full_b, SB, issued, parity_bits);
 }
 
 __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
@@ -959,7 +894,7 @@ __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s,
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(p, s, rt, tmem_base);
   } else if (warp == 2) {
-    producer_b(p, s, rt);
+    if (lane == 0) producer_b(p, s, rt);
   } else if (warp < 7) {
     epilogue(p, s, rt, tmem_base);
   } else if (kQ4 && warp >= 8) {
@@ -1014,6 +949,92 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 
 }  // namespace
 
+// Rows of chunk a that this CTA gathers. Pieces of four rows: piece q of
+// chunk a belongs to CTA (7 a + q) mod G. A chunk has at most 64 pieces,
+// fewer than the CTAs, so a CTA owns at most one piece of each chunk.
+__device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G, int* first) {
+  const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
+  const int q0 = static_cast<int>((static_cast<unsigned>(blockIdx.x) + static_cast<unsigned>(G) -
+                                   (7u * static_cast<unsigned>(a)) % static_cast<unsigned>(G)) %
+                                  static_cast<unsigned>(G));
+  *first = rt.off[a] + 4 * q0;
+  return q0 < n_q ? min(4, cnt - 4 * q0) : 0;
+}
+
+// Copies the normed rows of the routed chunks' tokens into expert order
+// (row r of the gathered buffer = normed row of token row_tok[r]), this
+// CTA's share of the pieces: warp 0 lists the rows (hottest chunks first),
+// thread 0 moves them with bulk copies through the still idle weight ring
+// (global -> shared -> global, one copy per row each way), waits for the
+// stores, and then every thread publishes, per chunk, how many rows this CTA
+// gathered (release). A gate/up unit of the chunk loads them once the
+// chunk's counter reaches its row count; there is no grid-wide wait. Called
+// by the whole CTA before the roles start. Returns false if a copy timed out.
+__device__ bool gather_chunks(const ExpertArgs& p, const Smem& s, const Rt& rt, const uint16_t* row_tok,
+                              uint64_t* gbar) {
+  const int G = gridDim.x, tid = threadIdx.x, lane = tid & 31;
+  uint16_t* list = reinterpret_cast<uint16_t*>(s.xch);  // the SwiGLU exchange buffer is idle until the first unit
+  const int n_list = 2 * 64 * 20 * 2;
+  __shared__ int s_n, s_ok;
+  if (tid < 32) {
+    int base = 0;
+    for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
+      const int a = a0 + lane;
+      int first = 0, nr = 0;
+      if (a < rt.n_exp && rt.act[a] != p.E) nr = owned_rows(rt, a, G, &first);
+      int incl = nr;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      for (int j = 0; j < nr; ++j)
+        if (base + incl - nr + j < n_list) list[base + incl - nr + j] = static_cast<uint16_t>(first + j);
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_n = min(base, n_list);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int n_rows = s_n;
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    const int per_round = static_cast<int>((static_cast<uint32_t>(p.smem_a) * s.a_stage_bytes) / row_bytes);
+    const uint32_t ring = smem_u32(s.a_ring);
+    uint32_t phase = 0;
+    int ok = 1;
+    for (int r0 = 0; r0 < n_rows && ok; r0 += per_round) {
+      const int n = min(per_round, n_rows - r0);
+      mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(n) * row_bytes);
+      for (int j = 0; j < n; ++j)
+        bulk_load(ring + j * row_bytes, p.xn + static_cast<size_t>(row_tok[list[r0 + j]]) * p.H, row_bytes, gbar);
+      if (!mbar_wait(gbar, phase, s.abort)) {
+        raise_abort(s, p.err, kErrMbarTimeout);
+        mbar_wait_for(gbar, phase, 200000000ull);  // no copy may still land in the ring
+        ok = 0;
+        break;
+      }
+      phase ^= 1u;
+      for (int j = 0; j < n; ++j)
+        bulk_store(p.xg + static_cast<size_t>(list[r0 + j]) * p.H, ring + j * row_bytes, row_bytes);
+      bulk_commit();
+      bulk_wait_read_all();  // the ring may take the next rows
+    }
+    bulk_wait_all();  // the rows are in global memory
+    fence_proxy_async_global();
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  if (!s_ok) return false;
+  for (int a = tid; a < rt.n_exp; a += blockDim.x) {
+    if (rt.act[a] == p.E) continue;
+    int first = 0;
+    const int nr = owned_rows(rt, a, G, &first);
+    if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
+  }
+  return true;
+}
+
 // Every CTA calls this last. The CTA that finishes last resets the unit
 // counter and the per-unit-table counters the launch used, so that the next
 // launch on the workspace finds them at zero without a barrier of its own
@@ -1021,7 +1042,7 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 // this grid complete). A clean launch leaves the unit counter at n_total
 // plus one failed draw per CTA; anything else (units skipped or never
 // drawn) is reported.
-__device__ void exit_reset(const ExpertArgs& p, int n_entries, int n_total) {
+__device__ void exit_reset(const ExpertArgs& p, int n_entries, int n_total, bool gathered) {
   __shared__ int s_lastx;
   __threadfence();
   __syncthreads();
@@ -1032,7 +1053,10 @@ __device__ void exit_reset(const ExpertArgs& p, int n_entries, int n_total) {
   __syncthreads();
   if (s_lastx) {
     __threadfence();
-    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) p.gu_done[i] = 0;
+    for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
+      p.gu_done[i] = 0;
+      if (gathered) p.gathered[i] = 0;
+    }
     if (threadIdx.x == 0) {
       if (n_total > 0 && *reinterpret_cast<volatile int*>(p.unit_ctr) != n_total + static_cast<int>(gridDim.x))
         atomicOr(p.err, kErrState);
@@ -1047,6 +1071,9 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     k_expert(const __grid_constant__ ExpertArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
+  // bulk-copy barrier of the gather (made visible by the prologue's fence)
+  uint64_t* gbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.tmem_slot) + 96);
+  if (threadIdx.x == 0) mbar_init(gbar, 1);
   const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
   pdl_wait();
   pdl_trigger();
@@ -1062,7 +1089,6 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   int* c_act = reinterpret_cast<int*>(s.rt_region + ((2 * MK + 15) & ~15));
   int* c_off = c_act + NC;
   int* c_cnt = c_off + NC;
-  uint32_t* rowoff = reinterpret_cast<uint32_t*>(c_cnt + NC);  // [kTileTokens]
   PermTables pt;
   const int ws = perm_stride(M);
   // (every table starts on a 16-byte boundary of the 1 KiB-aligned ring)
@@ -1139,10 +1165,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.n_exp = fits ? n_sh + n_chunks : 0;
   rt.dense = 0;
   rt.chunked = 1;
-  rt.row_tok = row_tok;
-  rt.rowoff = rowoff;
+  const int n_tab = rt.n_exp;
+  if (!gather_chunks(p, s, rt, row_tok, gbar)) rt.n_exp = 0;  // a CTA whose copies failed takes no units
   expert_roles<kQ4>(p, s, rt, tmem_base);
-  exit_reset(p, rt.n_exp, rt.n_exp * ((p.F >> 6) + (p.H >> 7)));
+  exit_reset(p, n_tab, n_tab * ((p.F >> 6) + (p.H >> 7)), true);
 }
 
 
@@ -1453,12 +1479,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.n_exp = (*s.abort) ? 0 : *s_nact + 1;  // after a failed barrier no unit runs
   rt.dense = 1;
   rt.chunked = 0;
-  rt.row_tok = nullptr;
-  rt.rowoff = nullptr;
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
   if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
-  exit_reset(p, E + 1, rt.n_exp * ((p.F >> 6) + (p.H >> 7)));
+  exit_reset(p, E + 1, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), false);
 }
 
 // smem_a: A stages in shared memory; stages_a: A barriers; kg: K groups of
@@ -1479,8 +1503,7 @@ size_t perm_smem_bytes(int M, int K, int E) {
 }
 
 size_t expert_tables_bytes(int M, int K, int max_chunks) {
-  return ((static_cast<size_t>(2) * M * K + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(3) * max_chunks * 4 +
-         static_cast<size_t>(kTileTokens) * 4;
+  return ((static_cast<size_t>(2) * M * K + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(3) * max_chunks * 4;
 }
 
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }

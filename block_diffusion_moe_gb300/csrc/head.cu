@@ -136,6 +136,10 @@ __device__ __forceinline__ void lse_merge_t(float& m, float& s, float& t, int& a
   }
 }
 
+// Weight (A) and position (B) tiles for the MMA. The head's weights are
+// written by no kernel, so the A tiles of the first ring's worth of stages
+// are requested before the dependency wait (overlapping the normalisation
+// kernel that writes the positions); their B tiles follow after it.
 __device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
   const uint64_t pol_w = l2_policy_evict_first();
   const uint64_t pol_x = l2_policy_evict_last();
@@ -146,32 +150,59 @@ __device__ void head_producer(const HeadArgs& p, const HeadSmem& s, int nb) {
   // consumes stages in issue order; only the accumulation order changes.
   const int kg = p.kg;
   const int rot = kg * static_cast<int>((blockIdx.x * 7u) % static_cast<unsigned>(nk / kg));
-  int st = 0;
-  uint32_t ph = 0, issued = 0, parity_bits = 0;
-  bool ok = true;
-  for (int tile = blockIdx.x; tile < p.n_tiles && ok; tile += gridDim.x) {
-    for (int kc0 = 0; kc0 < nk; kc0 += kg) {
-      const int kc = (kc0 + rot < nk) ? kc0 + rot : kc0 + rot - nk;
-      if (!mbar_wait(&s.empty[st], ph ^ 1u, s.abort)) {
-        atomicOr(p.err, kErrMbarTimeout);
-        *s.abort = 1u;
-        ok = false;
-        break;
-      }
-      const uint32_t dst0 = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
-      mbar_arrive_expect_tx(&s.full[st], s.stage_bytes);
-      for (int h = 0; h < kg; ++h) {  // half h: K group kc + h (A tile, then B tile)
-        const uint32_t dst = dst0 + h * s.half_bytes;
-        tma_load_2d(dst, &p.tm_w, &s.full[st], (kc + h) * 64, tile * 128, pol_w);
-        for (int i = 0; i < nb; i += p.x_box)
-          tma_load_2d(dst + kATileBytes + i * 128, &p.tm_x, &s.full[st], (kc + h) * 64, i, pol_x);
-      }
-      issued |= 1u << st;
-      parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
-      if (++st == p.stages) {
-        st = 0;
-        ph ^= 1u;
-      }
+  const int steps_per_tile = nk / kg;
+  const int my_tiles = (p.n_tiles > static_cast<int>(blockIdx.x)) ? (p.n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int n_steps = my_tiles * steps_per_tile;
+  // (tile, first K group) of pipeline step i
+  auto coords = [&](int i, int& tile, int& kc) {
+    const int t = i / steps_per_tile, k0 = (i - t * steps_per_tile) * kg;
+    tile = blockIdx.x + t * gridDim.x;
+    kc = (k0 + rot < nk) ? k0 + rot : k0 + rot - nk;
+  };
+  auto load_a = [&](int st, int tile, int kc) {
+    const uint32_t dst0 = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
+    for (int h = 0; h < kg; ++h)
+      tma_load_2d(dst0 + h * s.half_bytes, &p.tm_w, &s.full[st], (kc + h) * 64, tile * 128, pol_w);
+  };
+  auto load_b = [&](int st, int kc) {
+    const uint32_t dst0 = smem_u32(s.ring + static_cast<size_t>(st) * s.stage_bytes);
+    for (int h = 0; h < kg; ++h)
+      for (int i = 0; i < nb; i += p.x_box)
+        tma_load_2d(dst0 + h * s.half_bytes + kATileBytes + i * 128, &p.tm_x, &s.full[st], (kc + h) * 64, i, pol_x);
+  };
+  // first pass over the ring: the stages are free, nothing to wait for
+  const int pre = min(p.stages, n_steps);
+  for (int i = 0; i < pre; ++i) {
+    int tile, kc;
+    coords(i, tile, kc);
+    mbar_arrive_expect_tx(&s.full[i], s.stage_bytes);
+    load_a(i, tile, kc);
+  }
+  pdl_wait();
+  for (int i = 0; i < pre; ++i) {
+    int tile, kc;
+    coords(i, tile, kc);
+    load_b(i, kc);
+  }
+  int st = pre == p.stages ? 0 : pre;
+  uint32_t ph = pre == p.stages ? 1u : 0u;
+  uint32_t issued = (pre >= 32) ? 0xffffffffu : ((1u << pre) - 1u), parity_bits = 0;
+  for (int i = pre; i < n_steps; ++i) {
+    int tile, kc;
+    coords(i, tile, kc);
+    if (!mbar_wait(&s.empty[st], ph ^ 1u, s.abort)) {
+      atomicOr(p.err, kErrMbarTimeout);
+      *s.abort = 1u;
+      break;
+    }
+    mbar_arrive_expect_tx(&s.full[st], s.stage_bytes);
+    load_a(st, tile, kc);
+    load_b(st, kc);
+    issued |= 1u << st;
+    parity_bits = (parity_bits & ~(1u << st)) | (ph << st);
+    if (++st == p.stages) {
+      st = 0;
+      ph ^= 1u;
     }
   }
   if (*s.abort) {
@@ -557,7 +588,9 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s.tmem_slot;
-  pdl_wait();
+  // (the producer thread waits for the previous kernel itself, after it has
+  // requested the weight tiles that do not depend on it)
+  if (!(warp == 0 && lane == 0)) pdl_wait();
   pdl_trigger();
 
   if (warp == 0) {

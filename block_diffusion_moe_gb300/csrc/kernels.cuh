@@ -137,6 +137,7 @@ struct ExpertArgs {
   int* unit_ctr;
   int* gu_done;
   int* dn_done;
+  int* gathered;   // standalone kernel: [max_chunks] rows of each chunk gathered so far
   int* exit_ctr;   // CTAs that finished this launch; the last one resets the unit counters
   int max_chunks;  // standalone kernel: room of the chunk tables
   int* err;
