@@ -65,11 +65,12 @@ struct MoeLayout {
 
 // Most units tables a call can need: the standalone expert kernel cuts each
 // expert's rows (and the shared expert's) into chunks of at most
-// kTileTokens, so there are at most E + ceil(M K / kTileTokens) routed chunks
-// and ceil(M / kTileTokens) shared ones.
+// kExpertTileTokens, so there are at most E + ceil(M K / kExpertTileTokens)
+// routed chunks and ceil(M / kExpertTileTokens) shared ones.
 size_t max_chunks(const clover_dims& d, int M) {
   const size_t MK = static_cast<size_t>(M) * d.top_k;
-  return d.n_experts + (MK + kTileTokens - 1) / kTileTokens + (M + kTileTokens - 1) / kTileTokens + 1;
+  return d.n_experts + (MK + kExpertTileTokens - 1) / kExpertTileTokens +
+         (M + kExpertTileTokens - 1) / kExpertTileTokens + 1;
 }
 
 MoeLayout moe_layout(const clover_dims& d, int M) {
@@ -391,7 +392,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   }
   // B tiles move in boxes of up to 64 rows (one TMA instruction each), with
   // 16-row boxes for the rest; fewer, larger copies stream faster.
-  const int nb_rows = std::min((M + 15) & ~15, kTileTokens);
+  const int nb_rows = std::min((M + 15) & ~15, kExpertTileTokens);
   if (fused) {  // the gate/up B operand is the dense block of normed rows
     const bf16* xn_rows = xg + static_cast<size_t>(MK) * H;
     if ((rc = encode_bf16_2d(&xa.tm_xg, xn_rows, M, H, 16, "normed rows"))) return rc;
@@ -433,7 +434,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.F = F;
   xa.E = E;
   xa.K = K;
-  const int nb = std::min((M + 15) & ~15, kTileTokens);  // B-tile rows: one chunk at most
+  const int nb = std::min((M + 15) & ~15, kExpertTileTokens);  // B-tile rows: one chunk at most
   // Two K groups per A/B stage (8 MMAs per pipeline step instead of 4) when
   // the token tile is small; 256-token tiles keep one group per stage. The
   // low-bit path, whose A stages are written by the converter warps rather

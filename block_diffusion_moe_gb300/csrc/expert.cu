@@ -74,7 +74,7 @@ struct Rt {
   const float* topk_w;      // [M][K] weight of each selection
   int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
   int dense;                // gate/up B operand = all M normed rows
-  int chunked;              // standalone: units index chunks of at most kTileTokens rows
+  int chunked;              // standalone: units index chunks of at most kExpertTileTokens rows
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArgs& p) {
@@ -950,15 +950,19 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 }  // namespace
 
 // Rows of chunk a that this CTA gathers. Pieces of four rows: piece q of
-// chunk a belongs to CTA (7 a + q) mod G. A chunk has at most 64 pieces,
-// fewer than the CTAs, so a CTA owns at most one piece of each chunk.
-__device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G, int* first) {
+// chunk a belongs to CTA (7 a + q) mod G, so a CTA owns pieces q0, q0 + G,
+// ... of each chunk (usually at most one: a chunk has at most 32 pieces).
+__device__ __forceinline__ int first_piece(int a, int G) {
+  return static_cast<int>((static_cast<unsigned>(blockIdx.x) + static_cast<unsigned>(G) -
+                           (7u * static_cast<unsigned>(a)) % static_cast<unsigned>(G)) %
+                          static_cast<unsigned>(G));
+}
+
+__device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G) {
   const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
-  const int q0 = static_cast<int>((static_cast<unsigned>(blockIdx.x) + static_cast<unsigned>(G) -
-                                   (7u * static_cast<unsigned>(a)) % static_cast<unsigned>(G)) %
-                                  static_cast<unsigned>(G));
-  *first = rt.off[a] + 4 * q0;
-  return q0 < n_q ? min(4, cnt - 4 * q0) : 0;
+  int nr = 0;
+  for (int q = first_piece(a, G); q < n_q; q += G) nr += min(4, cnt - 4 * q);
+  return nr;
 }
 
 // Copies the normed rows of the routed chunks' tokens into expert order
@@ -980,16 +984,21 @@ __device__ bool gather_chunks(const ExpertArgs& p, const Smem& s, const Rt& rt, 
     int base = 0;
     for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
       const int a = a0 + lane;
-      int first = 0, nr = 0;
-      if (a < rt.n_exp && rt.act[a] != p.E) nr = owned_rows(rt, a, G, &first);
+      const bool mine = a < rt.n_exp && rt.act[a] != p.E;
+      const int nr = mine ? owned_rows(rt, a, G) : 0;
       int incl = nr;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += v;
       }
-      for (int j = 0; j < nr; ++j)
-        if (base + incl - nr + j < n_list) list[base + incl - nr + j] = static_cast<uint16_t>(first + j);
+      if (mine) {
+        int at = base + incl - nr;
+        const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
+        for (int q = first_piece(a, G); q < n_q; q += G)
+          for (int j = 4 * q; j < min(4 * q + 4, cnt); ++j, ++at)
+            if (at < n_list) list[at] = static_cast<uint16_t>(rt.off[a] + j);
+      }
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) s_n = min(base, n_list);
@@ -1028,8 +1037,7 @@ __device__ bool gather_chunks(const ExpertArgs& p, const Smem& s, const Rt& rt, 
   if (!s_ok) return false;
   for (int a = tid; a < rt.n_exp; a += blockDim.x) {
     if (rt.act[a] == p.E) continue;
-    int first = 0;
-    const int nr = owned_rows(rt, a, G, &first);
+    const int nr = owned_rows(rt, a, G);
     if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
   }
   return true;
@@ -1103,13 +1111,13 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pt.row_tok = row_tok;
   const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
   const int tid = threadIdx.x;
-  // Unit tables: the expert's tokens in chunks of at most kTileTokens rows
+  // Unit tables: the expert's tokens in chunks of at most kExpertTileTokens rows
   // (one accumulator's width): the shared expert's chunks first, then the
   // routed experts heaviest first (ties: lower id first), so that the
   // longest units are handed out first and do not end the launch; an
   // expert's chunks are adjacent, so its weight tiles are asked for at
   // nearly the same time by the CTAs that take them.
-  const int n_sh = (M + kTileTokens - 1) / kTileTokens;
+  const int n_sh = (M + kExpertTileTokens - 1) / kExpertTileTokens;
   if (tid < E) {
     const int c = pt.cnt[tid];
     if (c > 0) {
@@ -1131,20 +1139,20 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   }
   if (tid < n_sh) {
     c_act[tid] = E;
-    c_off[tid] = MK + tid * kTileTokens;
-    c_cnt[tid] = min(kTileTokens, M - tid * kTileTokens);
+    c_off[tid] = MK + tid * kExpertTileTokens;
+    c_cnt[tid] = min(kExpertTileTokens, M - tid * kExpertTileTokens);
   }
   __syncthreads();
   const int e = tid < n_act ? by_rank[tid] : 0;
   const int ce = tid < n_act ? pt.cnt[e] : 0;
-  const int nch = (ce + kTileTokens - 1) / kTileTokens;
+  const int nch = (ce + kExpertTileTokens - 1) / kExpertTileTokens;
   int n_chunks = 0;
   const int first = n_sh + block_excl_scan(nch, pt.tmp, &n_chunks);
   const bool fits = n_sh + n_chunks <= NC;  // the host sized the tables for the worst case
   for (int c = 0; c < nch && first + c < NC; ++c) {
     c_act[first + c] = e;
-    c_off[first + c] = pt.off[e] + c * kTileTokens;
-    c_cnt[first + c] = min(kTileTokens, ce - c * kTileTokens);
+    c_off[first + c] = pt.off[e] + c * kExpertTileTokens;
+    c_cnt[first + c] = min(kExpertTileTokens, ce - c * kExpertTileTokens);
   }
   if (blockIdx.x == 0) {
     if (!fits && tid == 0) atomicOr(p.err, kErrBadRoute);

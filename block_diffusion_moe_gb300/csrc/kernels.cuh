@@ -24,6 +24,13 @@ constexpr int kRouteChunk = 2048;
 // tcgen05.mma and of one TMEM accumulator).
 constexpr int kMaxTokens = 1024;
 constexpr int kTileTokens = 256;
+// The standalone expert kernel's token tile: an expert's tokens run in
+// chunks of at most this many rows. 128 rather than 256 halves the B stages
+// (16 KiB per K group), which leaves room for a deeper weight ring (the
+// weight stream's rate follows the bytes in flight); an expert with more
+// tokens streams its weights once per chunk, the chunks' requests for the
+// same tile arriving together (the repeat is served by L2).
+constexpr int kExpertTileTokens = 128;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 
