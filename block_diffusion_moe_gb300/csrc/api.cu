@@ -435,13 +435,14 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.E = E;
   xa.K = K;
   const int nb = std::min((M + 15) & ~15, kExpertTileTokens);  // B-tile rows: one chunk at most
-  // Two K groups per A/B stage (8 MMAs per pipeline step instead of 4) when
-  // the token tile is small; 256-token tiles keep one group per stage. The
-  // low-bit path, whose A stages are written by the converter warps rather
-  // than streamed, takes four (a whole staging slot, 16 MMAs per commit).
+  // Two K groups per A/B stage (8 MMAs per pipeline step instead of 4) up to
+  // 128 token columns: every pipeline step (waits, MMAs, commits) has a fixed
+  // cost of ~0.4 µs, so fewer, larger steps stream faster. The low-bit path,
+  // whose A stages are written by the converter warps rather than streamed,
+  // takes four (a whole staging slot, 16 MMAs per commit).
   const bool g4 = q4 && nb <= 64 && (H / 64) % 4 == 0 && (F / 64) % 4 == 0 && xa.kq_gu == 4 && xa.kq_dn == 4;
-  const int kg_gu = g4 ? 4 : ((nb <= 64 && (H / 64) % 2 == 0) ? 2 : 1);
-  const int kg_dn = g4 ? 4 : ((nb <= 64 && (F / 64) % 2 == 0) ? 2 : 1);
+  const int kg_gu = g4 ? 4 : ((nb <= 128 && (H / 64) % 2 == 0) ? 2 : 1);
+  const int kg_dn = g4 ? 4 : ((nb <= 128 && (F / 64) % 2 == 0) ? 2 : 1);
   const int kg = std::max(kg_gu, kg_dn);
   xa.kg_gu = kg_gu;
   xa.kg_dn = kg_dn;
@@ -472,6 +473,11 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     }
   } else if (nb <= 64) {
     sa = sb = static_cast<int>(std::min<size_t>(16, budget / (a_stage + b_stage)));
+  } else if (kg == 2) {
+    // wide B stages: two of them; the weight ring takes the rest
+    sb = 2;
+    const size_t used = static_cast<size_t>(sb) * b_stage;
+    sa = used < budget ? static_cast<int>(std::min<size_t>(16, (budget - used) / a_stage)) : 0;
   } else {
     sb = 3;
     const size_t used = static_cast<size_t>(sb) * b_stage;
