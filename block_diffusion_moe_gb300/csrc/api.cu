@@ -441,8 +441,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   // whose A stages are written by the converter warps rather than streamed,
   // takes four (a whole staging slot, 16 MMAs per commit).
   const bool g4 = q4 && nb <= 64 && (H / 64) % 4 == 0 && (F / 64) % 4 == 0 && xa.kq_gu == 4 && xa.kq_dn == 4;
-  const int kg_gu = g4 ? 4 : ((nb <= 128 && (H / 64) % 2 == 0) ? 2 : 1);
-  const int kg_dn = g4 ? 4 : ((nb <= 128 && (F / 64) % 2 == 0) ? 2 : 1);
+  const int kg2_cols = q4 ? 64 : 128;  // the low-bit path also needs room for its staging ring
+  const int kg_gu = g4 ? 4 : ((nb <= kg2_cols && (H / 64) % 2 == 0) ? 2 : 1);
+  const int kg_dn = g4 ? 4 : ((nb <= kg2_cols && (F / 64) % 2 == 0) ? 2 : 1);
   const int kg = std::max(kg_gu, kg_dn);
   xa.kg_gu = kg_gu;
   xa.kg_dn = kg_dn;
@@ -474,7 +475,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   } else if (nb <= 64) {
     sa = sb = static_cast<int>(std::min<size_t>(16, budget / (a_stage + b_stage)));
   } else if (kg == 2) {
-    // wide B stages: two of them; the weight ring takes the rest
+    // wide B stages (bf16, 65-128 columns): two of them; the weight ring takes the rest
     sb = 2;
     const size_t used = static_cast<size_t>(sb) * b_stage;
     sa = used < budget ? static_cast<int>(std::min<size_t>(16, (budget - used) / a_stage)) : 0;

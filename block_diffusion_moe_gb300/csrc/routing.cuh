@@ -399,9 +399,7 @@ struct PermTables {
 __host__ __device__ constexpr int perm_stride(int M) { return ((M + 31) >> 5) | 1; }
 
 // Builds, with every thread of the CTA (blockDim.x >= E), the permutation of
-// the M*K top-k selections: per-expert token bitmasks (word wd of an expert
-// written by warp wd alone: the lanes that chose the same expert in one
-// selection slot merge their bits), per-expert counts and a prefix count per
+// the M*K top-k selections: per-expert token bitmasks, per-expert counts and a prefix count per
 // word, a scan over experts for the row offsets, and each selection's row =
 // its expert's offset + the number of lower tokens routed to that expert, so
 // rows of one expert are in token order. Returns the number of active
@@ -429,14 +427,11 @@ __device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, i
   }
   for (int i = tid; i < E * ws; i += blockDim.x) t.bm[i] = 0u;
   __syncthreads();
-  for (int wd = warp; wd < nw; wd += blockDim.x >> 5) {
-    const int tk = wd * 32 + lane;
-    for (int k = 0; k < K; ++k) {
-      const int e = tk < M ? t.idx[tk * K + k] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && lane == __ffs(peers) - 1) t.bm[e * ws + wd] |= peers;
-      __syncwarp();
-    }
+  // one shared-memory OR per selection (order-independent, so every CTA gets
+  // the same bits)
+  for (int i = tid; i < MK; i += blockDim.x) {
+    const int tk = i / K;
+    atomicOr(&t.bm[t.idx[i] * ws + (tk >> 5)], 1u << (tk & 31));
   }
   __syncthreads();
   int c = 0;
