@@ -75,6 +75,11 @@ struct Rt {
   int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
   int dense;                // gate/up B operand = all M normed rows
   int chunked;              // standalone: units index chunks of at most kExpertTileTokens rows
+  // standalone: the spare warp gathers this CTA's share of the token rows
+  const uint16_t* row_tok;  // token of every routed row
+  uint16_t* list;           // [n_list] the rows this CTA gathers
+  int n_list;
+  uint64_t* gbar;           // bulk-copy barrier of the gather
 };
 
 __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArgs& p) {
@@ -885,6 +890,96 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
   return *s.tmem_slot;
 }
 
+// Rows of chunk a that this CTA gathers. Pieces of four rows: piece q of
+// chunk a belongs to CTA (7 a + q) mod G, so a CTA owns pieces q0, q0 + G,
+// ... of each chunk (usually at most one: a chunk has at most 32 pieces).
+__device__ __forceinline__ int first_piece(int a, int G) {
+  return static_cast<int>((static_cast<unsigned>(blockIdx.x) + static_cast<unsigned>(G) -
+                           (7u * static_cast<unsigned>(a)) % static_cast<unsigned>(G)) %
+                          static_cast<unsigned>(G));
+}
+
+__device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G) {
+  const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
+  int nr = 0;
+  for (int q = first_piece(a, G); q < n_q; q += G) nr += min(4, cnt - 4 * q);
+  return nr;
+}
+
+// The standalone kernel's spare warp (7), while the other roles start:
+// copies the normed rows of the routed chunks' tokens into expert order (row
+// r of the gathered buffer = normed row of token row_tok[r]), this CTA's
+// share of the pieces. It lists the rows (hottest chunks first), then lane 0
+// moves them with bulk copies through the activation ring (global -> shared
+// -> global, one copy per row each way; the activation producer, which
+// waits at named barrier 5, takes the ring once the copies have read it),
+// waits for the stores, and the warp publishes, per chunk, how many rows
+// this CTA gathered (release). A gate/up unit of the chunk loads them once
+// the chunk's counter reaches its row count; no CTA waits for all others.
+__device__ void gather_warp(const ExpertArgs& p, const Smem& s, const Rt& rt) {
+  const int G = gridDim.x, lane = threadIdx.x & 31;
+  int base = 0;
+  for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
+    const int a = a0 + lane;
+    const bool mine = a < rt.n_exp && rt.act[a] != p.E;
+    const int nr = mine ? owned_rows(rt, a, G) : 0;
+    int incl = nr;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (mine) {
+      int at = base + incl - nr;
+      const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
+      for (int q = first_piece(a, G); q < n_q; q += G)
+        for (int j = 4 * q; j < min(4 * q + 4, cnt); ++j, ++at)
+          if (at < rt.n_list) rt.list[at] = static_cast<uint16_t>(rt.off[a] + j);
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+  const int n_rows = min(base, rt.n_list);
+  int ok = 1;
+  if (lane == 0) {
+    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
+    const int per_round = static_cast<int>((static_cast<uint32_t>(p.stages_b) * s.b_stage_bytes) / row_bytes);
+    const uint32_t ring = smem_u32(s.b_ring);
+    uint32_t phase = 0;
+    for (int r0 = 0; r0 < n_rows; r0 += per_round) {
+      const int n = min(per_round, n_rows - r0);
+      mbar_arrive_expect_tx(rt.gbar, static_cast<uint32_t>(n) * row_bytes);
+      for (int j = 0; j < n; ++j)
+        bulk_load(ring + j * row_bytes, p.xn + static_cast<size_t>(rt.row_tok[rt.list[r0 + j]]) * p.H, row_bytes,
+                  rt.gbar);
+      if (!mbar_wait(rt.gbar, phase, s.abort)) {
+        raise_abort(s, p.err, kErrMbarTimeout);
+        mbar_wait_for(rt.gbar, phase, 200000000ull);  // no copy may still land in the ring
+        ok = 0;
+        break;
+      }
+      phase ^= 1u;
+      for (int j = 0; j < n; ++j)
+        bulk_store(p.xg + static_cast<size_t>(rt.list[r0 + j]) * p.H, ring + j * row_bytes, row_bytes);
+      bulk_commit();
+      bulk_wait_read_all();  // the ring may take the next rows
+    }
+  }
+  __syncwarp();
+  named_bar_arrive(5, 64);  // the activation ring is the B producer's now
+  if (lane == 0) {
+    bulk_wait_all();  // the rows are in global memory
+    fence_proxy_async_global();
+    __threadfence();
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  for (int a = lane; a < rt.n_exp; a += 32) {
+    if (rt.act[a] == p.E) continue;
+    const int nr = owned_rows(rt, a, G);
+    if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
+  }
+}
+
 template <bool kQ4>
 __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -894,12 +989,15 @@ __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s,
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(p, s, rt, tmem_base);
   } else if (warp == 2) {
+    if (rt.gbar != nullptr) named_bar_sync(5, 64);  // after the gather's copies have left the ring
     if (lane == 0) producer_b(p, s, rt);
   } else if (warp < 7) {
     epilogue(p, s, rt, tmem_base);
-  } else if (kQ4 && warp >= 8) {
+  } else if (warp == 7) {
+    if (rt.gbar != nullptr) gather_warp(p, s, rt);  // otherwise warp 7 has no role here
+  } else if (kQ4) {
     converter(p, s, rt);
-  }  // warp 7 has no role here
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -948,100 +1046,6 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 }
 
 }  // namespace
-
-// Rows of chunk a that this CTA gathers. Pieces of four rows: piece q of
-// chunk a belongs to CTA (7 a + q) mod G, so a CTA owns pieces q0, q0 + G,
-// ... of each chunk (usually at most one: a chunk has at most 32 pieces).
-__device__ __forceinline__ int first_piece(int a, int G) {
-  return static_cast<int>((static_cast<unsigned>(blockIdx.x) + static_cast<unsigned>(G) -
-                           (7u * static_cast<unsigned>(a)) % static_cast<unsigned>(G)) %
-                          static_cast<unsigned>(G));
-}
-
-__device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G) {
-  const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
-  int nr = 0;
-  for (int q = first_piece(a, G); q < n_q; q += G) nr += min(4, cnt - 4 * q);
-  return nr;
-}
-
-// Copies the normed rows of the routed chunks' tokens into expert order
-// (row r of the gathered buffer = normed row of token row_tok[r]), this
-// CTA's share of the pieces: warp 0 lists the rows (hottest chunks first),
-// thread 0 moves them with bulk copies through the still idle weight ring
-// (global -> shared -> global, one copy per row each way), waits for the
-// stores, and then every thread publishes, per chunk, how many rows this CTA
-// gathered (release). A gate/up unit of the chunk loads them once the
-// chunk's counter reaches its row count; there is no grid-wide wait. Called
-// by the whole CTA before the roles start. Returns false if a copy timed out.
-__device__ bool gather_chunks(const ExpertArgs& p, const Smem& s, const Rt& rt, const uint16_t* row_tok,
-                              uint64_t* gbar) {
-  const int G = gridDim.x, tid = threadIdx.x, lane = tid & 31;
-  uint16_t* list = reinterpret_cast<uint16_t*>(s.xch);  // the SwiGLU exchange buffer is idle until the first unit
-  const int n_list = 2 * 64 * 20 * 2;
-  __shared__ int s_n, s_ok;
-  if (tid < 32) {
-    int base = 0;
-    for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
-      const int a = a0 + lane;
-      const bool mine = a < rt.n_exp && rt.act[a] != p.E;
-      const int nr = mine ? owned_rows(rt, a, G) : 0;
-      int incl = nr;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (mine) {
-        int at = base + incl - nr;
-        const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
-        for (int q = first_piece(a, G); q < n_q; q += G)
-          for (int j = 4 * q; j < min(4 * q + 4, cnt); ++j, ++at)
-            if (at < n_list) list[at] = static_cast<uint16_t>(rt.off[a] + j);
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) s_n = min(base, n_list);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const int n_rows = s_n;
-    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
-    const int per_round = static_cast<int>((static_cast<uint32_t>(p.smem_a) * s.a_stage_bytes) / row_bytes);
-    const uint32_t ring = smem_u32(s.a_ring);
-    uint32_t phase = 0;
-    int ok = 1;
-    for (int r0 = 0; r0 < n_rows && ok; r0 += per_round) {
-      const int n = min(per_round, n_rows - r0);
-      mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(n) * row_bytes);
-      for (int j = 0; j < n; ++j)
-        bulk_load(ring + j * row_bytes, p.xn + static_cast<size_t>(row_tok[list[r0 + j]]) * p.H, row_bytes, gbar);
-      if (!mbar_wait(gbar, phase, s.abort)) {
-        raise_abort(s, p.err, kErrMbarTimeout);
-        mbar_wait_for(gbar, phase, 200000000ull);  // no copy may still land in the ring
-        ok = 0;
-        break;
-      }
-      phase ^= 1u;
-      for (int j = 0; j < n; ++j)
-        bulk_store(p.xg + static_cast<size_t>(list[r0 + j]) * p.H, ring + j * row_bytes, row_bytes);
-      bulk_commit();
-      bulk_wait_read_all();  // the ring may take the next rows
-    }
-    bulk_wait_all();  // the rows are in global memory
-    fence_proxy_async_global();
-    __threadfence();
-    s_ok = ok;
-  }
-  __syncthreads();
-  if (!s_ok) return false;
-  for (int a = tid; a < rt.n_exp; a += blockDim.x) {
-    if (rt.act[a] == p.E) continue;
-    const int nr = owned_rows(rt, a, G);
-    if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
-  }
-  return true;
-}
 
 // Every CTA calls this last. The CTA that finishes last resets the unit
 // counter and the per-unit-table counters the launch used, so that the next
@@ -1097,6 +1101,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   int* c_act = reinterpret_cast<int*>(s.rt_region + ((2 * MK + 15) & ~15));
   int* c_off = c_act + NC;
   int* c_cnt = c_off + NC;
+  uint16_t* list = reinterpret_cast<uint16_t*>(c_cnt + NC);  // [M*K] rows this CTA gathers
   PermTables pt;
   const int ws = perm_stride(M);
   // (every table starts on a 16-byte boundary of the 1 KiB-aligned ring)
@@ -1173,10 +1178,12 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.n_exp = fits ? n_sh + n_chunks : 0;
   rt.dense = 0;
   rt.chunked = 1;
-  const int n_tab = rt.n_exp;
-  if (!gather_chunks(p, s, rt, row_tok, gbar)) rt.n_exp = 0;  // a CTA whose copies failed takes no units
+  rt.row_tok = row_tok;
+  rt.list = list;
+  rt.n_list = MK;
+  rt.gbar = gbar;
   expert_roles<kQ4>(p, s, rt, tmem_base);
-  exit_reset(p, n_tab, n_tab * ((p.F >> 6) + (p.H >> 7)), true);
+  exit_reset(p, rt.n_exp, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), true);
 }
 
 
@@ -1487,6 +1494,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.n_exp = (*s.abort) ? 0 : *s_nact + 1;  // after a failed barrier no unit runs
   rt.dense = 1;
   rt.chunked = 0;
+  rt.row_tok = nullptr;
+  rt.list = nullptr;
+  rt.n_list = 0;
+  rt.gbar = nullptr;
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
   if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
@@ -1511,7 +1522,9 @@ size_t perm_smem_bytes(int M, int K, int E) {
 }
 
 size_t expert_tables_bytes(int M, int K, int max_chunks) {
-  return ((static_cast<size_t>(2) * M * K + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(3) * max_chunks * 4;
+  // row tokens [M*K] u16, chunk tables 3 x [max_chunks] i32, gather list [M*K] u16
+  return ((static_cast<size_t>(2) * M * K + 15) & ~static_cast<size_t>(15)) + static_cast<size_t>(3) * max_chunks * 4 +
+         ((static_cast<size_t>(2) * M * K + 15) & ~static_cast<size_t>(15));
 }
 
 size_t layer_rt_bytes(int M, int K, int E) { return static_cast<size_t>(4 * M * K + 7 * E + 16) * 4; }

@@ -406,7 +406,7 @@ __host__ __device__ constexpr int perm_stride(int M) { return ((M + 31) >> 5) | 
 // experts; `slot_out` (nullable) receives each selection's row.
 __device__ __forceinline__ int cta_permutation(const int32_t* topk_idx, int M, int K, int E, const PermTables& t,
                                                int32_t* slot_out) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int MK = M * K, nw = (M + 31) >> 5, ws = perm_stride(M);
   // Eight loads in flight per thread before any store: the loads read global
   // memory and the stores shared memory through generic pointers, so the
