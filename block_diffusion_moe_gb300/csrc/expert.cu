@@ -1224,8 +1224,18 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   // Router rows do not depend on earlier kernels: copy this CTA's slices
   // into the (still idle) weight ring before waiting.
   const int my_items = (n_items > static_cast<int>(blockIdx.x)) ? (n_items - 1 - blockIdx.x) / G + 1 : 0;
-  const uint32_t wslice = kRouteExperts * H * 2;
   const uint32_t ring_bytes = static_cast<uint32_t>(p.smem_a) * s.a_stage_bytes;
+  // At the Clover shape a CTA with one item of 8 experts contracts it on the
+  // warp tensor cores: router rows, token rows, normed rows and partials in
+  // the idle ring, the bf16 rows padded by 8 elements (bank-conflict-free
+  // fragment loads).
+  constexpr int kMmaH = 2048;
+  constexpr uint32_t kMmaRow = (kMmaH + 8) * 2;
+  const int my_ne = my_items == 1 ? min(kRouteExperts, E - (static_cast<int>(blockIdx.x) % n_eg) * kRouteExperts) : 0;
+  const bool mma_route = my_items == 1 && H == kMmaH && my_ne == kRouteExperts &&
+                         kRouteExperts * kMmaRow + kRouteTokens * kMmaH * 4 + kRouteTokens * kMmaRow +
+                                 kRouteTokens * kRouteTokens * 8 * 4 <= ring_bytes;
+  const uint32_t wslice = mma_route ? kRouteExperts * kMmaRow : kRouteExperts * H * 2;
   const bool wr_staged = my_items * wslice <= ring_bytes;
   // A CTA with one item also stages that item's token rows (contiguous in
   // x_in) behind its router slices, when they fit.
@@ -1233,6 +1243,8 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   const uint32_t x_off = my_items * wslice;
   const uint32_t x_bytes = my_items == 1 ? static_cast<uint32_t>(min(kRouteTokens, M - xt0)) * H * 4 : 0u;
   const bool x_staged = wr_staged && my_items == 1 && x_off + x_bytes <= ring_bytes;
+  const uint32_t xn_off = x_off + kRouteTokens * kMmaH * 4;            // mma_route: normed rows
+  const uint32_t part_off = xn_off + kRouteTokens * kMmaRow;           // mma_route: partial tiles
   if (threadIdx.x == 0 && wr_staged && my_items > 0) {
     uint32_t bytes = 0;
     for (int j = 0; j < my_items; ++j) {
@@ -1243,7 +1255,12 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     for (int j = 0; j < my_items; ++j) {
       const int eg = (blockIdx.x + j * G) % n_eg;
       const int ne = min(kRouteExperts, E - eg * kRouteExperts);
-      bulk_load(smem_u32(s.a_ring) + j * wslice, p.wr + static_cast<size_t>(eg) * kRouteExperts * H, ne * H * 2, wbar);
+      const bf16* src = p.wr + static_cast<size_t>(eg) * kRouteExperts * H;
+      if (mma_route) {
+        for (int r = 0; r < ne; ++r) bulk_load(smem_u32(s.a_ring) + r * kMmaRow, src + static_cast<size_t>(r) * H, H * 2, wbar);
+      } else {
+        bulk_load(smem_u32(s.a_ring) + j * wslice, src, ne * H * 2, wbar);
+      }
     }
   }
   unsigned long long* st = (kPhaseStamps && blockIdx.x == 0 && threadIdx.x == 0) ? p.stamps : nullptr;
@@ -1281,7 +1298,26 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     atomicOr(p.err, kErrMbarTimeout);
     *s.abort = 1u;
   }
-  for (int item = blockIdx.x, j = 0; item < n_items; item += G, ++j) {
+  if (mma_route && warp < kRouteTokens) {
+    const int item = blockIdx.x;
+    const int eg = item % n_eg, tg = item / n_eg;
+    const int e0 = eg * kRouteExperts;
+    const int t = tg * kRouteTokens + warp;
+    if (x_staged && !mbar_wait(xbar, 0, s.abort)) {
+      atomicOr(p.err, kErrMbarTimeout);
+      *s.abort = 1u;
+    }
+    const float lg = cta_router_item_mma<kMmaH>(smem_u32(s.a_ring + x_off), min(kRouteTokens, M - tg * kRouteTokens),
+                                                p.eps, smem_u32(s.a_ring), smem_u32(s.a_ring + xn_off),
+                                                reinterpret_cast<float*>(s.a_ring + part_off),
+                                                eg == 0 ? p.xn + static_cast<size_t>(tg) * kRouteTokens * H : nullptr,
+                                                warp, lane, 6);
+    if (t < M && lane < kRouteExperts) {
+      const float v = lg + (p.bias ? p.bias[e0 + lane] : 0.f);
+      p.logits[static_cast<size_t>(t) * E + e0 + lane] = v;
+    }
+  }
+  for (int item = blockIdx.x, j = 0; item < n_items && !mma_route; item += G, ++j) {
     const int eg = item % n_eg, tg = item / n_eg;
     const int e0 = eg * kRouteExperts;
     const int ne = min(kRouteExperts, E - e0);

@@ -148,6 +148,103 @@ __device__ __forceinline__ float warp_router_row_smem(uint32_t xr, float eps, ui
   return mine;
 }
 
+// D (16x8, fp32) += A (16x16, bf16, row-major) * B (16x8, bf16, column-major)
+// on the warp's tensor cores. Fragment ownership (g = lane / 4, q = lane % 4):
+// a0 = A[g][2q..2q+1], a1 = A[g+8][2q..], a2 = A[g][2q+8..], a3 = A[g+8][2q+8..];
+// b0 = B[2q..2q+1][g], b1 = B[2q+8..2q+9][g]; d = D[g][2q..2q+1], D[g+8][2q..2q+1].
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Router logits of one routing item on the warp tensor cores, at the Clover
+// shape: up to 8 tokens (fp32 rows of kH, staged in shared memory at x_rows)
+// against 8 experts (bf16 router rows at w_rows, row stride kH + 8
+// elements). Called by warps 0..7 together (named barrier `bar` of 256
+// threads). Warp w normalises token w (xn = bf16(x * rstd), stored into
+// shared memory at xn_rows with the same padded stride, and to
+// xn_out + w * kH when xn_out is non-null; rows past n_tok are zero), then
+// every warp contracts one eighth of the hidden size with mma.sync m16n8k16
+// (tokens x experts; the eight missing token rows of the 16-row tile are
+// zero registers), and the eight partial tiles (part: 8 x 8 x 8 floats) are
+// summed in warp order. The padding puts the eight rows a fragment load
+// touches in different banks. Lane e (< 8) of warp w receives the logit of
+// token w and expert e (without bias).
+template <int kH>
+__device__ __forceinline__ float cta_router_item_mma(uint32_t x_rows, int n_tok, float eps, uint32_t w_rows,
+                                                     uint32_t xn_rows, float* part, __nv_bfloat16* xn_out, int warp,
+                                                     int lane, uint32_t bar) {
+  constexpr int kLd = kH + 8;
+  constexpr int kChunks = kH / 128;
+  static_assert(kH % 128 == 0, "hidden size must be a multiple of 128");
+  const uint32_t my_row = xn_rows + static_cast<uint32_t>(warp * kLd) * 2u;
+  if (warp < n_tok) {
+    float4 xv[kChunks];
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+      const uint32_t a = x_rows + static_cast<uint32_t>(warp * kH + lane * 4 + 128 * j) * 4u;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(xv[j].x), "=f"(xv[j].y), "=f"(xv[j].z), "=f"(xv[j].w)
+                   : "r"(a));
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j)
+      ss += xv[j].x * xv[j].x + xv[j].y * xv[j].y + xv[j].z * xv[j].z + xv[j].w * xv[j].w;
+    ss = warp_sum_f(ss);
+    const float rstd = 1.0f / sqrtf(ss / static_cast<float>(kH) + eps);
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j) {
+      const int c = lane * 4 + 128 * j;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(xv[j].x * rstd, xv[j].y * rstd);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(xv[j].z * rstd, xv[j].w * rstd);
+      const uint32_t ulo = *reinterpret_cast<uint32_t*>(&lo), uhi = *reinterpret_cast<uint32_t*>(&hi);
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(my_row + static_cast<uint32_t>(c) * 2u), "r"(ulo), "r"(uhi)
+                   : "memory");
+      if (xn_out != nullptr) {
+        uint2 pk;
+        pk.x = ulo;
+        pk.y = uhi;
+        *reinterpret_cast<uint2*>(xn_out + static_cast<size_t>(warp) * kH + c) = pk;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kChunks; ++j)
+      asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(my_row + static_cast<uint32_t>(lane * 4 + 128 * j) * 2u),
+                   "r"(0u)
+                   : "memory");
+  }
+  named_bar_sync(bar, 256);
+  const int g = lane >> 2, q = lane & 3;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t xa = xn_rows + static_cast<uint32_t>(g * kLd + 2 * q) * 2u;
+  const uint32_t wa = w_rows + static_cast<uint32_t>(g * kLd + 2 * q) * 2u;
+#pragma unroll 4
+  for (int kb = warp * (kH / 8); kb < (warp + 1) * (kH / 8); kb += 16) {
+    uint32_t a0, a2, b0, b1;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(a0) : "r"(xa + kb * 2u));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(a2) : "r"(xa + (kb + 8) * 2u));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(b0) : "r"(wa + kb * 2u));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(b1) : "r"(wa + (kb + 8) * 2u));
+    mma_bf16_16816(acc, a0, 0u, a2, 0u, b0, b1);
+  }
+  // acc[0], acc[1]: token g, experts 2q and 2q + 1 (acc[2], acc[3]: the zero rows)
+  part[(warp * 8 + g) * 8 + 2 * q] = acc[0];
+  part[(warp * 8 + g) * 8 + 2 * q + 1] = acc[1];
+  named_bar_sync(bar, 256);
+  float lg = 0.f;
+  if (lane < 8) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) lg += part[(w * 8 + warp) * 8 + lane];
+  }
+  return lg;
+}
+
 // One warp, one token row xr: xn = bf16(xr * rstd) (stored to xn_out when
 // non-null) and the router logits of experts w_rows[0..ne) (ne <= 8), each a
 // bf16 row of H. Lane e (< ne) receives logit e (without bias).
@@ -338,18 +435,6 @@ __device__ __forceinline__ void warp_topk_n(const float* const (&rows)[NT], cons
 }
 
 
-// D (16x8, fp32) += A (16x16, bf16, row-major) * B (16x8, bf16, column-major)
-// on the warp's tensor cores. Fragment ownership (g = lane / 4, q = lane % 4):
-// a0 = A[g][2q..2q+1], a1 = A[g+8][2q..], a2 = A[g][2q+8..], a3 = A[g+8][2q+8..];
-// b0 = B[2q..2q+1][g], b1 = B[2q+8..2q+9][g]; d = D[g][2q..2q+1], D[g+8][2q..2q+1].
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of
 // 32, at most 512). Returns the exclusive prefix; *total receives the sum.
