@@ -1,12 +1,12 @@
 """Calls of more than 256 tokens (several 32-position blocks batched), against
 the oracle.
 
-An expert's tokens are processed in tiles of at most 256 (one accumulator's
-width): an expert that more than 256 tokens select runs as several chunks,
-and the head takes the positions in sub-calls of whole blocks. Zipf-biased
-routers make the hot experts carry far more than 256 tokens here, so the
-chunked units, the routing counters for more than 16 token tiles and the
-split head all run. Every call goes through the C ABI."""
+The standalone expert kernel processes an expert's tokens in chunks of at
+most 128 rows, and the head takes the positions in sub-calls of whole blocks
+of at most 256 positions. Zipf-biased routers make the hot experts carry far
+more than 256 tokens here, so multi-chunk experts, the routing counters for
+more than 16 token tiles and the split head all run. Every call goes through
+the C ABI."""
 import dataclasses
 
 import numpy as np
