@@ -680,7 +680,7 @@ def run_ours(args):
         return
     csum = clk.summary()
     fused = n_pos <= 32
-    per_layer = 1 if fused else 2         # fused layer kernel, or route + experts (the combine inside)
+    per_layer = 1 if fused else 3         # fused layer kernel, or route + experts + combine
     if sp.full:
         # embed, layers, the last deferred combine, norm + one head launch per 256 positions
         launches_per_step = 1 + per_layer * n_layers + (1 if fused else 0) + 1 + (n_pos + 255) // 256

@@ -495,10 +495,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.stages_q = sq;
   xa.nb_max = nb;
   // Up to 32 tokens the down unit that completes a hidden slice combines it
-  // (a few µs), or the next fused launch does; with more tokens that serial
-  // walk would dominate, so the standalone kernel ends with one grid barrier
-  // and a combine spread over all CTAs.
-  xa.combine = fused ? (defer ? 2 : 1) : 3;
+  // (a few µs); with more tokens that serial walk would dominate, so a
+  // parallel kernel does it.
+  xa.combine = fused ? (defer ? 2 : 1) : 0;
   xa.pend = pend ? 1 : 0;
   xa.fin_w = reinterpret_cast<float*>(data + L.fin_w);
   size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq, kg);

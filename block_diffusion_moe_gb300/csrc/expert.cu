@@ -706,40 +706,6 @@ __device__ void combine_token(const ExpertArgs& p, const Rt& rt, int j, int t, i
   combine_store(p, t, col, acc, ys, xi);
 }
 
-// Combines (token, 128-wide slice) pieces of the whole call with one warp
-// per piece, two pieces in flight per warp: piece pc, pc + n_warps, ... for
-// the warp with global index w0 = pc. The same fixed order as combine_slice.
-__device__ void combine_spread(const ExpertArgs& p, const Rt& rt, int w0, int n_warps, int lane) {
-  const int SH = p.H >> 7, n = p.M * SH, MK = p.M * p.K, K = p.K;
-  const size_t H = p.H;
-  for (int pc = w0; pc < n; pc += 2 * n_warps) {
-    const int pc2 = pc + n_warps;
-    const bool two = pc2 < n;
-    const int t = pc / SH, t2 = two ? pc2 / SH : t;
-    const size_t col = static_cast<size_t>(pc % SH) * 128 + lane * 4;
-    const size_t col2 = two ? static_cast<size_t>(pc2 % SH) * 128 + lane * 4 : col;
-    const float4 ys = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t) * H + col));
-    const float4 xi = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t) * H + col);
-    float4 ys2 = make_float4(0.f, 0.f, 0.f, 0.f), xi2 = ys2;
-    if (two) {
-      ys2 = __ldcg(reinterpret_cast<const float4*>(p.yslot + static_cast<size_t>(MK + t2) * H + col2));
-      xi2 = *reinterpret_cast<const float4*>(p.x_in + static_cast<size_t>(t2) * H + col2);
-    }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
-    for (int k0 = 0; k0 < K; k0 += 8) {
-      int r[8], r2[8];
-      float wk[8], wk2[8];
-      float4 y[8], y2[8];
-      combine_loads(p, rt, t, col, k0, r, wk, y);
-      if (two) combine_loads(p, rt, t2, col2, k0, r2, wk2, y2);
-      combine_accumulate(acc, wk, y, k0, K);
-      if (two) combine_accumulate(acc2, wk2, y2, k0, K);
-    }
-    combine_store(p, t, col, acc, ys, xi);
-    if (two) combine_store(p, t2, col2, acc2, ys2, xi2);
-  }
-}
-
 __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;             // TMEM lane quarter this warp may read
@@ -1217,15 +1183,6 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.n_list = MK;
   rt.gbar = gbar;
   expert_roles<kQ4>(p, s, rt, tmem_base);
-  if (p.combine == 3) {
-    // The call's combine: once every CTA's units are stored (one grid
-    // barrier), all CTAs sum the (token, 128-wide slice) pieces.
-    const bool ok = grid_barrier(p.bar_count, p.err);
-    if (ok) {
-      const int nw = blockDim.x >> 5;
-      combine_spread(p, rt, blockIdx.x + gridDim.x * (tid >> 5), gridDim.x * nw, tid & 31);
-    }
-  }
   exit_reset(p, rt.n_exp, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), true);
 }
 

@@ -151,8 +151,7 @@ struct ExpertArgs {
   int M, H, F, E, K;
   int stages_a, stages_b, nb_max;  // ring depths and B-tile rows per stage
   int combine;  // 1: the down unit that completes a hidden slice combines it; 0: k_combine does;
-                // 2 (fused kernel): no combine here, the final tables are published for a later one;
-                // 3 (standalone kernel): a grid barrier after the units, then every CTA combines
+                // 2 (fused kernel): no combine here, the final tables are published for a later one
   int pend;     // fused kernel: first combine the previous launch's deferred output (same workspace)
   float* fin_w; // [M][K] final selection weights published for a deferred combine
   // fused-layer launches only (k_layer)
