@@ -465,6 +465,8 @@ def run_ours(args):
         draft[3::4] = torch.randint(0, D.vocab, (len(range(3, n_pos, 4)),), generator=g).to(torch.int32).to(dev)
         draft[-1] = -1
     tokens, masked = synth.masked_block(D, n_pos, dev)
+    head_out = (clover.lmhead_unmask(D, head_w, x_fixed, tokens.clone(), masked.clone(), block=M, ws=ws)
+                if kind == "head" else None)
 
     # ---- block states for the full step: K copies of the block at evenly
     # spaced points of its loop, prepared by one walk through a block
@@ -501,7 +503,7 @@ def run_ours(args):
         elif kind == "accept":
             clover.lmhead_accept(D, head_w, x_fixed, draft, n_pos, clover.ACCEPT_EXACT, ws=ws, out=acc_out)
         else:
-            clover.lmhead_unmask(D, head_w, x_fixed, tokens, masked, block=M, ws=ws)
+            clover.lmhead_unmask(D, head_w, x_fixed, tokens, masked, block=M, ws=ws, out=head_out)
 
     if not sp.full:
         for _ in range(W):

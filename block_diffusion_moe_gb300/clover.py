@@ -227,16 +227,20 @@ def moe_block_step(d: synth.Dims, layer: synth.Layer, x_in: torch.Tensor, x_out:
 
 
 def lmhead_unmask(d: synth.Dims, head_w, x, tokens, masked, logit_scale=None, threshold: float = 0.95,
-                  block: int = 32, ws=None, stream=None) -> dict:
+                  block: int = 32, ws=None, stream=None, out=None) -> dict:
+    """Head statistics + unmask over M = x.shape[0] positions. `out` (a dict
+    this function returned before, for the same M) is reused; the library
+    writes every entry, including the committed count."""
     M = x.shape[0]
     dev = x.device
     if ws is None:
         ws = workspace(head_workspace_bytes(d, M), dev)
-    out = {"argmax": torch.empty(M, dtype=torch.int32, device=dev),
-           "max_logit": torch.empty(M, dtype=torch.float32, device=dev),
-           "lse": torch.empty(M, dtype=torch.float32, device=dev),
-           "max_prob": torch.empty(M, dtype=torch.float32, device=dev),
-           "n_committed": torch.zeros(1, dtype=torch.int32, device=dev)}
+    if out is None:
+        out = {"argmax": torch.empty(M, dtype=torch.int32, device=dev),
+               "max_logit": torch.empty(M, dtype=torch.float32, device=dev),
+               "lse": torch.empty(M, dtype=torch.float32, device=dev),
+               "max_prob": torch.empty(M, dtype=torch.float32, device=dev),
+               "n_committed": (torch.empty if M > 0 else torch.zeros)(1, dtype=torch.int32, device=dev)}
     dims = make_dims(d)
     _check(lib().clover_lmhead_unmask(ctypes.byref(dims), _ptr(head_w), _ptr(x), _ptr(logit_scale), threshold, block,
                                       _ptr(tokens), _ptr(masked), _ptr(out["argmax"]), _ptr(out["max_logit"]),

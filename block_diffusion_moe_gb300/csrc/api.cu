@@ -360,6 +360,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
 
   ExpertArgs xa;
   memset(&xa, 0, sizeof(xa));
+  xa.acc_cols = 256;
   const int R = MK + M;
   int rc;
   const bool q4 = layer_is_q4(layer);
@@ -468,6 +469,15 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     // stages one slot fills, the same for both unit kinds).
     const int per_slot_gu = xa.kq_gu / kg_gu, per_slot_dn = xa.kq_dn / kg_dn;
     xa.q_teams = 1;
+    if (fused && kg == 4) {
+      // A tiles in tensor memory (two 64-column accumulators, then the two
+      // 128-column A stages); the staging slots take the A ring, which the
+      // routing prelude uses before any slot is loaded.
+      xa.a_tmem = 1;
+      xa.q_in_a = 1;
+      xa.acc_cols = 64;
+      sq = static_cast<int>(std::min<size_t>(24, static_cast<size_t>(sa) * a_stage / kQSlotBytes));
+    }
     if (per_slot_gu == per_slot_dn && sa % (2 * per_slot_gu) == 0 && sq >= 2) {
       sq &= ~1;
       xa.q_teams = 2;
@@ -500,7 +510,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.combine = fused ? (defer ? 2 : 1) : 0;
   xa.pend = pend ? 1 : 0;
   xa.fin_w = reinterpret_cast<float*>(data + L.fin_w);
-  size_t smem = expert_smem_bytes(smem_a, sa, sb, nb, sq, kg);
+  // (slots inside the A ring add only their barriers)
+  size_t smem = xa.q_in_a ? expert_smem_bytes(smem_a, sa, sb, nb, 0, kg) + static_cast<size_t>(2 * sq) * 8
+                          : expert_smem_bytes(smem_a, sa, sb, nb, sq, kg);
   if (fused) {
     xa.wr = reinterpret_cast<const bf16*>(layer.router_w);
     xa.wr_next = reinterpret_cast<const bf16*>(next_router);

@@ -168,8 +168,9 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ExpertArgs& p) {
   s.a_stage_bytes = static_cast<uint32_t>(kATileBytes) * static_cast<uint32_t>(p.kg_stage);
   s.a_ring = base;
   s.b_ring = s.a_ring + static_cast<size_t>(p.smem_a) * s.a_stage_bytes;
-  s.q_ring = s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes;  // 1 KiB aligned
-  s.xch = reinterpret_cast<float*>(s.q_ring + static_cast<size_t>(p.stages_q) * kQSlotBytes);
+  uint8_t* after_b = s.b_ring + static_cast<size_t>(p.stages_b) * s.b_stage_bytes;  // 1 KiB aligned
+  s.q_ring = p.q_in_a ? s.a_ring : after_b;
+  s.xch = reinterpret_cast<float*>(p.q_in_a ? after_b : after_b + static_cast<size_t>(p.stages_q) * kQSlotBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(s.xch + 2 * 64 * 20);
   s.full_a = bars;
   s.empty_a = s.full_a + p.stages_a;
@@ -328,8 +329,11 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
 // Each pair of codes becomes a bf16x2 by the exponent trick
 // (0x4300 | u = 128 + u), then (128 + u) - 136 = u - 8 exactly and one bf16
 // multiply by the scale gives bf16((u - 8) s). The row is written in the
-// 128-byte swizzle the TMA would have used, so the MMA is unchanged.
-__device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
+// 128-byte swizzle the TMA would have used, so the MMA is unchanged; or, with
+// p.a_tmem, into tensor memory (the thread's own lane, 32 columns per group),
+// where the MMA reads A directly: no shared-memory stores, no proxy fence,
+// and the MMA reads only B from shared memory.
+__device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   // With p.q_teams == 2 two teams of four warps take the staging slots in
   // turn (team t: slots t, t + 2, ...). The host enables this only when the
   // slot count is even and the bf16 stage count a multiple of twice the
@@ -389,6 +393,7 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
           raise_abort(s, p.err, kErrMbarTimeout);
           ok = false;
         }
+        if (h == 0 && p.a_tmem) tc_fence_after();  // the MMAs that read this stage are complete
         if (ok) {
           // 128-byte code rows (kq = 4) arrive in the 128-byte swizzle
           const uint8_t* src = slot + r * kq * 32;
@@ -409,14 +414,26 @@ __device__ void converter(const ExpertArgs& p, const Smem& s, const Rt& rt) {
               o[4 * j + i] = *reinterpret_cast<const uint32_t*>(&v);
             }
           }
-          uint8_t* row = s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes + r * 128;
+          if (p.a_tmem) {
+            // lane r of the stage's columns (the warp's lane quarter is r / 32)
+            tmem_st32(tmem_base + (static_cast<uint32_t>(r & ~31) << 16) + static_cast<uint32_t>(kTmemAStage0) +
+                          static_cast<uint32_t>(sa) * 128u + static_cast<uint32_t>(h) * 32u,
+                      o);
+          } else {
+            uint8_t* row = s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes + r * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) =
-                make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(row + ((j ^ (r & 7)) << 4)) =
+                  make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          }
         }
         if (h == kg - 1) {
-          fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
+          if (p.a_tmem) {
+            tmem_wait_st();     // this thread's columns are written
+            tc_fence_before();  // ordered before the arrival the MMA waits on
+          } else {
+            fence_proxy_async_shared();  // the MMA reads the tile through the async proxy
+          }
           __syncwarp();
           if (lane == 0 && ok) mbar_arrive(&s.full_a[sa]);
           if (++sa == SA) {
@@ -564,7 +581,7 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uin
       break;
     }
     tc_fence_after();
-    const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * 256u;
+    const uint32_t d = tmem_base + static_cast<uint32_t>(acc) * static_cast<uint32_t>(p.acc_cols);
     bool ok = true;
     const int kg = unit_kg(w, p);
     for (int kc = 0; kc < nk; kc += kg) {
@@ -577,11 +594,20 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uin
       for (int h = 0; h < kg; ++h) {
         const uint64_t bd =
             umma_desc_sw128(smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes + h * s.b_half_bytes));
-        const uint64_t ad = umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes));
+        if (p.a_tmem) {
+          const uint32_t at = tmem_base + static_cast<uint32_t>(kTmemAStage0) + static_cast<uint32_t>(sa) * 128u +
+                              static_cast<uint32_t>(h) * 32u;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                    (kc | h | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)
+            umma_bf16_ta(d, at + 8u * k, bd + static_cast<uint64_t>(2 * k), idesc, (kc | h | k) != 0 ? 1u : 0u);
+        } else {
+          const uint64_t ad =
+              umma_desc_sw128(smem_u32(s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + h * kATileBytes));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_bf16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                      (kc | h | k) != 0 ? 1u : 0u);
+        }
       }
       umma_commit(&s.empty_a[sa]);
       umma_commit(&s.empty_b[sb]);
@@ -740,7 +766,8 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
     named_bar_sync(1, 128);
     if (!*s.s_ok) break;
     tc_fence_after();
-    const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * 256u;
+    const uint32_t tb =
+        tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * static_cast<uint32_t>(p.acc_cols);
     if (w.kind == 0) {
       // Rows 0..63 of the tile are gate rows f, rows 64..127 the up rows of
       // the same f. Per 32 columns the gate warps take columns 0..15 and the
@@ -996,7 +1023,7 @@ __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s,
   } else if (warp == 7) {
     if (rt.gbar != nullptr) gather_warp(p, s, rt);  // otherwise warp 7 has no role here
   } else if (kQ4) {
-    converter(p, s, rt);
+    converter(p, s, rt, tmem_base);
   }
   tc_fence_before();
   __syncthreads();

@@ -52,6 +52,9 @@ constexpr int kATileBytes = 128 * 64 * 2;  // 128 rows x 64 bf16
 constexpr int kQGroupBytes = 128 * 32 + 128 * 2;
 constexpr int kQSlotGroups = 4;
 constexpr int kQSlotBytes = kQSlotGroups * kQGroupBytes;
+// First TMEM column of the A stages when A lives in tensor memory (after the
+// two 64-column accumulators); each stage of four K groups takes 128 columns.
+constexpr int kTmemAStage0 = 128;
 constexpr int kSmemBudget = 227 * 1024;
 
 // Phase timestamps of the fused layer kernel (a diagnostic: a barrier and
@@ -124,6 +127,13 @@ struct ExpertArgs {
   int q4, stages_q;
   int q_teams;  // converter teams (1 or 2; 2 only when every team owns its stages and slots)
   int kq_gu, kq_dn;  // K groups per staging slot for gate/up and down units (1, 2 or 4)
+  // Low-bit, fused kernel, four K groups per stage: the converters write the
+  // bf16 A tiles into tensor memory (columns kTmemAStage0 + 128 s for stage
+  // s) and the MMA reads A from there; the staging slots then take the A
+  // ring's shared memory, which only the prelude uses.
+  int a_tmem;
+  int q_in_a;
+  int acc_cols;  // TMEM columns per accumulator: 256, or 64 with a_tmem
   int smem_a;  // A stages in shared memory (= stages_a)
   // K groups of 64 per A/B stage (1, 2, or 4 on the low-bit path) for
   // gate/up and down units; a stage holds kg_stage groups of room (part h
