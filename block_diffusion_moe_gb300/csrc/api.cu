@@ -674,9 +674,12 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
     ha.stages = static_cast<int>(std::min<size_t>(
         8 / kg, (static_cast<size_t>(kSmemBudget) - fixed) / (kg * (kATileBytes + static_cast<size_t>(nb) * 128))));
     const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
-    // The final merge reuses the ring for 12 (accept: 20) bytes x 32 positions x grid.
-    if (ha.stages < 1 || static_cast<size_t>(ha.stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) <
-                             static_cast<size_t>(grid) * 32 * (accept ? 20 : 12))
+    // The final merge reuses the ring for 12 (accept: 20) bytes x grid per
+    // position, 64 positions per round where they fit, else 32.
+    const size_t ring = static_cast<size_t>(std::max(ha.stages, 0)) * kg * (kATileBytes + static_cast<size_t>(nb) * 128);
+    const size_t per_pos = static_cast<size_t>(grid) * (accept ? 20 : 12);
+    ha.merge_rows = (m > 32 && ring >= 64 * per_pos) ? 64 : 32;
+    if (ha.stages < 1 || ring < 32 * per_pos)
       return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
     e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept, kg), stream, kPdl);
     if (e != cudaSuccess) return cuda_fail(e, "launch head");

@@ -207,6 +207,7 @@ struct HeadArgs {
   int accumulate;  // 1: add this call's counts to *n_committed / *n_masked_left (a later sub-call of a split call)
   int kg;     // K groups of 64 per pipeline stage (1 or 2)
   int x_box;  // rows per TMA box of the normed positions (a multiple of 16)
+  int merge_rows;  // positions per round of the last CTA's merge (32 or 64; G x rows partials fit the ring)
   float threshold;
   // Accept mode (self-speculative verify): blocks of `block` rows, row j
   // testing draft[j]; the unmask fields above are unused then.
