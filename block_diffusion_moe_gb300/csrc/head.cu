@@ -13,7 +13,8 @@
 // N side). The epilogue turns each 128 x N accumulator into per-position
 // (max, sum of exp relative to the max, argmax) and folds it into a running
 // per-CTA state, so the logits never leave the SM. The last CTA to finish
-// merges the G partial states in CTA order, derives log-sum-exp and the
+// merges the G partial states (maximum first, then the sums rescaled to it,
+// several threads per position combined in a fixed order), derives log-sum-exp and the
 // maximum probability, and applies the unmask rule to every block of
 // positions. Ties in the argmax go to the lowest vocabulary id at every level.
 //
@@ -49,7 +50,7 @@ struct HeadSmem {
   float* run_t;   // [nb]
   float* run_zd;  // [nb]
   float* tr;      // [4][32][33] per-warp transpose tiles
-  uint64_t *full, *empty, *tfull, *tempty, *drain;
+  uint64_t *full, *empty, *tfull, *tempty, *drain, *mrg;  // mrg: the last CTA's partial copies
   uint32_t* tmem_slot;
   volatile uint32_t* abort;
   volatile int* s_ok;
@@ -85,7 +86,8 @@ __device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int n
   s.tfull = s.empty + p.stages;
   s.tempty = s.tfull + 2;
   s.drain = s.tempty + 2;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+  s.mrg = s.drain + 1;
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.mrg + 1);
   s.abort = s.tmem_slot + 1;
   s.s_ok = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
   s.s_last = s.s_ok + 1;
@@ -434,10 +436,12 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   __threadfence();
   // The pipeline is drained, so the ring's shared memory is free: stage the
   // G partials of up to R positions at a time, then merge each position's
-  // partials in CTA order. The loads are issued in batches of 8 per thread
-  // before any of them is stored (a store to shared memory through a generic
-  // pointer would otherwise hold back the next L2 load, one round trip per
-  // element: ~14 us per 32 positions).
+  // partials. With rows of 16-byte multiples (M % 4 == 0) every (CTA, array)
+  // row of the round is one bulk copy, all in flight at once against one
+  // barrier; otherwise the loads are issued in batches of 8 per thread before
+  // any of them is stored (a store to shared memory through a generic pointer
+  // would hold back the next L2 load). Element loads cost one L2 round trip
+  // per batch, ~24 us per round of 64 positions; the copies about one.
   const int R = p.merge_rows;
   float* pm_s = reinterpret_cast<float*>(s.ring);
   float* ps_s = pm_s + G * R;
@@ -445,10 +449,36 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   float* pt_s = reinterpret_cast<float*>(pa_s + G * R);
   float* pz_s = pt_s + G * R;
   constexpr int kBatch = 8;
+  const bool bulk = (p.M & 3) == 0;
+  uint32_t mrg_phase = 0;
   for (int n0 = 0; n0 < p.M; n0 += R) {
     const int cnt = min(R, p.M - n0);
     const int tot = G * cnt;
-    for (int i0 = etid; i0 < tot; i0 += 128 * kBatch) {
+    if (bulk) {
+      const int n_arr = kAccept ? 5 : 3;
+      const uint32_t row_bytes = static_cast<uint32_t>(cnt) * 4u;
+      if (etid == 0) mbar_arrive_expect_tx(s.mrg, static_cast<uint32_t>(G * n_arr) * row_bytes);
+      named_bar_sync(1, 128);      // the expected bytes are registered before any copy lands
+      fence_proxy_async_global();  // the partials (generic writes) are read by the copies
+      for (int i = etid; i < G * n_arr; i += 128) {
+        const int arr = i / G, b = i - arr * G;
+        const size_t g = static_cast<size_t>(b) * p.M + n0;
+        const void* src = arr == 0   ? static_cast<const void*>(p.part_m + g)
+                          : arr == 1 ? static_cast<const void*>(p.part_s + g)
+                          : arr == 2 ? static_cast<const void*>(p.part_a + g)
+                          : arr == 3 ? static_cast<const void*>(p.part_t + g)
+                                     : static_cast<const void*>(p.part_zd + g);
+        float* dst = arr == 0   ? pm_s
+                     : arr == 1 ? ps_s
+                     : arr == 2 ? reinterpret_cast<float*>(pa_s)
+                     : arr == 3 ? pt_s
+                                : pz_s;
+        bulk_load(smem_u32(dst + b * R), src, row_bytes, s.mrg);
+      }
+      if (!mbar_wait(s.mrg, mrg_phase, s.abort)) atomicOr(p.err, kErrMbarTimeout);
+      mrg_phase ^= 1u;
+    }
+    for (int i0 = etid; !bulk && i0 < tot; i0 += 128 * kBatch) {
       float vm[kBatch], vs[kBatch], vt[kBatch], vz[kBatch];
       int va[kBatch];
 #pragma unroll
@@ -482,36 +512,76 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
       }
     }
     named_bar_sync(1, 128);
-    if (etid < cnt) {
-      const int n = n0 + etid;
-      float m = -INFINITY, sm = 0.f, t = 0.f, zd = -INFINITY;
+    {
+      // T consecutive threads per position (T = 128 / R), each over a
+      // contiguous range of CTAs: first the maximum and its token (ties to
+      // the lower id), then the sums rescaled to that maximum, each term
+      // independent of the others, so the exponentials pipeline instead of
+      // forming one 152-long dependency chain per position. The partial
+      // results combine in a fixed butterfly, so the outcome does not depend
+      // on timing.
+      const int T = 128 / R;
+      const int j = etid / T, q = etid - j * T;
+      const bool live = j < cnt;
+      const int b0 = (G * q) / T, b1 = (G * (q + 1)) / T;
+      float m = -INFINITY;
       int a = 0x7fffffff;
-      for (int b = 0; b < G; ++b) {
-        if (kAccept) {
-          lse_merge_t(m, sm, t, a, pm_s[b * R + etid], ps_s[b * R + etid], pt_s[b * R + etid],
-                      pa_s[b * R + etid]);
-          zd = fmaxf(zd, pz_s[b * R + etid]);
-        } else {
-          lse_merge(m, sm, a, pm_s[b * R + etid], ps_s[b * R + etid], pa_s[b * R + etid]);
+      if (live)
+        for (int b = b0; b < b1; ++b) {
+          const float v = pm_s[b * R + j];
+          const int ai = pa_s[b * R + j];
+          if (v > m || (v == m && ai < a)) {
+            m = v;
+            a = ai;
+          }
+        }
+      for (int o = 1; o < T; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+        if (m2 > m || (m2 == m && a2 < a)) {
+          m = m2;
+          a = a2;
         }
       }
-      const float lse = m + logf(sm);
-      const float pmax = 1.0f / sm;  // = exp(m - lse)
-      if (p.argmax) p.argmax[n] = a;
-      if (p.max_logit) p.max_logit[n] = m;
-      if (p.lse) p.lse[n] = lse;
-      if (p.max_prob) p.max_prob[n] = pmax;
-      if (kAccept) {
-        const float ent = fmaxf(logf(sm) - t / sm, 0.f);  // t <= 0
-        const float pd = expf(zd - lse);                   // 0 for a draft never seen
-        if (p.entropy) p.entropy[n] = ent;
-        if (p.p_draft) p.p_draft[n] = pd;
-        s.run_m[n] = pd;
-        s.run_s[n] = ent;
-      } else {
-        s.run_m[n] = pmax;  // reuse: per-position max probability
+      float sm = 0.f, t = 0.f, zd = -INFINITY;
+      if (live && m != -INFINITY)
+        for (int b = b0; b < b1; ++b) {
+          const float mb = pm_s[b * R + j];
+          if (mb == -INFINITY) continue;  // an empty partial (s = t = 0)
+          const float f = expf(mb - m);
+          sm += ps_s[b * R + j] * f;
+          if (kAccept) {
+            t += f * (pt_s[b * R + j] + (mb - m) * ps_s[b * R + j]);
+            zd = fmaxf(zd, pz_s[b * R + j]);
+          }
+        }
+      for (int o = 1; o < T; o <<= 1) {
+        sm += __shfl_xor_sync(0xffffffffu, sm, o);
+        if (kAccept) {
+          t += __shfl_xor_sync(0xffffffffu, t, o);
+          zd = fmaxf(zd, __shfl_xor_sync(0xffffffffu, zd, o));
+        }
       }
-      s.run_a[n] = a;
+      if (live && q == 0) {
+        const int n = n0 + j;
+        const float lse = m + logf(sm);
+        const float pmax = 1.0f / sm;  // = exp(m - lse)
+        if (p.argmax) p.argmax[n] = a;
+        if (p.max_logit) p.max_logit[n] = m;
+        if (p.lse) p.lse[n] = lse;
+        if (p.max_prob) p.max_prob[n] = pmax;
+        if (kAccept) {
+          const float ent = fmaxf(logf(sm) - t / sm, 0.f);  // t <= 0
+          const float pd = expf(zd - lse);                   // 0 for a draft never seen
+          if (p.entropy) p.entropy[n] = ent;
+          if (p.p_draft) p.p_draft[n] = pd;
+          s.run_m[n] = pd;
+          s.run_s[n] = ent;
+        } else {
+          s.run_m[n] = pmax;  // reuse: per-position max probability
+        }
+        s.run_a[n] = a;
+      }
     }
     named_bar_sync(1, 128);
   }
@@ -601,6 +671,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
       mbar_init(&s.tempty[i], 4);  // one arrival per epilogue warp
     }
     mbar_init(s.drain, 1);
+    mbar_init(s.mrg, 1);
     *s.abort = 0u;
     fence_mbar_init();
   }
@@ -640,7 +711,7 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
 size_t head_smem_bytes(int stages, int nb, bool accept, int kg) {
   return 1024 + static_cast<size_t>(stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) +
          static_cast<size_t>(nb) * (4 * 12 + 12 + 4 + (accept ? 4 * 8 + 8 : 0)) + 4 * 32 * 33 * sizeof(float) +
-         static_cast<size_t>(2 * stages + 5) * 8 + 64;
+         static_cast<size_t>(2 * stages + 6) * 8 + 64;
 }
 
 cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl) {
