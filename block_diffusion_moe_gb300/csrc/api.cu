@@ -321,7 +321,8 @@ int resident_per_sm(bool fused, bool q4, size_t smem, int* out) {
 // launch on the same workspace (which takes `pend`) or to enqueue_combine.
 int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const float* x_in, float* x_out,
                       int32_t* out_idx, float* out_w, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
-                      cudaStream_t stream, const void* next_router = nullptr, bool defer = false, bool pend = false) {
+                      cudaStream_t stream, const void* next_router = nullptr, bool defer = false, bool pend = false,
+                      bool xn_ready = false, bool norm_next = false) {
   const MoeLayout L = moe_layout(d, M);
   const int H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
   const int MK = M * K;
@@ -353,6 +354,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     ra.E = E;
     ra.K = K;
     ra.eps = d.rms_eps;
+    ra.xn_ready = xn_ready ? 1 : 0;
     e = launch_route(ra, stream, kPdl);
     if (e != cudaSuccess) return cuda_fail(e, "launch route");
 
@@ -449,6 +451,14 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.kg_gu = kg_gu;
   xa.kg_dn = kg_dn;
   xa.kg_stage = kg;
+  // Above 256 tokens, hot experts in chunks of up to 256 rows where a B
+  // stage (two K groups of 128 rows) holds one K group of 256: their weights
+  // then stream half as often. At 256 tokens the narrower chunks are faster
+  // (the hottest expert's units run in parallel on more SMs and do not end
+  // the launch).
+  xa.tile_rows = (!fused && !q4 && M > 2 * kExpertTileTokens && kg_gu == 2 && kg_dn == 2 && nb == kExpertTileTokens)
+                     ? 2 * kExpertTileTokens
+                     : kExpertTileTokens;
   const size_t a_stage = static_cast<size_t>(kg) * kATileBytes;
   const size_t b_stage = static_cast<size_t>(kg) * nb * 128;
   const size_t tables = fused ? layer_rt_bytes(M, K, E) : expert_tables_bytes(M, K, n_chunks);
@@ -549,6 +559,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   if (e != cudaSuccess) return cuda_fail(e, fused ? "launch layer" : "launch expert");
   if (!xa.combine) {
     CombineArgs ca;
+    memset(&ca, 0, sizeof(ca));
     ca.x_in = x_in;
     ca.x_out = x_out;
     ca.yslot = xa.yslot;
@@ -557,7 +568,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     ca.M = M;
     ca.H = H;
     ca.K = K;
-    e = launch_combine(ca, stream, kPdl);
+    ca.xn_out = norm_next ? xg + static_cast<size_t>(MK) * H : nullptr;
+    ca.eps = d.rms_eps;
+    e = norm_next ? launch_combine_norm(ca, stream, kPdl) : launch_combine(ca, stream, kPdl);
     if (e != cudaSuccess) return cuda_fail(e, "launch combine");
   }
   if (g_prof.end && g_prof.cap > 0) {
@@ -572,6 +585,7 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
 int enqueue_combine(const clover_dims& d, float* x, int M, uint8_t* data, cudaStream_t stream) {
   const MoeLayout L = moe_layout(d, M);
   CombineArgs ca;
+  memset(&ca, 0, sizeof(ca));
   ca.x_in = x;
   ca.x_out = x;
   ca.yslot = reinterpret_cast<float*>(data + L.yslot);
@@ -747,10 +761,15 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
   // rows instead of a serial walk at the end of the launch); the last one is
   // a combine kernel.
   const bool defer = plan::moe_fused(M, dims->n_experts, plan.sms);
+  // Above 32 positions each layer's combine also writes the next layer's
+  // normed rows, which the next routing kernel copies instead of
+  // normalising them again in every expert tile.
+  const bool chain_norm = !defer && dims->hidden <= kRouteChunk;
   for (int l = 0; l < n_layers; ++l) {
     rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,
                            reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s,
-                           l + 1 < n_layers ? layers[l + 1].router_w : nullptr, defer, defer && l > 0);
+                           l + 1 < n_layers ? layers[l + 1].router_w : nullptr, defer, defer && l > 0,
+                           chain_norm && l > 0, chain_norm && l + 1 < n_layers);
     if (rc) return rc;
   }
   if (defer && n_layers > 0 && (rc = enqueue_combine(*dims, x, M, ws + L.moe, s))) return rc;

@@ -74,7 +74,7 @@ struct Rt {
   const float* topk_w;      // [M][K] weight of each selection
   int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
   int dense;                // gate/up B operand = all M normed rows
-  int chunked;              // standalone: units index chunks of at most kExpertTileTokens rows
+  int chunked;              // standalone: units index chunks of at most p.tile_rows rows
   // standalone: the spare warp gathers this CTA's share of the token rows
   const uint16_t* row_tok;  // token of every routed row
   uint16_t* list;           // [n_list] the rows this CTA gathers
@@ -128,7 +128,10 @@ __device__ __forceinline__ int unit_kq(const Unit& w, const ExpertArgs& p) {
 }
 
 // K groups per A/B stage of a unit (1, 2 or 4).
-__device__ __forceinline__ int unit_kg(const Unit& w, const ExpertArgs& p) { return w.kind == 0 ? p.kg_gu : p.kg_dn; }
+__device__ __forceinline__ int unit_kg(const Unit& w, const ExpertArgs& p) {
+  if (w.cnt > kExpertTileTokens) return 1;  // a wide chunk: one K group fills a B stage
+  return w.kind == 0 ? p.kg_gu : p.kg_dn;
+}
 
 // Granularity of a unit's K walk: a low-bit slot (kq groups, a multiple of
 // kg) or one A/B stage (kg groups).
@@ -1143,13 +1146,14 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pt.row_tok = row_tok;
   const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
   const int tid = threadIdx.x;
-  // Unit tables: the expert's tokens in chunks of at most kExpertTileTokens rows
+  // Unit tables: the expert's tokens in chunks of at most p.tile_rows rows
   // (one accumulator's width): the shared expert's chunks first, then the
   // routed experts heaviest first (ties: lower id first), so that the
   // longest units are handed out first and do not end the launch; an
   // expert's chunks are adjacent, so its weight tiles are asked for at
   // nearly the same time by the CTAs that take them.
-  const int n_sh = (M + kExpertTileTokens - 1) / kExpertTileTokens;
+  const int TR = p.tile_rows;
+  const int n_sh = (M + TR - 1) / TR;
   if (tid < E) {
     const int c = pt.cnt[tid];
     if (c > 0) {
@@ -1171,20 +1175,20 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   }
   if (tid < n_sh) {
     c_act[tid] = E;
-    c_off[tid] = MK + tid * kExpertTileTokens;
-    c_cnt[tid] = min(kExpertTileTokens, M - tid * kExpertTileTokens);
+    c_off[tid] = MK + tid * TR;
+    c_cnt[tid] = min(TR, M - tid * TR);
   }
   __syncthreads();
   const int e = tid < n_act ? by_rank[tid] : 0;
   const int ce = tid < n_act ? pt.cnt[e] : 0;
-  const int nch = (ce + kExpertTileTokens - 1) / kExpertTileTokens;
+  const int nch = (ce + TR - 1) / TR;
   int n_chunks = 0;
   const int first = n_sh + block_excl_scan(nch, pt.tmp, &n_chunks);
   const bool fits = n_sh + n_chunks <= NC;  // the host sized the tables for the worst case
   for (int c = 0; c < nch && first + c < NC; ++c) {
     c_act[first + c] = e;
-    c_off[first + c] = pt.off[e] + c * kExpertTileTokens;
-    c_cnt[first + c] = min(kExpertTileTokens, ce - c * kExpertTileTokens);
+    c_off[first + c] = pt.off[e] + c * TR;
+    c_cnt[first + c] = min(TR, ce - c * TR);
   }
   if (blockIdx.x == 0) {
     if (!fits && tid == 0) atomicOr(p.err, kErrBadRoute);

@@ -92,6 +92,7 @@ struct RouteArgs {
   float* topk_w;        // [M][K]
   int M, H, E, K;
   float eps;
+  int xn_ready;  // 1: xn_rows already hold the normed rows (the previous layer's combine wrote them; H <= kRouteChunk)
 };
 
 
@@ -102,6 +103,8 @@ struct CombineArgs {
   const int32_t* tok_slot;  // [M][K]
   const float* topk_w;      // [M][K]
   int M, H, K;
+  bf16* xn_out;  // non-null: also write the next layer's normed rows [M][H] (H <= kRouteChunk)
+  float eps;
 };
 
 struct ExpertArgs {
@@ -134,6 +137,11 @@ struct ExpertArgs {
   int a_tmem;
   int q_in_a;
   int acc_cols;  // TMEM columns per accumulator: 256, or 64 with a_tmem
+  // Standalone kernel: rows per expert chunk, kExpertTileTokens or twice that
+  // when a B stage of two K groups x kExpertTileTokens rows can instead hold
+  // one K group of a wider chunk (units of more than kExpertTileTokens rows
+  // then take one K group per stage).
+  int tile_rows;
   int smem_a;  // A stages in shared memory (= stages_a)
   // K groups of 64 per A/B stage (1, 2, or 4 on the low-bit path) for
   // gate/up and down units; a stage holds kg_stage groups of room (part h
@@ -235,6 +243,8 @@ cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
+// k_combine_norm: the combine, then rmsnorm of each output row into a.xn_out.
+cudaError_t launch_combine_norm(const CombineArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_expert(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 cudaError_t launch_layer(const ExpertArgs& a, int grid, size_t smem, cudaStream_t s, bool pdl);
 // (both launch the low-bit form when a.q4 != 0)

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
   bf16* s_x = s_w + kRouteTileExperts * ld;                                        // [16][ld]
   float* s_part = reinterpret_cast<float*>(s_x + kRouteTileTokens * ld);          // [8][16][32]
   uint64_t* wbar = reinterpret_cast<uint64_t*>(s_part + 8 * kRouteTileTokens * kRouteTileExperts + 16);
+  uint64_t* xbar = wbar + 1;  // the normed rows, when the previous combine wrote them
   __shared__ int s_last;
   __shared__ int s_bad;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
   if (tid == 0) {
     s_bad = 0;
     mbar_init(wbar, 1);
+    mbar_init(xbar, 1);
     fence_mbar_init();
     const int len = min(H, kRouteChunk);
     mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(ne * len * 2));
@@ -120,7 +122,18 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
 
   // This warp's two token rows: tile rows warp and warp + 8.
   float rs[2];
-  if (H <= kRouteChunk) {
+  if (a.xn_ready) {
+    // The previous layer's combine wrote the normed rows: copy them in.
+    if (tid == 0) {
+      mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(nt * H * 2));
+      for (int r = 0; r < nt; ++r)
+        bulk_load(smem_u32(s_x + r * ld), a.xn_rows + static_cast<size_t>(t0 + r) * H, static_cast<uint32_t>(H * 2), xbar);
+    }
+    if (!mbar_wait_for(xbar, 0, kWaitLimitNs) && lane == 0) {
+      atomicOr(a.err, kErrMbarTimeout);
+      s_bad = 1;
+    }
+  } else if (H <= kRouteChunk) {
     float4 xv[2][16];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -133,14 +146,7 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
       }
     }
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      float ss = 0.f;
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        ss += xv[j][c].x * xv[j][c].x + xv[j][c].y * xv[j][c].y + xv[j][c].z * xv[j][c].z + xv[j][c].w * xv[j][c].w;
-      ss = warp_sum_f(ss);
-      rs[j] = 1.0f / sqrtf(ss / static_cast<float>(H) + a.eps);
-    }
+    for (int j = 0; j < 2; ++j) rs[j] = rstd_row16(xv[j], H, a.eps);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int r = warp + 8 * j;
@@ -241,6 +247,7 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
   // (bounded) so that no copy is still writing shared memory when this CTA
   // exits, and carry on so that the arrival counters stay consistent.
   if (s_bad) mbar_wait_for(wbar, static_cast<uint32_t>((n_chunks - 1) & 1), kWaitLimitNs);
+  if (s_bad && a.xn_ready) mbar_wait_for(xbar, 0, kWaitLimitNs);
   for (int o = tid; o < kRouteTileTokens * kRouteTileExperts; o += blockDim.x) {
     const int r = o / kRouteTileExperts, c = o % kRouteTileExperts;
     float sum = 0.f;
@@ -334,6 +341,85 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
   *reinterpret_cast<float4*>(a.x_out + static_cast<size_t>(t) * H + col) = o;
 }
 
+// Combine + the next layer's input normalisation, one token per CTA of 512
+// threads: every thread combines one float4 of the row (the same arithmetic
+// as k_combine; H <= 2,048) and stages it in shared memory; warp 0 then takes the row in
+// the router's layout (16 float4 per lane) for rstd_row16, so the normed
+// row is bit-identical to the one the routing kernel would compute, and all
+// threads write it as bf16.
+__global__ void __launch_bounds__(512) k_combine_norm(CombineArgs a) {
+  __shared__ __align__(16) float s_row[kRouteChunk];
+  __shared__ float s_rs;
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  const int H = a.H, K = a.K, MK = a.M * a.K;
+  const int q = H >> 2;
+  for (int f = threadIdx.x; f < q; f += blockDim.x) {
+    const size_t col = static_cast<size_t>(f) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      int r[8];
+      float wk[8];
+      float4 y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool v = k0 + j < K;
+        r[j] = v ? a.tok_slot[t * K + k0 + j] : MK + t;
+        wk[j] = v ? a.topk_w[t * K + k0 + j] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        y[j] = __ldcg(reinterpret_cast<const float4*>(a.yslot + static_cast<size_t>(r[j]) * H + col));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (k0 + j < K) {
+          acc.x = fmaf(wk[j], y[j].x, acc.x);
+          acc.y = fmaf(wk[j], y[j].y, acc.y);
+          acc.z = fmaf(wk[j], y[j].z, acc.z);
+          acc.w = fmaf(wk[j], y[j].w, acc.w);
+        }
+      }
+    }
+    const float4 ys = __ldcg(reinterpret_cast<const float4*>(a.yslot + static_cast<size_t>(MK + t) * H + col));
+    const float4 xi = *reinterpret_cast<const float4*>(a.x_in + static_cast<size_t>(t) * H + col);
+    acc.x += ys.x;
+    acc.y += ys.y;
+    acc.z += ys.z;
+    acc.w += ys.w;
+    float4 o;
+    o.x = xi.x + acc.x;
+    o.y = xi.y + acc.y;
+    o.z = xi.z + acc.z;
+    o.w = xi.w + acc.w;
+    *reinterpret_cast<float4*>(a.x_out + static_cast<size_t>(t) * H + col) = o;
+    *reinterpret_cast<float4*>(s_row + col) = o;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float4 xv[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int col = lane * 4 + 128 * c;
+      xv[c] = col < H ? *reinterpret_cast<const float4*>(s_row + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float rs = rstd_row16(xv, H, a.eps);
+    if (lane == 0) s_rs = rs;
+  }
+  __syncthreads();
+  const float rs = s_rs;
+  for (int f = threadIdx.x; f < q; f += blockDim.x) {
+    const float4 o = *reinterpret_cast<const float4*>(s_row + static_cast<size_t>(f) * 4);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * rs, o.y * rs);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * rs, o.w * rs);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(a.xn_out + static_cast<size_t>(t) * H + static_cast<size_t>(f) * 4) = pk;
+  }
+}
+
 // ---------------------------------------------------------------- launches
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl) {
@@ -341,6 +427,10 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl) {
   return launch_kernel(k_combine, dim3((n + 255) / 256), dim3(256), 0, s, pdl, a);
 }
 
+
+cudaError_t launch_combine_norm(const CombineArgs& a, cudaStream_t s, bool pdl) {
+  return launch_kernel(k_combine_norm, dim3(a.M), dim3(512), 0, s, pdl, a);
+}
 
 cudaError_t launch_embed(const EmbedArgs& a, cudaStream_t s, bool pdl) {
   return launch_kernel(k_embed, dim3(a.M), dim3(256), 0, s, pdl, a);
@@ -353,7 +443,7 @@ cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s, bool pdl) {
 size_t route_smem_bytes(int H) {
   const size_t ld = static_cast<size_t>(std::min(H, kRouteChunk)) + 8;
   return (kRouteTileExperts + kRouteTileTokens) * ld * sizeof(bf16) +
-         (8 * kRouteTileTokens * kRouteTileExperts + 16) * sizeof(float) + sizeof(uint64_t);
+         (8 * kRouteTileTokens * kRouteTileExperts + 16) * sizeof(float) + 2 * sizeof(uint64_t);
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, bool pdl) {

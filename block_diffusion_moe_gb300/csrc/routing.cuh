@@ -29,6 +29,24 @@ __device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int
   return 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
 }
 
+// Reciprocal RMS of a row of H <= 2,048 values that a warp holds as 16
+// float4 per lane (lane l: columns 4l + 128c, zeros past H): the lane's sum
+// of squares in column order, then the warp butterfly. Every rounding is
+// explicit, so the standalone routing kernel and the combine that normalises
+// the next layer's input compute the same bits.
+__device__ __forceinline__ float rstd_row16(const float4 (&xv)[16], int H, float eps) {
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const float4 v = xv[c];
+    const float p = __fadd_rn(__fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y)),
+                              __fadd_rn(__fmul_rn(v.z, v.z), __fmul_rn(v.w, v.w)));
+    ss = __fadd_rn(ss, p);
+  }
+  ss = warp_sum_f(ss);
+  return 1.0f / sqrtf(ss / static_cast<float>(H) + eps);
+}
+
 // As row_rstd + warp_router_dots for H <= 128 * kChunks, with the row held
 // in registers between the two (one load of the row, all loads in flight at
 // once). Same arithmetic order, so the results are identical.
