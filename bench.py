@@ -684,14 +684,16 @@ def run_ours(args):
     fused = n_pos <= 32
     per_layer = 1 if fused else 3         # fused layer kernel, or route + experts + combine
     if sp.full:
-        # embed, layers, the last deferred combine, norm + one head launch per 256 positions
-        launches_per_step = 1 + per_layer * n_layers + (1 if fused else 0) + 1 + (n_pos + 255) // 256
+        # embed, layers, the last deferred combine, norm + a head launch and its merge launch
+        # per 256 positions
+        launches_per_step = 1 + per_layer * n_layers + (1 if fused else 0) + 1 + 2 * ((n_pos + 255) // 256)
     elif sp.one_layer:
         launches_per_step = per_layer
     else:
-        launches_per_step = 2
-    roof_kernel = ("k_head + k_rmsnorm (head statistics and unmask)" if kind == "head"
-                   else "k_head<accept> + k_rmsnorm (head statistics, entropy and the accept test)"
+        launches_per_step = 3          # norm, head, merge
+    roof_kernel = ("k_rmsnorm + k_head + k_head_merge (head statistics and unmask)" if kind == "head"
+                   else "k_rmsnorm + k_head<accept> + k_head_merge<accept> (head statistics, entropy and the "
+                        "accept test)"
                    if kind == "accept"
                    else "k_layer (routing + grouped SwiGLU experts + combine, one launch per MoE layer)"
                    if fused else "k_expert (grouped SwiGLU experts + combine, one launch per MoE layer)")

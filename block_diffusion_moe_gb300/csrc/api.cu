@@ -108,7 +108,7 @@ MoeLayout moe_layout(const clover_dims& d, int M) {
 }
 
 struct HeadLayout {
-  size_t xn, part_m, part_s, part_a, part_t, part_zd, bytes;
+  size_t xn, part_m, part_s, part_a, part_t, part_zd, dec_m, dec_s, dec_a, bytes;
 };
 
 // The accept form adds two more [G][M] partial arrays.
@@ -127,6 +127,9 @@ HeadLayout head_layout(const clover_dims& d, int M, bool accept = false) {
   L.part_a = take(static_cast<size_t>(kHeadMaxCtas) * ms * 4);
   L.part_t = accept ? take(static_cast<size_t>(kHeadMaxCtas) * ms * 4) : 0;
   L.part_zd = accept ? take(static_cast<size_t>(kHeadMaxCtas) * ms * 4) : 0;
+  L.dec_m = take(ms * 4);
+  L.dec_s = accept ? take(ms * 4) : 0;
+  L.dec_a = take(ms * 4);
   L.bytes = o;
   return L;
 }
@@ -688,15 +691,15 @@ int enqueue_head(const clover_dims& d, const uint16_t* head_w, const float* x, c
     ha.stages = static_cast<int>(std::min<size_t>(
         8 / kg, (static_cast<size_t>(kSmemBudget) - fixed) / (kg * (kATileBytes + static_cast<size_t>(nb) * 128))));
     const int grid = std::max(1, std::min(std::min(ha.n_tiles, plan.sms), kHeadMaxCtas));
-    // The final merge reuses the ring for 12 (accept: 20) bytes x grid per
-    // position, 64 positions per round where they fit, else 32.
-    const size_t ring = static_cast<size_t>(std::max(ha.stages, 0)) * kg * (kATileBytes + static_cast<size_t>(nb) * 128);
-    const size_t per_pos = static_cast<size_t>(grid) * (accept ? 20 : 12);
-    ha.merge_rows = (m > 32 && ring >= 64 * per_pos) ? 64 : 32;
-    if (ha.stages < 1 || ring < 32 * per_pos)
-      return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head ring too small for the final merge");
+    if (ha.stages < 1) return fail(CLOVER_ERR_UNSUPPORTED_SHAPE, "head pipeline does not fit in shared memory");
+    ha.n_parts = grid;
+    ha.dec_m = reinterpret_cast<float*>(data + L.dec_m);
+    ha.dec_s = accept ? reinterpret_cast<float*>(data + L.dec_s) : nullptr;
+    ha.dec_a = reinterpret_cast<int*>(data + L.dec_a);
     e = launch_head(ha, accept, grid, head_smem_bytes(ha.stages, nb, accept, kg), stream, kPdl);
     if (e != cudaSuccess) return cuda_fail(e, "launch head");
+    e = launch_head_merge(ha, accept, stream, kPdl);
+    if (e != cudaSuccess) return cuda_fail(e, "launch head merge");
   }
   return CLOVER_OK;
 }

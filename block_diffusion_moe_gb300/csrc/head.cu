@@ -12,11 +12,12 @@
 // 128 head rows (the M = 128 side of tcgen05.mma) against all positions (the
 // N side). The epilogue turns each 128 x N accumulator into per-position
 // (max, sum of exp relative to the max, argmax) and folds it into a running
-// per-CTA state, so the logits never leave the SM. The last CTA to finish
-// merges the G partial states (maximum first, then the sums rescaled to it,
-// several threads per position combined in a fixed order), derives log-sum-exp and the
-// maximum probability, and applies the unmask rule to every block of
-// positions. Ties in the argmax go to the lowest vocabulary id at every level.
+// per-CTA state, so the logits never leave the SM. A second, small launch
+// (k_head_merge) merges the G partial states, one warp per position
+// (maximum first, then the sums rescaled to it, combined in a fixed order),
+// derives log-sum-exp and the maximum probability, and its last CTA applies
+// the unmask rule to every block of positions. Ties in the argmax go to the
+// lowest vocabulary id at every level.
 //
 // The accept form (section "Two ways to run it": self-speculative decoding
 // keeps the longest prefix of drafts that the causal pass accepts, plus one
@@ -24,8 +25,8 @@
 // one whose probability is at least min(ratio, delta e^-H)) carries two more
 // per-position quantities through the same pipeline: t = sum of
 // e^(z - m) (z - m), from which the entropy is H = ln s - t / s, and the
-// draft token's logit. The last CTA then takes the accept test per block of
-// rows instead of the unmask rule.
+// draft token's logit. The merge launch's last CTA then takes the accept
+// test per block of rows instead of the unmask rule.
 #include <math.h>
 
 #include "kernels.cuh"
@@ -50,7 +51,7 @@ struct HeadSmem {
   float* run_t;   // [nb]
   float* run_zd;  // [nb]
   float* tr;      // [4][32][33] per-warp transpose tiles
-  uint64_t *full, *empty, *tfull, *tempty, *drain, *mrg;  // mrg: the last CTA's partial copies
+  uint64_t *full, *empty, *tfull, *tempty, *drain;
   uint32_t* tmem_slot;
   volatile uint32_t* abort;
   volatile int* s_ok;
@@ -86,8 +87,7 @@ __device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int n
   s.tfull = s.empty + p.stages;
   s.tempty = s.tfull + 2;
   s.drain = s.tempty + 2;
-  s.mrg = s.drain + 1;
-  s.tmem_slot = reinterpret_cast<uint32_t*>(s.mrg + 1);
+  s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
   s.abort = s.tmem_slot + 1;
   s.s_ok = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
   s.s_last = s.s_ok + 1;
@@ -411,8 +411,7 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
   named_bar_sync(1, 128);
   if (!*s.s_ok) return;
 
-  // Publish this CTA's partial state, then let the last CTA merge all of them.
-  const int G = gridDim.x;
+  // Publish this CTA's partial state; k_head_merge combines them.
   for (int n = etid; n < p.M; n += 128) {
     const size_t g = static_cast<size_t>(blockIdx.x) * p.M + n;
     p.part_m[g] = s.run_m[n];
@@ -422,234 +421,6 @@ __device__ void head_epilogue(const HeadArgs& p, const HeadSmem& s, int nb, uint
       p.part_t[g] = s.run_t[n];
       p.part_zd[g] = s.run_zd[n];
     }
-  }
-  __threadfence();
-  named_bar_sync(1, 128);
-  if (etid == 0) {
-    const int old = atomicAdd(p.done_ctr, 1);
-    *s.s_last = (old == G - 1) ? 1 : 0;
-    s.s_counts[0] = 0;
-    s.s_counts[1] = 0;
-  }
-  named_bar_sync(1, 128);
-  if (!*s.s_last) return;
-  __threadfence();
-  // The pipeline is drained, so the ring's shared memory is free: stage the
-  // G partials of up to R positions at a time, then merge each position's
-  // partials. With rows of 16-byte multiples (M % 4 == 0) every (CTA, array)
-  // row of the round is one bulk copy, all in flight at once against one
-  // barrier; otherwise the loads are issued in batches of 8 per thread before
-  // any of them is stored (a store to shared memory through a generic pointer
-  // would hold back the next L2 load). Element loads cost one L2 round trip
-  // per batch, ~24 us per round of 64 positions; the copies about one.
-  const int R = p.merge_rows;
-  float* pm_s = reinterpret_cast<float*>(s.ring);
-  float* ps_s = pm_s + G * R;
-  int* pa_s = reinterpret_cast<int*>(ps_s + G * R);
-  float* pt_s = reinterpret_cast<float*>(pa_s + G * R);
-  float* pz_s = pt_s + G * R;
-  constexpr int kBatch = 8;
-  const bool bulk = (p.M & 3) == 0;
-  uint32_t mrg_phase = 0;
-  for (int n0 = 0; n0 < p.M; n0 += R) {
-    const int cnt = min(R, p.M - n0);
-    const int tot = G * cnt;
-    if (bulk) {
-      const int n_arr = kAccept ? 5 : 3;
-      const uint32_t row_bytes = static_cast<uint32_t>(cnt) * 4u;
-      if (etid == 0) mbar_arrive_expect_tx(s.mrg, static_cast<uint32_t>(G * n_arr) * row_bytes);
-      named_bar_sync(1, 128);      // the expected bytes are registered before any copy lands
-      fence_proxy_async_global();  // the partials (generic writes) are read by the copies
-      for (int i = etid; i < G * n_arr; i += 128) {
-        const int arr = i / G, b = i - arr * G;
-        const size_t g = static_cast<size_t>(b) * p.M + n0;
-        const void* src = arr == 0   ? static_cast<const void*>(p.part_m + g)
-                          : arr == 1 ? static_cast<const void*>(p.part_s + g)
-                          : arr == 2 ? static_cast<const void*>(p.part_a + g)
-                          : arr == 3 ? static_cast<const void*>(p.part_t + g)
-                                     : static_cast<const void*>(p.part_zd + g);
-        float* dst = arr == 0   ? pm_s
-                     : arr == 1 ? ps_s
-                     : arr == 2 ? reinterpret_cast<float*>(pa_s)
-                     : arr == 3 ? pt_s
-                                : pz_s;
-        bulk_load(smem_u32(dst + b * R), src, row_bytes, s.mrg);
-      }
-      if (!mbar_wait(s.mrg, mrg_phase, s.abort)) atomicOr(p.err, kErrMbarTimeout);
-      mrg_phase ^= 1u;
-    }
-    for (int i0 = etid; !bulk && i0 < tot; i0 += 128 * kBatch) {
-      float vm[kBatch], vs[kBatch], vt[kBatch], vz[kBatch];
-      int va[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i = i0 + 128 * u;
-        if (i < tot) {
-          const int b = i / cnt, j = i - b * cnt;
-          const size_t g = static_cast<size_t>(b) * p.M + n0 + j;
-          vm[u] = __ldcg(p.part_m + g);
-          vs[u] = __ldcg(p.part_s + g);
-          va[u] = __ldcg(p.part_a + g);
-          if (kAccept) {
-            vt[u] = __ldcg(p.part_t + g);
-            vz[u] = __ldcg(p.part_zd + g);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i = i0 + 128 * u;
-        if (i < tot) {
-          const int b = i / cnt, j = i - b * cnt;
-          pm_s[b * R + j] = vm[u];
-          ps_s[b * R + j] = vs[u];
-          pa_s[b * R + j] = va[u];
-          if (kAccept) {
-            pt_s[b * R + j] = vt[u];
-            pz_s[b * R + j] = vz[u];
-          }
-        }
-      }
-    }
-    named_bar_sync(1, 128);
-    {
-      // T consecutive threads per position (T = 128 / R), each over a
-      // contiguous range of CTAs: first the maximum and its token (ties to
-      // the lower id), then the sums rescaled to that maximum, each term
-      // independent of the others, so the exponentials pipeline instead of
-      // forming one 152-long dependency chain per position. The partial
-      // results combine in a fixed butterfly, so the outcome does not depend
-      // on timing.
-      const int T = 128 / R;
-      const int j = etid / T, q = etid - j * T;
-      const bool live = j < cnt;
-      const int b0 = (G * q) / T, b1 = (G * (q + 1)) / T;
-      float m = -INFINITY;
-      int a = 0x7fffffff;
-      if (live)
-        for (int b = b0; b < b1; ++b) {
-          const float v = pm_s[b * R + j];
-          const int ai = pa_s[b * R + j];
-          if (v > m || (v == m && ai < a)) {
-            m = v;
-            a = ai;
-          }
-        }
-      for (int o = 1; o < T; o <<= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
-        if (m2 > m || (m2 == m && a2 < a)) {
-          m = m2;
-          a = a2;
-        }
-      }
-      float sm = 0.f, t = 0.f, zd = -INFINITY;
-      if (live && m != -INFINITY)
-        for (int b = b0; b < b1; ++b) {
-          const float mb = pm_s[b * R + j];
-          if (mb == -INFINITY) continue;  // an empty partial (s = t = 0)
-          const float f = expf(mb - m);
-          sm += ps_s[b * R + j] * f;
-          if (kAccept) {
-            t += f * (pt_s[b * R + j] + (mb - m) * ps_s[b * R + j]);
-            zd = fmaxf(zd, pz_s[b * R + j]);
-          }
-        }
-      for (int o = 1; o < T; o <<= 1) {
-        sm += __shfl_xor_sync(0xffffffffu, sm, o);
-        if (kAccept) {
-          t += __shfl_xor_sync(0xffffffffu, t, o);
-          zd = fmaxf(zd, __shfl_xor_sync(0xffffffffu, zd, o));
-        }
-      }
-      if (live && q == 0) {
-        const int n = n0 + j;
-        const float lse = m + logf(sm);
-        const float pmax = 1.0f / sm;  // = exp(m - lse)
-        if (p.argmax) p.argmax[n] = a;
-        if (p.max_logit) p.max_logit[n] = m;
-        if (p.lse) p.lse[n] = lse;
-        if (p.max_prob) p.max_prob[n] = pmax;
-        if (kAccept) {
-          const float ent = fmaxf(logf(sm) - t / sm, 0.f);  // t <= 0
-          const float pd = expf(zd - lse);                   // 0 for a draft never seen
-          if (p.entropy) p.entropy[n] = ent;
-          if (p.p_draft) p.p_draft[n] = pd;
-          s.run_m[n] = pd;
-          s.run_s[n] = ent;
-        } else {
-          s.run_m[n] = pmax;  // reuse: per-position max probability
-        }
-        s.run_a[n] = a;
-      }
-    }
-    named_bar_sync(1, 128);
-  }
-  named_bar_sync(1, 128);
-  if (kAccept) {
-    // Accept test, one thread per block of rows: the longest prefix of
-    // accepted drafts, then the boundary row's argmax.
-    const int nblk = p.M / p.block;
-    for (int b = etid; b < nblk; b += 128) {
-      const int p0 = b * p.block;
-      int r = 0;
-      while (r < p.block - 1) {
-        const int i = p0 + r;
-        const bool acc = (p.rule == 0) ? (p.draft[i] == s.run_a[i])
-                                       : (s.run_m[i] >= fminf(p.ratio, p.delta * expf(-s.run_s[i])));
-        if (!acc) break;
-        ++r;
-      }
-      p.accept_len[b] = r;
-      for (int j = 0; j < p.block; ++j)
-        p.out_tokens[p0 + j] = (j < r) ? p.draft[p0 + j] : (j == r ? s.run_a[p0 + j] : -1);
-    }
-    named_bar_sync(1, 128);
-    if (etid == 0) *p.done_ctr = 0;
-    return;
-  }
-  // Unmask rule, one thread per block of positions.
-  const int nblk = (p.M + p.block - 1) / p.block;
-  for (int b = etid; b < nblk; b += 128) {
-    const int p0 = b * p.block, p1 = min(p.M, p0 + p.block);
-    int n_commit = 0, best = -1;
-    float best_p = 0.f;
-    bool bad = false;
-    for (int i = p0; i < p1; ++i) {
-      if (!p.masked[i]) {
-        // a committed slot must hold a vocabulary id; report one that does not
-        const int tk = p.tokens[i];
-        bad |= (tk < 0 || tk >= p.V);
-        continue;
-      }
-      const float pm = s.run_m[i];
-      if (pm > p.threshold) ++n_commit;
-      if (best < 0 || pm > best_p) {
-        best = i;
-        best_p = pm;
-      }
-    }
-    int still = 0, done = 0;
-    for (int i = p0; i < p1; ++i) {
-      if (!p.masked[i]) continue;
-      const bool c = (n_commit > 0) ? (s.run_m[i] > p.threshold) : (i == best);
-      if (c) {
-        p.tokens[i] = s.run_a[i];
-        p.masked[i] = 0;
-        ++done;
-      } else {
-        ++still;
-      }
-    }
-    atomicAdd(&s.s_counts[0], done);
-    atomicAdd(&s.s_counts[1], still);
-    if (bad) atomicOr(p.err, kErrBadToken);
-  }
-  named_bar_sync(1, 128);
-  if (etid == 0) {
-    if (p.n_committed) *p.n_committed = (p.accumulate ? *p.n_committed : 0) + s.s_counts[0];
-    if (p.n_masked_left) *p.n_masked_left = (p.accumulate ? *p.n_masked_left : 0) + s.s_counts[1];
-    *p.done_ctr = 0;
   }
 }
 
@@ -671,7 +442,6 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
       mbar_init(&s.tempty[i], 4);  // one arrival per epilogue warp
     }
     mbar_init(s.drain, 1);
-    mbar_init(s.mrg, 1);
     *s.abort = 0u;
     fence_mbar_init();
   }
@@ -708,10 +478,167 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
   }
 }
 
+// Merge of the G per-CTA partial states of one k_head launch, one warp per
+// position: each lane takes CTAs lane, lane + 32, ..., first the maximum and
+// its token (ties to the lower id), then the sums rescaled to that maximum;
+// the lanes' results combine in a fixed butterfly, so the outcome does not
+// depend on timing. The last CTA to finish then applies the unmask rule (or
+// the accept test) to every block of positions, reading the per-position
+// decision inputs back from the workspace.
+template <bool kAccept>
+__global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ HeadArgs p) {
+  __shared__ int s_last;
+  __shared__ int s_counts[2];
+  pdl_wait();
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = p.n_parts;
+  const int n = blockIdx.x * 8 + warp;
+  if (n < p.M) {
+    float m = -INFINITY;
+    int a = 0x7fffffff;
+    for (int b = lane; b < G; b += 32) {
+      const size_t g = static_cast<size_t>(b) * p.M + n;
+      const float v = __ldcg(p.part_m + g);
+      const int ai = __ldcg(p.part_a + g);
+      if (v > m || (v == m && ai < a)) {
+        m = v;
+        a = ai;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const int a2 = __shfl_xor_sync(0xffffffffu, a, o);
+      if (m2 > m || (m2 == m && a2 < a)) {
+        m = m2;
+        a = a2;
+      }
+    }
+    float sm = 0.f, t = 0.f, zd = -INFINITY;
+    if (m != -INFINITY)
+      for (int b = lane; b < G; b += 32) {
+        const size_t g = static_cast<size_t>(b) * p.M + n;
+        const float mb = __ldcg(p.part_m + g);
+        if (mb == -INFINITY) continue;  // an empty partial (s = t = 0)
+        const float ps = __ldcg(p.part_s + g);
+        const float f = expf(mb - m);
+        sm += ps * f;
+        if (kAccept) {
+          t += f * (__ldcg(p.part_t + g) + (mb - m) * ps);
+          zd = fmaxf(zd, __ldcg(p.part_zd + g));
+        }
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if (kAccept) {
+        t += __shfl_xor_sync(0xffffffffu, t, o);
+        zd = fmaxf(zd, __shfl_xor_sync(0xffffffffu, zd, o));
+      }
+    }
+    if (lane == 0) {
+      const float lse = m + logf(sm);
+      const float pmax = 1.0f / sm;  // = exp(m - lse)
+      if (p.argmax) p.argmax[n] = a;
+      if (p.max_logit) p.max_logit[n] = m;
+      if (p.lse) p.lse[n] = lse;
+      if (p.max_prob) p.max_prob[n] = pmax;
+      if (kAccept) {
+        const float ent = fmaxf(logf(sm) - t / sm, 0.f);  // t <= 0
+        const float pd = expf(zd - lse);                   // 0 for a draft never seen
+        if (p.entropy) p.entropy[n] = ent;
+        if (p.p_draft) p.p_draft[n] = pd;
+        p.dec_m[n] = pd;
+        p.dec_s[n] = ent;
+      } else {
+        p.dec_m[n] = pmax;
+      }
+      p.dec_a[n] = a;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(p.done_ctr, 1);
+    s_last = (old == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
+    s_counts[0] = 0;
+    s_counts[1] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (kAccept) {
+    // Accept test, one thread per block of rows: the longest prefix of
+    // accepted drafts, then the boundary row's argmax.
+    const int nblk = p.M / p.block;
+    for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+      const int p0 = b * p.block;
+      int r = 0;
+      while (r < p.block - 1) {
+        const int i = p0 + r;
+        const bool acc = (p.rule == 0) ? (p.draft[i] == __ldcg(p.dec_a + i))
+                                       : (__ldcg(p.dec_m + i) >= fminf(p.ratio, p.delta * expf(-__ldcg(p.dec_s + i))));
+        if (!acc) break;
+        ++r;
+      }
+      p.accept_len[b] = r;
+      for (int j = 0; j < p.block; ++j)
+        p.out_tokens[p0 + j] = (j < r) ? p.draft[p0 + j] : (j == r ? __ldcg(p.dec_a + p0 + j) : -1);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *p.done_ctr = 0;
+    return;
+  }
+  // Unmask rule, one thread per block of positions.
+  const int nblk = (p.M + p.block - 1) / p.block;
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) {
+    const int p0 = b * p.block, p1 = min(p.M, p0 + p.block);
+    int n_commit = 0, best = -1;
+    float best_p = 0.f;
+    bool bad = false;
+    for (int i = p0; i < p1; ++i) {
+      if (!p.masked[i]) {
+        // a committed slot must hold a vocabulary id; report one that does not
+        const int tk = p.tokens[i];
+        bad |= (tk < 0 || tk >= p.V);
+        continue;
+      }
+      const float pm = __ldcg(p.dec_m + i);
+      if (pm > p.threshold) ++n_commit;
+      if (best < 0 || pm > best_p) {
+        best = i;
+        best_p = pm;
+      }
+    }
+    int still = 0, done = 0;
+    for (int i = p0; i < p1; ++i) {
+      if (!p.masked[i]) continue;
+      const bool c = (n_commit > 0) ? (__ldcg(p.dec_m + i) > p.threshold) : (i == best);
+      if (c) {
+        p.tokens[i] = __ldcg(p.dec_a + i);
+        p.masked[i] = 0;
+        ++done;
+      } else {
+        ++still;
+      }
+    }
+    atomicAdd(&s_counts[0], done);
+    atomicAdd(&s_counts[1], still);
+    if (bad) atomicOr(p.err, kErrBadToken);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (p.n_committed) *p.n_committed = (p.accumulate ? *p.n_committed : 0) + s_counts[0];
+    if (p.n_masked_left) *p.n_masked_left = (p.accumulate ? *p.n_masked_left : 0) + s_counts[1];
+    *p.done_ctr = 0;
+  }
+}
+
 size_t head_smem_bytes(int stages, int nb, bool accept, int kg) {
   return 1024 + static_cast<size_t>(stages) * kg * (kATileBytes + static_cast<size_t>(nb) * 128) +
          static_cast<size_t>(nb) * (4 * 12 + 12 + 4 + (accept ? 4 * 8 + 8 : 0)) + 4 * 32 * 33 * sizeof(float) +
-         static_cast<size_t>(2 * stages + 6) * 8 + 64;
+         static_cast<size_t>(2 * stages + 5) * 8 + 64;
 }
 
 cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl) {
@@ -719,6 +646,11 @@ cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, c
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   return launch_kernel(k, dim3(grid), dim3(kHeadThreads), smem, s, pdl, a);
+}
+
+cudaError_t launch_head_merge(const HeadArgs& a, bool accept, cudaStream_t s, bool pdl) {
+  auto* k = accept ? k_head_merge<true> : k_head_merge<false>;
+  return launch_kernel(k, dim3((a.M + 7) / 8), dim3(256), 0, s, pdl, a);
 }
 
 }  // namespace clover

@@ -201,7 +201,11 @@ struct HeadArgs {
   float* part_m;       // [G][M]
   float* part_s;       // [G][M]
   int* part_a;         // [G][M]
-  int* done_ctr;       // scalar, zero between launches
+  int* done_ctr;       // scalar, zero between launches (the merge kernel's arrivals)
+  float* dec_m;        // [M] per-position decision input: max probability (accept: p(draft))
+  float* dec_s;        // [M] accept: entropy
+  int* dec_a;          // [M] argmax
+  int n_parts;         // G: CTAs of the head launch (partial states to merge)
   int32_t* tokens;     // [M] in/out
   uint8_t* masked;     // [M] in/out
   int32_t* argmax;     // [M] out (nullable)
@@ -215,7 +219,6 @@ struct HeadArgs {
   int accumulate;  // 1: add this call's counts to *n_committed / *n_masked_left (a later sub-call of a split call)
   int kg;     // K groups of 64 per pipeline stage (1 or 2)
   int x_box;  // rows per TMA box of the normed positions (a multiple of 16)
-  int merge_rows;  // positions per round of the last CTA's merge (32 or 64; G x rows partials fit the ring)
   float threshold;
   // Accept mode (self-speculative verify): blocks of `block` rows, row j
   // testing draft[j]; the unmask fields above are unused then.
@@ -261,6 +264,9 @@ size_t expert_tables_bytes(int M, int K, int max_chunks);
 constexpr int kLayerMaxTokens = 32;
 // Launches the unmask or the accept form of the head kernel.
 cudaError_t launch_head(const HeadArgs& a, bool accept, int grid, size_t smem, cudaStream_t s, bool pdl);
+// k_head_merge: merges the partial states of a k_head launch (one warp per
+// position) and applies the unmask rule / accept test per block.
+cudaError_t launch_head_merge(const HeadArgs& a, bool accept, cudaStream_t s, bool pdl);
 
 size_t expert_smem_bytes(int smem_a, int stages_a, int stages_b, int nb_max, int stages_q, int kg);
 size_t head_smem_bytes(int stages, int nb, bool accept, int kg);
