@@ -487,25 +487,47 @@ __global__ void __launch_bounds__(kHeadThreads, 1) k_head(const __grid_constant_
 // decision inputs back from the workspace.
 template <bool kAccept>
 __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ HeadArgs p) {
+  constexpr int kPer = kHeadMaxCtas / 32;  // partials per lane at most
   __shared__ int s_last;
   __shared__ int s_counts[2];
+  __shared__ float s_dm[kTileTokens];
+  __shared__ float s_ds[kTileTokens];
+  __shared__ int s_da[kTileTokens];
   pdl_wait();
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.n_parts;
   const int n = blockIdx.x * 8 + warp;
   if (n < p.M) {
-    float m = -INFINITY;
-    int a = 0x7fffffff;
-    for (int b = lane; b < G; b += 32) {
-      const size_t g = static_cast<size_t>(b) * p.M + n;
-      const float v = __ldcg(p.part_m + g);
-      const int ai = __ldcg(p.part_a + g);
-      if (v > m || (v == m && ai < a)) {
-        m = v;
-        a = ai;
+    // every partial of this lane in registers, all loads in flight at once
+    float vm[kPer], vs[kPer], vt[kPer], vz[kPer];
+    int va[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int b = lane + 32 * i;
+      vm[i] = -INFINITY;
+      vs[i] = vt[i] = 0.f;
+      vz[i] = -INFINITY;
+      va[i] = 0x7fffffff;
+      if (b < G) {
+        const size_t g = static_cast<size_t>(b) * p.M + n;
+        vm[i] = __ldcg(p.part_m + g);
+        vs[i] = __ldcg(p.part_s + g);
+        va[i] = __ldcg(p.part_a + g);
+        if (kAccept) {
+          vt[i] = __ldcg(p.part_t + g);
+          vz[i] = __ldcg(p.part_zd + g);
+        }
       }
     }
+    float m = -INFINITY;
+    int a = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (vm[i] > m || (vm[i] == m && va[i] < a)) {
+        m = vm[i];
+        a = va[i];
+      }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -516,19 +538,18 @@ __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ Head
       }
     }
     float sm = 0.f, t = 0.f, zd = -INFINITY;
-    if (m != -INFINITY)
-      for (int b = lane; b < G; b += 32) {
-        const size_t g = static_cast<size_t>(b) * p.M + n;
-        const float mb = __ldcg(p.part_m + g);
-        if (mb == -INFINITY) continue;  // an empty partial (s = t = 0)
-        const float ps = __ldcg(p.part_s + g);
-        const float f = expf(mb - m);
-        sm += ps * f;
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        if (vm[i] == -INFINITY) continue;  // an empty partial (s = t = 0), or none
+        const float f = expf(vm[i] - m);
+        sm += vs[i] * f;
         if (kAccept) {
-          t += f * (__ldcg(p.part_t + g) + (mb - m) * ps);
-          zd = fmaxf(zd, __ldcg(p.part_zd + g));
+          t += f * (vt[i] + (vm[i] - m) * vs[i]);
+          zd = fmaxf(zd, vz[i]);
         }
       }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       sm += __shfl_xor_sync(0xffffffffu, sm, o);
@@ -568,6 +589,17 @@ __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ Head
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // The last CTA: every position's decision inputs into shared memory at
+  // once (M <= kTileTokens per launch), then one thread per block.
+  for (int i = threadIdx.x; i < p.M; i += blockDim.x) {
+    const float dm = __ldcg(p.dec_m + i);
+    const int da = __ldcg(p.dec_a + i);
+    const float ds = kAccept ? __ldcg(p.dec_s + i) : 0.f;
+    s_dm[i] = dm;
+    s_da[i] = da;
+    s_ds[i] = ds;
+  }
+  __syncthreads();
   if (kAccept) {
     // Accept test, one thread per block of rows: the longest prefix of
     // accepted drafts, then the boundary row's argmax.
@@ -577,14 +609,14 @@ __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ Head
       int r = 0;
       while (r < p.block - 1) {
         const int i = p0 + r;
-        const bool acc = (p.rule == 0) ? (p.draft[i] == __ldcg(p.dec_a + i))
-                                       : (__ldcg(p.dec_m + i) >= fminf(p.ratio, p.delta * expf(-__ldcg(p.dec_s + i))));
+        const bool acc = (p.rule == 0) ? (p.draft[i] == s_da[i])
+                                       : (s_dm[i] >= fminf(p.ratio, p.delta * expf(-s_ds[i])));
         if (!acc) break;
         ++r;
       }
       p.accept_len[b] = r;
       for (int j = 0; j < p.block; ++j)
-        p.out_tokens[p0 + j] = (j < r) ? p.draft[p0 + j] : (j == r ? __ldcg(p.dec_a + p0 + j) : -1);
+        p.out_tokens[p0 + j] = (j < r) ? p.draft[p0 + j] : (j == r ? s_da[p0 + j] : -1);
     }
     __syncthreads();
     if (threadIdx.x == 0) *p.done_ctr = 0;
@@ -604,7 +636,7 @@ __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ Head
         bad |= (tk < 0 || tk >= p.V);
         continue;
       }
-      const float pm = __ldcg(p.dec_m + i);
+      const float pm = s_dm[i];
       if (pm > p.threshold) ++n_commit;
       if (best < 0 || pm > best_p) {
         best = i;
@@ -614,9 +646,9 @@ __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ Head
     int still = 0, done = 0;
     for (int i = p0; i < p1; ++i) {
       if (!p.masked[i]) continue;
-      const bool c = (n_commit > 0) ? (__ldcg(p.dec_m + i) > p.threshold) : (i == best);
+      const bool c = (n_commit > 0) ? (s_dm[i] > p.threshold) : (i == best);
       if (c) {
-        p.tokens[i] = __ldcg(p.dec_a + i);
+        p.tokens[i] = s_da[i];
         p.masked[i] = 0;
         ++done;
       } else {
