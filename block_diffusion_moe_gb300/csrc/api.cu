@@ -462,6 +462,16 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.tile_rows = (!fused && !q4 && M > 2 * kExpertTileTokens && kg_gu == 2 && kg_dn == 2 && nb == kExpertTileTokens)
                      ? 2 * kExpertTileTokens
                      : kExpertTileTokens;
+  // Up to 256 tokens every chunk runs as paired units: two weight slices
+  // share each B tile (an A stage of two K groups holds one K group of two
+  // slices; two 128-column accumulators), halving the token rows each SM
+  // takes in per weight byte. (Pairing only experts above 16, 32 or 64
+  // tokens was slower on the same box: 3.68, 3.69, 3.71 against 3.64 ms per
+  // Zipf step; none: 3.79.)
+  xa.pair_rows = (!fused && !q4 && xa.tile_rows == kExpertTileTokens && kg_gu == 2 && kg_dn == 2 &&
+                  (F / 64) % 2 == 0 && (H / 128) % 2 == 0)
+                     ? 0
+                     : -1;
   const size_t a_stage = static_cast<size_t>(kg) * kATileBytes;
   const size_t b_stage = static_cast<size_t>(kg) * nb * 128;
   const size_t tables = fused ? layer_rt_bytes(M, K, E) : expert_tables_bytes(M, K, n_chunks);

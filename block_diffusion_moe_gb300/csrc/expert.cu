@@ -61,6 +61,7 @@ struct Unit {
   int slice;  // F/64 slice (gate/up) or H/128 slice (down)
   int cnt;    // tokens of the expert (chunk)
   int off;    // first row of the expert (chunk) in the gathered buffers
+  int pair;   // 1: slices slice and slice + 1 together (two accumulators sharing each B tile)
 };
 
 // Where a launch finds its routing: global tables written in the prologue
@@ -73,6 +74,7 @@ struct Rt {
   const int32_t* tok_slot;  // [M][K] row of each selection
   const float* topk_w;      // [M][K] weight of each selection
   int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
+  int n_pair;               // standalone: the leading chunks whose units are paired (0: none)
   int dense;                // gate/up B operand = all M normed rows
   int chunked;              // standalone: units index chunks of at most p.tile_rows rows
   // standalone: the spare warp gathers this CTA's share of the token rows
@@ -82,19 +84,43 @@ struct Rt {
   uint64_t* gbar;           // bulk-copy barrier of the gather
 };
 
+// Unit numbering: the gate/up units of the paired chunks (two slices each),
+// then those of the other chunks, then the down units in the same pattern.
+__device__ __forceinline__ int n_units(const Rt& rt, const ExpertArgs& p) {
+  const int SF = p.F >> 6, SH = p.H >> 7;
+  return rt.n_pair * ((SF + SH) >> 1) + (rt.n_exp - rt.n_pair) * (SF + SH);
+}
+
 __device__ __forceinline__ Unit decode_unit(int u, const Rt& rt, const ExpertArgs& p) {
   const int SF = p.F >> 6, SH = p.H >> 7;
+  const int P = rt.n_pair;
   Unit w;
-  const int n_gu = rt.n_exp * SF;
-  if (u < n_gu) {
+  const int g_pair = P * (SF >> 1);
+  const int n_gu = g_pair + (rt.n_exp - P) * SF;
+  w.pair = 0;
+  if (u < g_pair) {
     w.kind = 0;
-    w.a = u / SF;
-    w.slice = u - w.a * SF;
+    w.a = u / (SF >> 1);
+    w.slice = 2 * (u - w.a * (SF >> 1));
+    w.pair = 1;
+  } else if (u < n_gu) {
+    const int v = u - g_pair;
+    w.kind = 0;
+    w.a = P + v / SF;
+    w.slice = v - (w.a - P) * SF;
   } else {
     const int v = u - n_gu;
+    const int d_pair = P * (SH >> 1);
     w.kind = 1;
-    w.a = v / SH;
-    w.slice = v - w.a * SH;
+    if (v < d_pair) {
+      w.a = v / (SH >> 1);
+      w.slice = 2 * (v - w.a * (SH >> 1));
+      w.pair = 1;
+    } else {
+      const int v2 = v - d_pair;
+      w.a = P + v2 / SH;
+      w.slice = v2 - (w.a - P) * SH;
+    }
   }
   if (rt.chunked) {
     w.e = rt.act[w.a];
@@ -130,6 +156,7 @@ __device__ __forceinline__ int unit_kq(const Unit& w, const ExpertArgs& p) {
 // K groups per A/B stage of a unit (1, 2 or 4).
 __device__ __forceinline__ int unit_kg(const Unit& w, const ExpertArgs& p) {
   if (w.cnt > kExpertTileTokens) return 1;  // a wide chunk: one K group fills a B stage
+  if (w.pair) return 1;                     // two weight slices of one K group fill an A stage
   return w.kind == 0 ? p.kg_gu : p.kg_dn;
 }
 
@@ -302,14 +329,18 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
         }
       } else {
         const uint32_t dst0 = smem_u32(s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes);
-        mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(kg * kATileBytes));
-        for (int h = 0; h < kg; ++h) {
+        // kg K groups of one slice, or one K group of a pair's two slices
+        const int nt = w.pair ? 2 : kg;
+        mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(nt * kATileBytes));
+        for (int h = 0; h < nt; ++h) {
           const uint32_t dst = dst0 + h * kATileBytes;
+          const int kx = w.pair ? kc : kc + h;
+          const int rx = w.pair ? row + h * (w.kind == 0 ? 64 : 128) : row;
           if (w.kind == 0) {
-            tma_load_2d(dst, m, &full[sa], (kc + h) * 64, row, pol);            // 64 gate rows
-            tma_load_2d(dst + 8192, m, &full[sa], (kc + h) * 64, row + p.F, pol);  // 64 up rows
+            tma_load_2d(dst, m, &full[sa], kx * 64, rx, pol);            // 64 gate rows
+            tma_load_2d(dst + 8192, m, &full[sa], kx * 64, rx + p.F, pol);  // 64 up rows
           } else {
-            tma_load_2d(dst, m, &full[sa], (kc + h) * 64, row, pol);  // 128 down rows
+            tma_load_2d(dst, m, &full[sa], kx * 64, rx, pol);  // 128 down rows
           }
         }
       }
@@ -597,7 +628,18 @@ __device__ void mma_issuer(const ExpertArgs& p, const Smem& s, const Rt& rt, uin
       for (int h = 0; h < kg; ++h) {
         const uint64_t bd =
             umma_desc_sw128(smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes + h * s.b_half_bytes));
-        if (p.a_tmem) {
+        if (w.pair) {
+          // the pair's two slices, each into its own accumulator (128 columns apart)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint64_t ad = umma_desc_sw128(
+                smem_u32(s.a_ring + static_cast<size_t>(sa) * s.a_stage_bytes + t * kATileBytes));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_bf16(d + 128u * t, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                        (kc | k) != 0 ? 1u : 0u);
+          }
+        } else if (p.a_tmem) {
           const uint32_t at = tmem_base + static_cast<uint32_t>(kTmemAStage0) + static_cast<uint32_t>(sa) * 128u +
                               static_cast<uint32_t>(h) * 32u;
 #pragma unroll
@@ -769,15 +811,18 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
     named_bar_sync(1, 128);
     if (!*s.s_ok) break;
     tc_fence_after();
-    const uint32_t tb =
+    const uint32_t tb0 =
         tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc) * static_cast<uint32_t>(p.acc_cols);
     if (w.kind == 0) {
+     for (int t = 0; t <= w.pair; ++t) {  // a pair's second slice is 128 columns on
+      const uint32_t tb = tb0 + 128u * static_cast<uint32_t>(t);
+      const int slice = w.slice + t;
       // Rows 0..63 of the tile are gate rows f, rows 64..127 the up rows of
       // the same f. Per 32 columns the gate warps take columns 0..15 and the
       // up warps 16..31, each handing the other half of its values over.
       const bool gate_half = q < 2;
       const int r64 = gate_half ? row : row - 64;
-      bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + w.slice * 64 + r64;
+      bf16* hrow = p.hbuf + static_cast<size_t>(w.off) * p.F + slice * 64 + r64;
       float* x_up = s.xch;              // [64][20] up values of columns 0..15
       float* x_gate = s.xch + 64 * 20;  // [64][20] gate values of columns 16..31
       const uint32_t tm = (rt.dense && w.e != p.E) ? rt.mask[w.e] : 0xffffffffu;
@@ -827,24 +872,28 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
           if (keep) hrow[static_cast<size_t>(slot) * p.F] = __float2bfloat16_rn(hv[j]);
         }
       }
+     }
       tc_fence_before();
       fence_proxy_async_global();
       __threadfence();
       named_bar_sync(1, 128);
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
-        red_release_gpu_add(&p.gu_done[w.a], 1);
+        red_release_gpu_add(&p.gu_done[w.a], 1 + w.pair);
       }
     } else {
-      float* ycol = p.yslot + static_cast<size_t>(w.off) * p.H + static_cast<size_t>(w.slice) * 128 + row;
-      for (int c0 = 0; c0 < n; c0 += 32) {
-        float v[32];
-        __syncwarp();
-        tmem_ld32(tb + c0, v);  // columns past n are read but never stored
+      for (int t = 0; t <= w.pair; ++t) {
+        const uint32_t tb = tb0 + 128u * static_cast<uint32_t>(t);
+        float* ycol = p.yslot + static_cast<size_t>(w.off) * p.H + static_cast<size_t>(w.slice + t) * 128 + row;
+        for (int c0 = 0; c0 < n; c0 += 32) {
+          float v[32];
+          __syncwarp();
+          tmem_ld32(tb + c0, v);  // columns past n are read but never stored
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int c = c0 + j;
-          if (c < w.cnt) ycol[static_cast<size_t>(c) * p.H] = v[j];
+          for (int j = 0; j < 32; ++j) {
+            const int c = c0 + j;
+            if (c < w.cnt) ycol[static_cast<size_t>(c) * p.H] = v[j];
+          }
         }
       }
       tc_fence_before();
@@ -1013,7 +1062,7 @@ __device__ void gather_warp(const ExpertArgs& p, const Smem& s, const Rt& rt) {
 template <bool kQ4>
 __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s, const Rt& rt, uint32_t tmem_base) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_total = rt.n_exp * ((p.F >> 6) + (p.H >> 7));
+  const int n_total = n_units(rt, p);
   if (warp == 0) {
     if (lane == 0) producer_a<kQ4>(p, s, rt, n_total);
   } else if (warp == 1) {
@@ -1197,6 +1246,13 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     if (p.out_w)
       for (int i = tid; i < MK; i += blockDim.x) p.out_w[i] = p.topk_w[i];
   }
+  // Paired chunks: those of the experts with more than p.pair_rows tokens, a
+  // prefix of the chunk list (the shared expert's chunks first, then the
+  // routed experts heaviest first).
+  __shared__ int s_npair;
+  if (tid == 0) s_npair = 0;
+  __syncthreads();
+  if (p.pair_rows >= 0 && tid < n_act && ce > p.pair_rows) atomicAdd(&s_npair, nch);
   fence_proxy_async_shared();  // the ring was used generically; TMA refills it
   __syncthreads();
   Rt rt;
@@ -1207,6 +1263,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.tok_slot = p.tok_slot;
   rt.topk_w = p.topk_w;
   rt.n_exp = fits ? n_sh + n_chunks : 0;
+  rt.n_pair = (p.pair_rows >= 0 && M > p.pair_rows && fits) ? n_sh + s_npair : 0;
   rt.dense = 0;
   rt.chunked = 1;
   rt.row_tok = row_tok;
@@ -1214,7 +1271,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.n_list = MK;
   rt.gbar = gbar;
   expert_roles<kQ4>(p, s, rt, tmem_base);
-  exit_reset(p, rt.n_exp, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), true);
+  exit_reset(p, rt.n_exp, n_units(rt, p), true);
 }
 
 
@@ -1559,6 +1616,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.tok_slot = s_slot;
   rt.topk_w = s_w;
   rt.n_exp = (*s.abort) ? 0 : *s_nact + 1;  // after a failed barrier no unit runs
+  rt.n_pair = 0;
   rt.dense = 1;
   rt.chunked = 0;
   rt.row_tok = nullptr;
@@ -1568,7 +1626,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
   if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
-  exit_reset(p, E + 1, rt.n_exp * ((p.F >> 6) + (p.H >> 7)), false);
+  exit_reset(p, E + 1, n_units(rt, p), false);
 }
 
 // smem_a: A stages in shared memory; stages_a: A barriers; kg: K groups of

@@ -142,6 +142,11 @@ struct ExpertArgs {
   // one K group of a wider chunk (units of more than kExpertTileTokens rows
   // then take one K group per stage).
   int tile_rows;
+  // Standalone bf16 kernel: the chunks of experts with more than pair_rows
+  // tokens run as paired units (two weight slices of one K group per stage,
+  // two accumulators of at most 128 columns sharing each B tile); negative:
+  // none.
+  int pair_rows;
   int smem_a;  // A stages in shared memory (= stages_a)
   // K groups of 64 per A/B stage (1, 2, or 4 on the low-bit path) for
   // gate/up and down units; a stage holds kg_stage groups of room (part h
