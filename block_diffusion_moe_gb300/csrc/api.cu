@@ -454,21 +454,13 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.kg_gu = kg_gu;
   xa.kg_dn = kg_dn;
   xa.kg_stage = kg;
-  // Above 256 tokens, hot experts in chunks of up to 256 rows where a B
-  // stage (two K groups of 128 rows) holds one K group of 256: their weights
-  // then stream half as often. At 256 tokens the narrower chunks are faster
-  // (the hottest expert's units run in parallel on more SMs and do not end
-  // the launch).
-  xa.tile_rows = (!fused && !q4 && M > 2 * kExpertTileTokens && kg_gu == 2 && kg_dn == 2 && nb == kExpertTileTokens)
-                     ? 2 * kExpertTileTokens
-                     : kExpertTileTokens;
-  // Up to 256 tokens every chunk runs as paired units: two weight slices
+  // Every chunk of the standalone kernel runs as paired units: two weight slices
   // share each B tile (an A stage of two K groups holds one K group of two
   // slices; two 128-column accumulators), halving the token rows each SM
   // takes in per weight byte. (Pairing only experts above 16, 32 or 64
   // tokens was slower on the same box: 3.68, 3.69, 3.71 against 3.64 ms per
   // Zipf step; none: 3.79.)
-  xa.pair_rows = (!fused && !q4 && xa.tile_rows == kExpertTileTokens && kg_gu == 2 && kg_dn == 2 &&
+  xa.pair_rows = (!fused && !q4 && kg_gu == 2 && kg_dn == 2 &&
                   (F / 64) % 2 == 0 && (H / 128) % 2 == 0)
                      ? 0
                      : -1;

@@ -76,7 +76,7 @@ struct Rt {
   int n_exp;                // fused: active routed experts + the shared expert; standalone: chunks
   int n_pair;               // standalone: the leading chunks whose units are paired (0: none)
   int dense;                // gate/up B operand = all M normed rows
-  int chunked;              // standalone: units index chunks of at most p.tile_rows rows
+  int chunked;              // standalone: units index chunks of at most kExpertTileTokens rows
   // standalone: the spare warp gathers this CTA's share of the token rows
   const uint16_t* row_tok;  // token of every routed row
   uint16_t* list;           // [n_list] the rows this CTA gathers
@@ -155,7 +155,6 @@ __device__ __forceinline__ int unit_kq(const Unit& w, const ExpertArgs& p) {
 
 // K groups per A/B stage of a unit (1, 2 or 4).
 __device__ __forceinline__ int unit_kg(const Unit& w, const ExpertArgs& p) {
-  if (w.cnt > kExpertTileTokens) return 1;  // a wide chunk: one K group fills a B stage
   if (w.pair) return 1;                     // two weight slices of one K group fill an A stage
   return w.kind == 0 ? p.kg_gu : p.kg_dn;
 }
@@ -1195,13 +1194,13 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   pt.row_tok = row_tok;
   const int n_act = cta_permutation(p.topk_idx, M, K, E, pt, blockIdx.x == 0 ? p.tok_slot : nullptr);
   const int tid = threadIdx.x;
-  // Unit tables: the expert's tokens in chunks of at most p.tile_rows rows
+  // Unit tables: the expert's tokens in chunks of at most kExpertTileTokens rows
   // (one accumulator's width): the shared expert's chunks first, then the
   // routed experts heaviest first (ties: lower id first), so that the
   // longest units are handed out first and do not end the launch; an
   // expert's chunks are adjacent, so its weight tiles are asked for at
   // nearly the same time by the CTAs that take them.
-  const int TR = p.tile_rows;
+  constexpr int TR = kExpertTileTokens;
   const int n_sh = (M + TR - 1) / TR;
   if (tid < E) {
     const int c = pt.cnt[tid];

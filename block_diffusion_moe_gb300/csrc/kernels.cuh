@@ -137,11 +137,6 @@ struct ExpertArgs {
   int a_tmem;
   int q_in_a;
   int acc_cols;  // TMEM columns per accumulator: 256, or 64 with a_tmem
-  // Standalone kernel: rows per expert chunk, kExpertTileTokens or twice that
-  // when a B stage of two K groups x kExpertTileTokens rows can instead hold
-  // one K group of a wider chunk (units of more than kExpertTileTokens rows
-  // then take one K group per stage).
-  int tile_rows;
   // Standalone bf16 kernel: the chunks of experts with more than pair_rows
   // tokens run as paired units (two weight slices of one K group per stage,
   // two accumulators of at most 128 columns sharing each B tile); negative:

@@ -31,11 +31,10 @@
  *     top_k <= n_experts <= 256, hidden <= 8192, 1 <= tokens <= 1024,
  *     vocab >= 2, 0 <= mask_id < vocab. Other shapes return
  *     CLOVER_ERR_UNSUPPORTED_SHAPE; there is no fallback path. Above 32
- *     tokens an expert's tokens are processed in tiles of at most 128 (256
- *     above 256 tokens, bf16 weights): an expert that more tokens select is
- *     streamed once per tile of its tokens (the tiles run side by side, so
- *     the repeat reads mostly come from L2); above 256 positions the head
- *     streams once per 256 positions.
+ *     tokens an expert's tokens are processed in tiles of at most 128: an
+ *     expert that more tokens select is streamed once per tile of its tokens
+ *     (the tiles run side by side, so the repeat reads mostly come from L2);
+ *     above 256 positions the head streams once per 256 positions.
  */
 #ifndef CLOVER_H_
 #define CLOVER_H_
@@ -119,9 +118,8 @@ size_t clover_moe_workspace_bytes(const clover_dims* dims, int32_t max_tokens);
  * not allowed. topk_idx (int32 [M][K]) and topk_w (fp32 [M][K]) receive the
  * selection in descending probability order; either may be NULL.
  * Each selected expert's weights are read from HBM once per call (up to 32
- * tokens; above, once per tile of 128 of its tokens, 256 above 256 tokens,
- * the repeats of one expert's tiles requested together so that L2 serves
- * them). */
+ * tokens; above, once per tile of 128 of its tokens, the repeats of one
+ * expert's tiles requested together so that L2 serves them). */
 int clover_moe_block_step(const clover_dims* dims, const clover_moe_layer* layer,
                           const float* x_in, float* x_out,
                           int32_t* topk_idx, float* topk_w, int32_t M,
