@@ -55,8 +55,6 @@ struct HeadSmem {
   uint32_t* tmem_slot;
   volatile uint32_t* abort;
   volatile int* s_ok;
-  volatile int* s_last;
-  int* s_counts;  // [2]: committed, still masked
   uint32_t half_bytes;   // one K group: A tile 16 KiB + B tile nb x 128 B
   uint32_t stage_bytes;  // kg K groups
 };
@@ -90,8 +88,6 @@ __device__ __forceinline__ HeadSmem carve(uint8_t* raw, const HeadArgs& p, int n
   s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
   s.abort = s.tmem_slot + 1;
   s.s_ok = reinterpret_cast<volatile int*>(s.tmem_slot + 2);
-  s.s_last = s.s_ok + 1;
-  s.s_counts = const_cast<int*>(s.s_last + 1);
   return s;
 }
 

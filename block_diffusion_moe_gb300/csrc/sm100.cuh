@@ -114,21 +114,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Gathers four rows of a 2-D tensor into shared memory: rows r0..r3 (any
-// order, any rows of the tensor), columns c0..c0+box-1 each, written as four
-// consecutive rows at dst (swizzled like a tiled load of those rows). The
-// tensor map's box is one row high. Completion is signalled on `bar` as
-// 4 x box row bytes. c0 must be a multiple of 8 for 16-bit types.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int32_t c0, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "l"(policy)
-      : "memory");
-}
-
 // Contiguous bulk copy global -> shared (16-byte aligned, size % 16 == 0),
 // completing as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
