@@ -325,7 +325,7 @@ int resident_per_sm(bool fused, bool q4, size_t smem, int* out) {
 int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const float* x_in, float* x_out,
                       int32_t* out_idx, float* out_w, int M, uint8_t* data, int* ctrl, int* err, const Plan& plan,
                       cudaStream_t stream, const void* next_router = nullptr, bool defer = false, bool pend = false,
-                      bool xn_ready = false, bool norm_next = false) {
+                      bool xn_ready = false, bool norm_next = false, const clover_moe_layer* next_layer = nullptr) {
   const MoeLayout L = moe_layout(d, M);
   const int H = d.hidden, F = d.d_ff, E = d.n_experts, K = d.top_k;
   const int MK = M * K;
@@ -523,6 +523,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   // (a few µs); with more tokens that serial walk would dominate, so a
   // parallel kernel does it.
   xa.combine = fused ? (defer ? 2 : 1) : 0;
+  // the next layer's shared expert, prefetched into L2 by CTAs that have run out of units
+  xa.sgu_next = (next_layer && !q4) ? reinterpret_cast<const bf16*>(next_layer->sh_gate_up) : nullptr;
+  xa.sdn_next = (next_layer && !q4) ? reinterpret_cast<const bf16*>(next_layer->sh_down) : nullptr;
   xa.pend = pend ? 1 : 0;
   xa.fin_w = reinterpret_cast<float*>(data + L.fin_w);
   // (slots inside the A ring add only their barriers)
@@ -774,7 +777,7 @@ int denoise_step_impl(const clover_dims* dims, const clover_moe_layer* layers, i
     rc = enqueue_moe_layer(*dims, layers[l], x, x, nullptr, nullptr, M, ws + L.moe,
                            reinterpret_cast<int*>(ws + L.moe_ctrl), err, plan, s,
                            l + 1 < n_layers ? layers[l + 1].router_w : nullptr, defer, defer && l > 0,
-                           chain_norm && l > 0, chain_norm && l + 1 < n_layers);
+                           chain_norm && l > 0, chain_norm && l + 1 < n_layers, l + 1 < n_layers ? &layers[l + 1] : nullptr);
     if (rc) return rc;
   }
   if (defer && n_layers > 0 && (rc = enqueue_combine(*dims, x, M, ws + L.moe, s))) return rc;

@@ -174,6 +174,8 @@ struct ExpertArgs {
   float* fin_w; // [M][K] final selection weights published for a deferred combine
   // fused-layer launches only (k_layer)
   const bf16* wr;      // [E][H] router
+  const bf16* sgu_next;  // the next layer's shared expert (nullable): prefetched into L2 at the end
+  const bf16* sdn_next;
   const bf16* wr_next; // [E][H] the next layer's router (nullable): its slices are prefetched into L2
   const float* bias;   // [E] or null
   float* logits;       // [M][E]
