@@ -1114,8 +1114,12 @@ namespace {
 // timeout.
 __device__ bool grid_barrier(unsigned long long* count, int* err) {
   __shared__ int s_pass;
+  // Ordering: the CTA barrier orders every thread's earlier stores before
+  // thread 0's release (its acq_rel arrival), and thread 0's acquire before
+  // every thread's later loads (which read other CTAs' data through L2 or
+  // TMA), so no thread needs a fence of its own (same box: a fence in every
+  // thread on both sides cost 5.690 vs 5.630 ms per step).
   fence_proxy_async_global();  // rows stored before the barrier are read by TMA after it
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const unsigned long long g = gridDim.x;
@@ -1136,7 +1140,6 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
     s_pass = pass;
   }
   __syncthreads();
-  __threadfence();
   fence_proxy_async_global();
   return s_pass != 0;
 }
@@ -1441,10 +1444,10 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
       if (x_staged && wr_staged && H == 2048 && ne == kRouteExperts) {
         lg = warp_router_row_smem<kRouteExperts, 2048>(smem_u32(xr), p.eps, smem_u32(w_rows), lane, xn_out);
       } else if (H <= 128 * 16) {
-        lg = warp_router_row_reg<kRouteExperts, 16>(xr, p.eps, w_rows, ne, H, lane, xn_out);
+        lg = warp_router_row_reg<kRouteExperts, 16>(xr, p.eps, w_rows, ne, H, lane, xn_out, !x_staged);
       } else {
-        const float rstd = row_rstd(xr, H, p.eps, lane);
-        lg = warp_router_dots<kRouteExperts>(xr, rstd, w_rows, ne, H, lane, xn_out);
+        const float rstd = row_rstd(xr, H, p.eps, lane, !x_staged);
+        lg = warp_router_dots<kRouteExperts>(xr, rstd, w_rows, ne, H, lane, xn_out, !x_staged);
       }
       if (lane < ne) {
         const float v = lg + (p.bias ? p.bias[e0 + lane] : 0.f);

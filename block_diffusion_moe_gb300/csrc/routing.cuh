@@ -18,11 +18,17 @@ namespace clover {
 
 // Reciprocal RMS of one row, computed by one warp: 1 / sqrt(mean(x^2) + eps).
 // Loads are unrolled so that several are in flight per lane.
-__device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int lane) {
+// (l2: the row is global memory that other CTAs of this launch wrote, read
+// through L2 rather than the SM's L1.)
+__device__ __forceinline__ float4 row_load4(const float* p, bool l2) {
+  return l2 ? __ldcg(reinterpret_cast<const float4*>(p)) : *reinterpret_cast<const float4*>(p);
+}
+
+__device__ __forceinline__ float row_rstd(const float* xr, int H, float eps, int lane, bool l2 = false) {
   float ss = 0.f;
 #pragma unroll 8
   for (int c = lane * 4; c < H; c += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    const float4 v = row_load4(xr + c, l2);
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = warp_sum_f(ss);
@@ -52,12 +58,12 @@ __device__ __forceinline__ float rstd_row16(const float4 (&xv)[16], int H, float
 // once). Same arithmetic order, so the results are identical.
 template <int kMaxE, int kChunks>
 __device__ __forceinline__ float warp_router_row_reg(const float* xr, float eps, const __nv_bfloat16* w_rows, int ne,
-                                                     int H, int lane, __nv_bfloat16* xn_out) {
+                                                     int H, int lane, __nv_bfloat16* xn_out, bool l2 = false) {
   float4 xv[kChunks];
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) {
     const int c = lane * 4 + 128 * j;
-    xv[j] = (c < H) ? *reinterpret_cast<const float4*>(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    xv[j] = (c < H) ? row_load4(xr + c, l2) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float ss = 0.f;
 #pragma unroll
@@ -268,13 +274,13 @@ __device__ __forceinline__ float cta_router_item_mma(uint32_t x_rows, int n_tok,
 // bf16 row of H. Lane e (< ne) receives logit e (without bias).
 template <int kMaxE>
 __device__ __forceinline__ float warp_router_dots(const float* xr, float rstd, const __nv_bfloat16* w_rows, int ne,
-                                                  int H, int lane, __nv_bfloat16* xn_out) {
+                                                  int H, int lane, __nv_bfloat16* xn_out, bool l2 = false) {
   float acc[kMaxE];
 #pragma unroll
   for (int e = 0; e < kMaxE; ++e) acc[e] = 0.f;
 #pragma unroll 4
   for (int c = lane * 4; c < H; c += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(xr + c);
+    const float4 v = row_load4(xr + c, l2);
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * rstd, v.y * rstd);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * rstd, v.w * rstd);
     if (xn_out != nullptr) {
