@@ -890,9 +890,11 @@ __device__ void epilogue(const ExpertArgs& p, const Smem& s, const Rt& rt, uint3
         }
       }
      }
+      // The h rows are published by one release after the epilogue barrier
+      // (which orders every epilogue thread's stores before it); each thread
+      // orders its stores for the TMA loads that read them.
       tc_fence_before();
       fence_proxy_async_global();
-      __threadfence();
       named_bar_sync(1, 128);
       if (etid == 0) {
         mbar_arrive(&s.tempty[acc]);
@@ -1155,15 +1157,15 @@ __device__ bool grid_barrier(unsigned long long* count, int* err) {
 // drawn) is reported.
 __device__ void exit_reset(const ExpertArgs& p, int n_entries, int n_total, bool gathered) {
   __shared__ int s_lastx;
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();  // (cumulative over the CTA's accesses ordered by the barrier)
     const int old = atomicAdd(p.exit_ctr, 1);
+    __threadfence();
     s_lastx = (old == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
   }
   __syncthreads();
   if (s_lastx) {
-    __threadfence();
     for (int i = threadIdx.x; i < n_entries; i += blockDim.x) {
       p.gu_done[i] = 0;
       if (gathered) p.gathered[i] = 0;

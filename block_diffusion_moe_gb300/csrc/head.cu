@@ -574,17 +574,17 @@ __global__ void __launch_bounds__(256) k_head_merge(const __grid_constant__ Head
       p.dec_a[n] = a;
     }
   }
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();  // (cumulative over the CTA's stores ordered by the barrier)
     const int old = atomicAdd(p.done_ctr, 1);
+    __threadfence();
     s_last = (old == static_cast<int>(gridDim.x) - 1) ? 1 : 0;
     s_counts[0] = 0;
     s_counts[1] = 0;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   // The last CTA: every position's decision inputs into shared memory at
   // once (M <= kTileTokens per launch), then one thread per block.
   for (int i = threadIdx.x; i < p.M; i += blockDim.x) {

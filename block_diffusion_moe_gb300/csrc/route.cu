@@ -258,15 +258,17 @@ __global__ void __launch_bounds__(256, 1) k_route(RouteArgs a) {
       a.logits[static_cast<size_t>(t0 + r) * E + e] = sum + (a.bias ? a.bias[e] : 0.f);
     }
   }
-  __threadfence();
+  // One fence on each side by the arriving thread: the CTA barrier orders the
+  // other threads' logit stores before it, and their later loads after it.
   __syncthreads();
   if (tid == 0) {
+    __threadfence();
     const int old = atomicAdd(&a.tg_ctr[blockIdx.y], 1);
+    __threadfence();
     s_last = (old == static_cast<int>(gridDim.x) - 1);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   // Top-k for this token tile: warp w takes tile rows w and w + 8 together.
   const float* rows[2];
