@@ -250,6 +250,39 @@ int encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return CLOVER_OK;
 }
 
+// A rank-n strided bf16 view (dims[0] innermost, contiguous; strides in
+// bytes of dims 1..n-1), boxes with 128-byte swizzle.
+int encode_bf16_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box, const char* what) {
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(CLOVER_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
+  return CLOVER_OK;
+}
+
+// The whole-stage views of one expert stack (n experts; see ExpertArgs):
+// gate/up [n][2F][H], down [n][H][F]. A view is encoded only for the shapes
+// whose units use it (two-group stages need an even number of K groups).
+int encode_stage_maps(CUtensorMap* gu_k2, CUtensorMap* dn_k2, const void* gate_up, const void* down, uint64_t n,
+                      uint64_t H, uint64_t F) {
+  int rc;
+  if ((H / 64) % 2 == 0) {  // (64 c, rows, gate|up, K group): gate row r, its up row r + F
+    const cuuint64_t dims[4] = {64, n * 2 * F - F, 2, H / 64};
+    const cuuint64_t str[3] = {H * 2, F * H * 2, 128};
+    const cuuint32_t box[4] = {64, 64, 2, 2};
+    if ((rc = encode_bf16_nd(gu_k2, gate_up, 4, dims, str, box, "gate_up stage view"))) return rc;
+  }
+  if ((F / 64) % 2 == 0) {  // (64 c, rows, K group)
+    const cuuint64_t dims[3] = {64, n * H, F / 64};
+    const cuuint64_t str[2] = {F * 2, 128};
+    const cuuint32_t box[3] = {64, 128, 2};
+    if ((rc = encode_bf16_nd(dn_k2, down, 3, dims, str, box, "down stage view"))) return rc;
+  }
+  return CLOVER_OK;
+}
+
 // 4-bit codes as bytes: rows of `cols_bytes`, boxes of box_cols bytes x
 // box_rows (the converter warps read them).
 int encode_u8_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols_bytes, uint32_t box_cols,
@@ -395,6 +428,9 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
     if ((rc = encode_bf16_2d(&xa.tm_sgu, layer.sh_gate_up, 2ull * F, H, 64, "shared gate_up"))) return rc;
     if ((rc = encode_bf16_2d(&xa.tm_dn, layer.down, static_cast<uint64_t>(E) * H, F, 128, "down"))) return rc;
     if ((rc = encode_bf16_2d(&xa.tm_sdn, layer.sh_down, H, F, 128, "shared down"))) return rc;
+    if ((rc = encode_stage_maps(&xa.tm_gu_k2, &xa.tm_dn_k2, layer.gate_up, layer.down, E, H, F))) return rc;
+    if ((rc = encode_stage_maps(&xa.tm_sgu_k2, &xa.tm_sdn_k2, layer.sh_gate_up, layer.sh_down, 1, H, F))) return rc;
+    xa.stage_maps = 1;
   }
   // B tiles move in boxes of up to 64 rows (one TMA instruction each), with
   // 16-row boxes for the rest; fewer, larger copies stream faster.

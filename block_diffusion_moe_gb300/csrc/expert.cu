@@ -349,7 +349,17 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
         // kg K groups of one slice, or one K group of a pair's two slices
         const int nt = w.pair ? 2 : kg;
         mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(nt * kATileBytes));
-        for (int h = 0; h < nt; ++h) {
+        // Two K groups of one slice in one box (same layout). (One box for a
+        // pair's two slices measured 0.4% slower on the batched step.)
+        const bool one_box = p.stage_maps && !w.pair && kg == 2;
+        if (one_box) {
+          const bool sh = w.e == p.E;
+          if (w.kind == 0)
+            tma_load_4d(dst0, sh ? &p.tm_sgu_k2 : &p.tm_gu_k2, &full[sa], 0, row, 0, kc, pol);
+          else
+            tma_load_3d(dst0, sh ? &p.tm_sdn_k2 : &p.tm_dn_k2, &full[sa], 0, row, kc, pol);
+        }
+        for (int h = 0; h < nt && !one_box; ++h) {
           const uint32_t dst = dst0 + h * kATileBytes;
           const int kx = w.pair ? kc : kc + h;
           const int rx = w.pair ? row + h * (w.kind == 0 ? 64 : 128) : row;
@@ -971,6 +981,12 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
     tma_prefetch_desc(kQ4 ? &p.tm_sgu_q : &p.tm_sgu);
     tma_prefetch_desc(kQ4 ? &p.tm_dn_q : &p.tm_dn);
     tma_prefetch_desc(kQ4 ? &p.tm_sdn_q : &p.tm_sdn);
+    if (!kQ4 && p.stage_maps) {
+      tma_prefetch_desc(&p.tm_gu_k2);
+      tma_prefetch_desc(&p.tm_sgu_k2);
+      tma_prefetch_desc(&p.tm_dn_k2);
+      tma_prefetch_desc(&p.tm_sdn_k2);
+    }
   }
   if (warp == 2 && lane == 0) {
     tma_prefetch_desc(&p.tm_xg);

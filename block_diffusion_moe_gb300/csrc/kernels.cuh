@@ -112,6 +112,14 @@ struct ExpertArgs {
   CUtensorMap tm_sgu;  // shared gate/up  [2F][H]
   CUtensorMap tm_dn;   // routed down     [E*H][F]
   CUtensorMap tm_sdn;  // shared down     [H][F]
+  // Whole-stage views of the same bf16 weights (stage_maps != 0): an A
+  // stage of two K groups of one slice in one TMA instruction instead of
+  // two (down) or four (gate/up): gate/up (64 c, rows, gate|up, K group),
+  // box 64 x 64 x 2 x 2; down (64 c, rows, K group), box 64 x 128 x 2. Each
+  // view aliases dimensions of the 2-D matrix, its row extent cut so that
+  // no in-range coordinate reaches past the tensor.
+  CUtensorMap tm_gu_k2, tm_sgu_k2, tm_dn_k2, tm_sdn_k2;
+  int stage_maps;
   CUtensorMap tm_xg;   // gathered inputs [M*K+M][H], boxes of 16 rows
   CUtensorMap tm_h;    // SwiGLU outputs  [M*K+M][F], boxes of 16 rows
   CUtensorMap tm_xg_big;  // the same, boxes of xg_box rows
