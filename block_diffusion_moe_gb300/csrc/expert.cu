@@ -77,11 +77,11 @@ struct Rt {
   int n_pair;               // standalone: the leading chunks whose units are paired (0: none)
   int dense;                // gate/up B operand = all M normed rows
   int chunked;              // standalone: units index chunks of at most kExpertTileTokens rows
-  // standalone: the spare warp gathers this CTA's share of the token rows
+  // standalone: warps 3-7 gather this CTA's share of the token rows
   const uint16_t* row_tok;  // token of every routed row
   uint16_t* list;           // [n_list] the rows this CTA gathers
   int n_list;
-  uint64_t* gbar;           // bulk-copy barrier of the gather
+  int gather;
 };
 
 // Unit numbering: the gate/up units of the paired chunks (two slices each),
@@ -543,7 +543,7 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       box = p.xg_box;
       nk = p.H >> 6;
       if (rt.chunked && w.e != p.E) {
-        // The chunk's token rows are gathered by the CTAs' spare warps at
+        // The chunk's token rows are gathered by warps 3-7 of every CTA at
         // the start of the launch: wait (bounded) until all of them are in.
         const unsigned long long t0 = global_ns();
         bool ok = true;
@@ -1020,77 +1020,84 @@ __device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G) {
   return nr;
 }
 
-// The standalone kernel's spare warp (7), while the other roles start:
-// copies the normed rows of the routed chunks' tokens into expert order (row
-// r of the gathered buffer = normed row of token row_tok[r]), this CTA's
-// share of the pieces. It lists the rows (hottest chunks first), then lane 0
-// moves them with bulk copies through the activation ring (global -> shared
-// -> global, one copy per row each way; the activation producer, which
-// waits at named barrier 5, takes the ring once the copies have read it),
-// waits for the stores, and the warp publishes, per chunk, how many rows
-// this CTA gathered (release). A gate/up unit of the chunk loads them once
-// the chunk's counter reaches its row count; no CTA waits for all others.
-__device__ void gather_warp(const ExpertArgs& p, const Smem& s, const Rt& rt) {
-  const int G = gridDim.x, lane = threadIdx.x & 31;
-  int base = 0;
-  for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
-    const int a = a0 + lane;
-    const bool mine = a < rt.n_exp && rt.act[a] != p.E;
-    const int nr = mine ? owned_rows(rt, a, G) : 0;
-    int incl = nr;
+// The standalone kernel's gather, by warps 3-7 while the other roles start
+// (the epilogue warps have no accumulator to drain yet): copies the normed
+// rows of the routed chunks' tokens into expert order (row r of the
+// gathered buffer = normed row of token row_tok[r]), this CTA's share of the
+// pieces. Warp 7 lists the rows (hottest chunks first); then each of the
+// five warps copies every fifth row with 16-byte loads and stores, two rows
+// in flight (no bulk copies: a CTA's TMA unit takes one copy at a time, and
+// a few µs of its own row copies had held up the first units); finally warp
+// 7 publishes, per chunk, how many rows this CTA gathered (release). A
+// gate/up unit of the chunk loads them once the chunk's counter reaches its
+// row count; no CTA waits for all others.
+__device__ void gather_rows(const ExpertArgs& p, const Rt& rt) {
+  constexpr int kW = 5;
+  const int G = gridDim.x, lane = threadIdx.x & 31, gw = (threadIdx.x >> 5) - 3;
+  __shared__ int s_nrows;
+  if (gw == kW - 1) {
+    int base = 0;
+    for (int a0 = 0; a0 < rt.n_exp; a0 += 32) {
+      const int a = a0 + lane;
+      const bool mine = a < rt.n_exp && rt.act[a] != p.E;
+      const int nr = mine ? owned_rows(rt, a, G) : 0;
+      int incl = nr;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (mine) {
-      int at = base + incl - nr;
-      const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
-      for (int q = first_piece(a, G); q < n_q; q += G)
-        for (int j = 4 * q; j < min(4 * q + 4, cnt); ++j, ++at)
-          if (at < rt.n_list) rt.list[at] = static_cast<uint16_t>(rt.off[a] + j);
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  __syncwarp();
-  const int n_rows = min(base, rt.n_list);
-  int ok = 1;
-  if (lane == 0) {
-    const uint32_t row_bytes = static_cast<uint32_t>(p.H) * 2u;
-    const int per_round = static_cast<int>((static_cast<uint32_t>(p.stages_b) * s.b_stage_bytes) / row_bytes);
-    const uint32_t ring = smem_u32(s.b_ring);
-    uint32_t phase = 0;
-    for (int r0 = 0; r0 < n_rows; r0 += per_round) {
-      const int n = min(per_round, n_rows - r0);
-      mbar_arrive_expect_tx(rt.gbar, static_cast<uint32_t>(n) * row_bytes);
-      for (int j = 0; j < n; ++j)
-        bulk_load(ring + j * row_bytes, p.xn + static_cast<size_t>(rt.row_tok[rt.list[r0 + j]]) * p.H, row_bytes,
-                  rt.gbar);
-      if (!mbar_wait(rt.gbar, phase, s.abort)) {
-        raise_abort(s, p.err, kErrMbarTimeout);
-        mbar_wait_for(rt.gbar, phase, 200000000ull);  // no copy may still land in the ring
-        ok = 0;
-        break;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      phase ^= 1u;
-      for (int j = 0; j < n; ++j)
-        bulk_store(p.xg + static_cast<size_t>(rt.list[r0 + j]) * p.H, ring + j * row_bytes, row_bytes);
-      bulk_commit();
-      bulk_wait_read_all();  // the ring may take the next rows
+      if (mine) {
+        int at = base + incl - nr;
+        const int cnt = rt.cnt[a], n_q = (cnt + 3) >> 2;
+        for (int q = first_piece(a, G); q < n_q; q += G)
+          for (int j = 4 * q; j < min(4 * q + 4, cnt); ++j, ++at)
+            if (at < rt.n_list) rt.list[at] = static_cast<uint16_t>(rt.off[a] + j);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s_nrows = min(base, rt.n_list);
+  }
+  named_bar_sync(5, 32 * kW);
+  const int n_rows = s_nrows;
+  const int nv = p.H >> 3;  // 16-byte pieces per row
+  for (int r = gw; r < n_rows; r += 2 * kW) {
+    const bool two = r + kW < n_rows;
+    const int ra = rt.list[r], rb = two ? rt.list[r + kW] : ra;
+    const uint4* a_src = reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(rt.row_tok[ra]) * p.H);
+    const uint4* b_src = reinterpret_cast<const uint4*>(p.xn + static_cast<size_t>(rt.row_tok[rb]) * p.H);
+    uint4* a_dst = reinterpret_cast<uint4*>(p.xg + static_cast<size_t>(ra) * p.H);
+    uint4* b_dst = reinterpret_cast<uint4*>(p.xg + static_cast<size_t>(rb) * p.H);
+    for (int v0 = 0; v0 < nv; v0 += 256) {
+      uint4 va[8], vb[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int v = v0 + 32 * j + lane;
+        if (v < nv) {
+          va[j] = __ldcg(a_src + v);
+          if (two) vb[j] = __ldcg(b_src + v);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int v = v0 + 32 * j + lane;
+        if (v < nv) {
+          a_dst[v] = va[j];
+          if (two) b_dst[v] = vb[j];
+        }
+      }
     }
   }
-  __syncwarp();
-  named_bar_arrive(5, 64);  // the activation ring is the B producer's now
-  if (lane == 0) {
-    bulk_wait_all();  // the rows are in global memory
-    fence_proxy_async_global();
-    __threadfence();
-  }
-  if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-  for (int a = lane; a < rt.n_exp; a += 32) {
-    if (rt.act[a] == p.E) continue;
-    const int nr = owned_rows(rt, a, G);
-    if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
+  // each thread orders its stores for the TMA loads that read them; the
+  // barrier orders all of them before warp 7's releases
+  fence_proxy_async_global();
+  named_bar_sync(5, 32 * kW);
+  if (gw == kW - 1) {
+    for (int a = lane; a < rt.n_exp; a += 32) {
+      if (rt.act[a] == p.E) continue;
+      const int nr = owned_rows(rt, a, G);
+      if (nr > 0) red_release_gpu_add(&p.gathered[a], nr);
+    }
   }
 }
 
@@ -1103,12 +1110,12 @@ __device__ __forceinline__ void expert_roles(const ExpertArgs& p, const Smem& s,
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(p, s, rt, tmem_base);
   } else if (warp == 2) {
-    if (rt.gbar != nullptr) named_bar_sync(5, 64);  // after the gather's copies have left the ring
     if (lane == 0) producer_b(p, s, rt);
   } else if (warp < 7) {
+    if (rt.gather) gather_rows(p, rt);
     epilogue(p, s, rt, tmem_base);
   } else if (warp == 7) {
-    if (rt.gbar != nullptr) gather_warp(p, s, rt);  // otherwise warp 7 has no role here
+    if (rt.gather) gather_rows(p, rt);  // otherwise warp 7 has no role here
   } else if (kQ4) {
     converter(p, s, rt, tmem_base);
   }
@@ -1200,9 +1207,6 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
     k_expert(const __grid_constant__ ExpertArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
-  // bulk-copy barrier of the gather (made visible by the prologue's fence)
-  uint64_t* gbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(s.tmem_slot) + 96);
-  if (threadIdx.x == 0) mbar_init(gbar, 1);
   const uint32_t tmem_base = expert_prologue<kQ4>(p, s);
   pdl_wait();
   pdl_trigger();
@@ -1211,7 +1215,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   // scratch in the still idle weight ring) and keeps the token of every row
   // and the unit tables in its own shared memory, so no CTA waits for
   // another before its units: the weight stream starts right after the
-  // permutation, while the spare warps gather the token rows chunk by chunk
+  // permutation, while warps 3-7 gather the token rows chunk by chunk
   // and each gate/up unit waits only for its own chunk's rows.
   uint16_t* row_tok = reinterpret_cast<uint16_t*>(s.rt_region);
   const int NC = p.max_chunks;
@@ -1307,7 +1311,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.row_tok = row_tok;
   rt.list = list;
   rt.n_list = MK;
-  rt.gbar = gbar;
+  rt.gather = 1;
   expert_roles<kQ4>(p, s, rt, tmem_base);
   exit_reset(p, rt.n_exp, n_units(rt, p), true);
 }
@@ -1660,7 +1664,7 @@ __global__ void __launch_bounds__(kQ4 ? kExpertThreadsQ4 : kExpertThreads, 1)
   rt.row_tok = nullptr;
   rt.list = nullptr;
   rt.n_list = 0;
-  rt.gbar = nullptr;
+  rt.gather = 0;
   if (st) st[4] = global_ns();
   expert_roles<kQ4>(p, s, rt, tmem_base);
   if (kPhaseStamps && p.stamps != nullptr && threadIdx.x == 0) atomicMax(p.stamps + 5, global_ns());
