@@ -250,16 +250,23 @@ int encode_bf16_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return CLOVER_OK;
 }
 
-// A rank-n strided bf16 view (dims[0] innermost, contiguous; strides in
-// bytes of dims 1..n-1), boxes with 128-byte swizzle.
-int encode_bf16_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                   const cuuint32_t* box, const char* what) {
+// A rank-n strided view (dims[0] innermost, contiguous; strides in bytes of
+// dims 1..n-1).
+int encode_nd(CUtensorMap* m, CUtensorMapDataType type, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle, const char* what) {
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
-                        dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = g_encode(m, type, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(CLOVER_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, static_cast<int>(r));
   return CLOVER_OK;
+}
+
+// The same for bf16 with 128-byte swizzle (the layout the UMMA descriptors expect).
+int encode_bf16_nd(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box, const char* what) {
+  return encode_nd(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                   what);
 }
 
 // The whole-stage views of one expert stack (n experts; see ExpertArgs):
@@ -418,6 +425,38 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
       return rc;
     if ((rc = encode_u8_2d(&xa.tm_sdn_q, layer.sh_down_q, H, F / 2, xa.kq_dn * 32, 128, "shared down codes")))
       return rc;
+    for (int sh = 0; sh < 2; ++sh) {  // the whole-slot views, routed then shared
+      const uint64_t n = sh ? 1 : E;
+      {  // codes: (H/2 bytes, gate rows, gate|up)
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(H / 2), n * 2 * F - F, 2};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(H / 2), static_cast<cuuint64_t>(F) * (H / 2)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(xa.kq_gu * 32), 64, 2};
+        if ((rc = encode_nd(sh ? &xa.tm_sgu_q3 : &xa.tm_gu_q3, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                            sh ? layer.sh_gate_up_q : layer.gate_up_q, 3, dims, str, box,
+                            xa.kq_gu * 32 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                            "gate_up code view")))
+          return rc;
+      }
+      {  // gate/up scales [n][H/64][2F]: (gate scale, gate|up, K group)
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(F), 2, n * (H / 64)};
+        const cuuint64_t str[2] = {static_cast<cuuint64_t>(F) * 2, static_cast<cuuint64_t>(F) * 4};
+        const cuuint32_t box[3] = {64, 2, static_cast<cuuint32_t>(xa.kq_gu)};
+        if ((rc = encode_nd(sh ? &xa.tm_sgu_sv : &xa.tm_gu_sv, CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                            sh ? layer.sh_gate_up_s : layer.gate_up_s, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            "gate_up scale view")))
+          return rc;
+      }
+      {  // down scales [n][F/64][H]: (scale, K group)
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), n * (F / 64)};
+        const cuuint64_t str[1] = {static_cast<cuuint64_t>(H) * 2};
+        const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(xa.kq_dn)};
+        if ((rc = encode_nd(sh ? &xa.tm_sdn_sv : &xa.tm_dn_sv, CU_TENSOR_MAP_DATA_TYPE_UINT16,
+                            sh ? layer.sh_down_s : layer.down_s, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            "down scale view")))
+          return rc;
+      }
+    }
+    xa.q4_views = 1;
     xa.gu_s = layer.gate_up_s;
     xa.sgu_s = layer.sh_gate_up_s;
     xa.dn_s = layer.down_s;

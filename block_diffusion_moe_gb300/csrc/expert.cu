@@ -327,7 +327,16 @@ __device__ void producer_a(const ExpertArgs& p, const Smem& s, const Rt& rt, int
         const uint32_t dst = smem_u32(s.q_ring + static_cast<size_t>(sa) * kQSlotBytes);
         mbar_arrive_expect_tx(&full[sa], static_cast<uint32_t>(kq * kQGroupBytes));
         const uint32_t sdst = dst + kq * 4096;
-        if (w.kind == 0) {
+        const bool sh = w.e == p.E;
+        if (p.q4_views && w.kind == 0) {  // gate and up codes in one box, the kq groups' scales in another
+          tma_load_3d(dst, sh ? &p.tm_sgu_q3 : &p.tm_gu_q3, &full[sa], kc * 32, row, 0, pol);
+          tma_load_3d(sdst, sh ? &p.tm_sgu_sv : &p.tm_gu_sv, &full[sa], w.slice * 64, 0,
+                      (sh ? 0 : w.e * (p.H >> 6)) + kc, pol);
+        } else if (p.q4_views) {
+          tma_load_2d(dst, sh ? &p.tm_sdn_q : &p.tm_dn_q, &full[sa], kc * 32, row, pol);
+          tma_load_2d(sdst, sh ? &p.tm_sdn_sv : &p.tm_dn_sv, &full[sa], w.slice * 128,
+                      (sh ? 0 : w.e * (p.F >> 6)) + kc, pol);
+        } else if (w.kind == 0) {
           const CUtensorMap* mq = (w.e == p.E) ? &p.tm_sgu_q : &p.tm_gu_q;
           tma_load_2d(dst, mq, &full[sa], kc * 32, row, pol);
           tma_load_2d(dst + kq * 2048, mq, &full[sa], kc * 32, row + p.F, pol);
@@ -981,6 +990,14 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
     tma_prefetch_desc(kQ4 ? &p.tm_sgu_q : &p.tm_sgu);
     tma_prefetch_desc(kQ4 ? &p.tm_dn_q : &p.tm_dn);
     tma_prefetch_desc(kQ4 ? &p.tm_sdn_q : &p.tm_sdn);
+    if (kQ4 && p.q4_views) {
+      tma_prefetch_desc(&p.tm_gu_q3);
+      tma_prefetch_desc(&p.tm_sgu_q3);
+      tma_prefetch_desc(&p.tm_gu_sv);
+      tma_prefetch_desc(&p.tm_sgu_sv);
+      tma_prefetch_desc(&p.tm_dn_sv);
+      tma_prefetch_desc(&p.tm_sdn_sv);
+    }
     if (!kQ4 && p.stage_maps) {
       tma_prefetch_desc(&p.tm_gu_k2);
       tma_prefetch_desc(&p.tm_sgu_k2);
