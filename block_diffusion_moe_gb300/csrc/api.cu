@@ -529,6 +529,15 @@ int enqueue_moe_layer(const clover_dims& d, const clover_moe_layer& layer, const
   xa.kg_gu = kg_gu;
   xa.kg_dn = kg_dn;
   xa.kg_stage = kg;
+  if (fused && kg_gu > 1) {
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(H / 64)};
+    const cuuint64_t str[2] = {static_cast<cuuint64_t>(H) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(nb_rows), static_cast<cuuint32_t>(kg_gu)};
+    if ((rc = encode_bf16_nd(&xa.tm_xg_k, xg + static_cast<size_t>(MK) * H, 3, dims, str, box,
+                             "normed rows stage view")))
+      return rc;
+    xa.xg_k = 1;
+  }
   // Every chunk of the standalone kernel runs as paired units: two weight slices
   // share each B tile (an A stage of two K groups holds one K group of two
   // slices; two 128-column accumulators), halving the token rows each SM

@@ -606,7 +606,11 @@ __device__ void producer_b(const ExpertArgs& p, const Smem& s, const Rt& rt) {
       }
       const uint32_t dst0 = smem_u32(s.b_ring + static_cast<size_t>(sb) * s.b_stage_bytes);
       mbar_arrive_expect_tx(&s.full_b[sb], static_cast<uint32_t>(kg * nrows) * 128u);
-      for (int h = 0; h < kg; ++h) {
+      // the dense normed rows of all kg groups in one box (same layout)
+      const bool one_box = p.xg_k && w.kind == 0 && rt.dense && kg == p.kg_gu && nrows == box &&
+                           static_cast<uint32_t>(nrows) * 128u == s.b_half_bytes;
+      if (one_box) tma_load_3d(dst0, &p.tm_xg_k, &s.full_b[sb], 0, 0, kc, pol);
+      for (int h = 0; h < kg && !one_box; ++h) {
         const uint32_t dst = dst0 + h * s.b_half_bytes;
         for (int i = 0; i < nrows;) {
           const bool big = nrows - i >= box;
@@ -990,6 +994,7 @@ __device__ __forceinline__ uint32_t expert_prologue(const ExpertArgs& p, const S
     tma_prefetch_desc(kQ4 ? &p.tm_sgu_q : &p.tm_sgu);
     tma_prefetch_desc(kQ4 ? &p.tm_dn_q : &p.tm_dn);
     tma_prefetch_desc(kQ4 ? &p.tm_sdn_q : &p.tm_sdn);
+    if (p.xg_k) tma_prefetch_desc(&p.tm_xg_k);
     if (kQ4 && p.q4_views) {
       tma_prefetch_desc(&p.tm_gu_q3);
       tma_prefetch_desc(&p.tm_sgu_q3);

@@ -125,6 +125,11 @@ struct ExpertArgs {
   CUtensorMap tm_xg_big;  // the same, boxes of xg_box rows
   CUtensorMap tm_h_big;   // the same, boxes of h_box rows
   int xg_box, h_box;      // rows per big box (multiples of 16)
+  // Fused kernel (xg_k != 0): the normed rows of a gate/up stage's kg_gu K
+  // groups in one box (64 c, rows, K group at a stride of 128 bytes; box 64 x
+  // xg_box x kg_gu), the same layout as kg_gu 2-D boxes.
+  CUtensorMap tm_xg_k;
+  int xg_k;
   // Low-bit expert weights (q4 != 0): codes by TMA (uint8, box 32 B x rows),
   // scales by bulk copy; stages_q staging slots of kQSlotBytes.
   CUtensorMap tm_gu_q;   // [E*2F][H/2]
