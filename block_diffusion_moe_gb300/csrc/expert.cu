@@ -1048,9 +1048,11 @@ __device__ __forceinline__ int owned_rows(const Rt& rt, int a, int G) {
 // gathered buffer = normed row of token row_tok[r]), this CTA's share of the
 // pieces. Warp 7 lists the rows (hottest chunks first); then each of the
 // five warps copies every fifth row with 16-byte loads and stores, two rows
-// in flight (no bulk copies: a CTA's TMA unit takes one copy at a time, and
-// a few µs of its own row copies had held up the first units); finally warp
-// 7 publishes, per chunk, how many rows this CTA gathered (release). A
+// in flight (one lane moving the rows with bulk copies, one per row each
+// way, was slower: the rate of an SM's copies follows their number more
+// than their size, and the first units waited ~4 µs for their rows);
+// finally warp 7 publishes, per chunk, how many rows this CTA gathered
+// (release). A
 // gate/up unit of the chunk loads them once the chunk's counter reaches its
 // row count; no CTA waits for all others.
 __device__ void gather_rows(const ExpertArgs& p, const Rt& rt) {

@@ -140,7 +140,7 @@ struct ExpertArgs {
   // (kq*32 bytes, 64 rows, gate|up at a stride of F rows) and every slot's
   // scales in one box (gate/up: 64 scales, gate|up, kq K groups; down: 128
   // scales, kq K groups) instead of two code boxes and 2 kq (gate/up) or kq
-  // (down) scale copies: a CTA's copies pass its TMA unit one at a time.
+  // (down) scale copies (fewer copies per slot measured faster).
   CUtensorMap tm_gu_q3, tm_sgu_q3, tm_gu_sv, tm_sgu_sv, tm_dn_sv, tm_sdn_sv;
   int q4_views;
   const uint16_t* gu_s;   // [E][H/64][2F]
